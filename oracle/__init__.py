@@ -1,0 +1,242 @@
+"""FP64 CPU oracle of the quantized weight-streaming GEMV (ctypes wrapper of
+oracle.c).
+
+TEST INFRASTRUCTURE ONLY.  The tests, the smoke check and the benchmark's CPU
+baseline may import this package; the product library never does, and the
+product path must fail loudly rather than fall back to it.
+
+Definitions followed (details and citations in oracle.h):
+
+* Q8_0 -- "Kipp Architecture", section "Weight quantization": 32-weight blocks,
+  fp16 scale d and int8 codes, value d*q, quantized against the fp16-rounded
+  scale.
+* PQ2_0 -- "Bonsai 2 27B - ternary g128 + blockwise Hadamard", section 3.1:
+  128-weight 34-byte blocks, 2-bit codes at bit offset 2*(j%4), value
+  (q-1)*d, d = max|w|, q = round(w/d) + 1.
+* Rotation -- same page, sections 4.1-4.2: R = H_n / sqrt(n) (Sylvester,
+  natural order) block-diagonal along K; W' = W R^T is stored (rotate, then
+  quantize); the activation gets x' = R x before the product.
+
+Outputs of the GEMV are FP64 sums with the per-row acceptance scale
+absdot_i = sum_j |w_ij x_j|; a result passes when |y - y_oracle| <= 1e-4 *
+absdot_i.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+ORC_OK, ORC_ERR_SHAPE, ORC_ERR_NONFINITE, ORC_ERR_RANGE = 0, 1, 2, 3
+Q8_0_QK, PQ2_0_QK, BLOCK_BYTES = 32, 128, 34
+HADAMARD_N = 128
+TOLERANCE = 1e-4
+
+_lib = None
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        _build.build()
+        L = ctypes.CDLL(_build.LIB)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        L.orc_half_from_float.argtypes = [ctypes.c_float]
+        L.orc_half_from_float.restype = ctypes.c_uint16
+        L.orc_float_from_half.argtypes = [ctypes.c_uint16]
+        L.orc_float_from_half.restype = ctypes.c_float
+        L.orc_half_from_float_array.argtypes = [P, I64, P]
+        L.orc_float_from_half_array.argtypes = [P, I64, P]
+        for name in ("orc_q8_0_quantize", "orc_q8_0_dequant", "orc_pq2_0_quantize", "orc_pq2_0_dequant"):
+            getattr(L, name).argtypes = [P, I64, I64, P]
+            getattr(L, name).restype = ctypes.c_int
+        L.orc_hadamard.argtypes = [ctypes.c_int32, P]
+        L.orc_hadamard.restype = ctypes.c_int
+        L.orc_rotate_rows.argtypes = [P, I64, I64, ctypes.c_int32, P, P]
+        L.orc_rotate_rows.restype = ctypes.c_int
+        L.orc_gemv_f64.argtypes = [P, I64, I64, P, P, I64, ctypes.c_int32, P, P]
+        L.orc_gemv_f64.restype = ctypes.c_int
+        L.orc_max_threads.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(rc, what):
+    if rc != ORC_OK:
+        raise OracleError(f"{what}: oracle status {rc}")
+
+
+def _f32(a):
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def max_threads():
+    return lib().orc_max_threads()
+
+
+# -- binary16 -----------------------------------------------------------------
+
+def half_bits(values):
+    v = _f32(values).ravel()
+    out = np.empty(v.size, dtype=np.uint16)
+    lib().orc_half_from_float_array(v.ctypes.data, v.size, out.ctypes.data)
+    return out.reshape(np.shape(values))
+
+
+def half_value(bits):
+    b = np.ascontiguousarray(bits, dtype=np.uint16).ravel()
+    out = np.empty(b.size, dtype=np.float32)
+    lib().orc_float_from_half_array(b.ctypes.data, b.size, out.ctypes.data)
+    return out.reshape(np.shape(bits))
+
+
+# -- formats ------------------------------------------------------------------
+
+def q8_0_quantize(w):
+    """n x k fp32 -> uint8 array [n, k/32, 34] of Q8_0 blocks."""
+    w = _f32(w)
+    n, k = w.shape
+    if k % Q8_0_QK:
+        raise OracleError("k % 32 != 0")
+    out = np.zeros((n, k // Q8_0_QK, BLOCK_BYTES), dtype=np.uint8)
+    _check(lib().orc_q8_0_quantize(w.ctypes.data, n, k, out.ctypes.data), "q8_0_quantize")
+    return out
+
+
+def q8_0_dequant(blocks, n, k):
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    out = np.empty((n, k), dtype=np.float32)
+    _check(lib().orc_q8_0_dequant(b.ctypes.data, n, k, out.ctypes.data), "q8_0_dequant")
+    return out
+
+
+def pq2_0_quantize(w_rot):
+    """Rotated n x k fp32 -> uint8 array [n, k/128, 34] of PQ2_0 blocks."""
+    w = _f32(w_rot)
+    n, k = w.shape
+    if k % PQ2_0_QK:
+        raise OracleError("k % 128 != 0")
+    out = np.zeros((n, k // PQ2_0_QK, BLOCK_BYTES), dtype=np.uint8)
+    _check(lib().orc_pq2_0_quantize(w.ctypes.data, n, k, out.ctypes.data), "pq2_0_quantize")
+    return out
+
+
+def pq2_0_dequant(blocks, n, k):
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    out = np.empty((n, k), dtype=np.float32)
+    _check(lib().orc_pq2_0_dequant(b.ctypes.data, n, k, out.ctypes.data), "pq2_0_dequant")
+    return out
+
+
+# -- rotation -----------------------------------------------------------------
+
+def hadamard(n):
+    """Unnormalised Sylvester Hadamard matrix H_n (entries +-1), FP64."""
+    out = np.empty((n, n), dtype=np.float64)
+    _check(lib().orc_hadamard(int(n), out.ctypes.data), "hadamard")
+    return out
+
+
+def rotate_rows(x, n=HADAMARD_N):
+    """Blockwise R = H_n/sqrt(n) along the last axis.  Returns (fp64, fp32)."""
+    x = _f32(x)
+    shape = x.shape
+    x2 = x.reshape(-1, shape[-1])
+    rows, k = x2.shape
+    o64 = np.empty((rows, k), dtype=np.float64)
+    o32 = np.empty((rows, k), dtype=np.float32)
+    _check(lib().orc_rotate_rows(x2.ctypes.data, rows, k, int(n), o64.ctypes.data, o32.ctypes.data), "rotate_rows")
+    return o64.reshape(shape), o32.reshape(shape)
+
+
+# -- GEMV ---------------------------------------------------------------------
+
+def gemv(w, x64, rows=None, rows_are_packed=False, n_total=None):
+    """FP64 y = W x and absdot = |W| |x| (elementwise products) for the listed
+    rows of W (all rows when rows is None)."""
+    w = _f32(w)
+    x = np.ascontiguousarray(x64, dtype=np.float64)
+    k = w.shape[1]
+    if x.shape != (k,):
+        raise OracleError("x length mismatch")
+    if rows is None:
+        n = w.shape[0]
+        r_ptr, nr = None, n
+    else:
+        r = np.ascontiguousarray(rows, dtype=np.int64)
+        n = n_total if n_total is not None else w.shape[0]
+        r_ptr, nr = r.ctypes.data, r.size
+    y = np.empty(nr, dtype=np.float64)
+    a = np.empty(nr, dtype=np.float64)
+    _check(lib().orc_gemv_f64(w.ctypes.data, n, k, x.ctypes.data, r_ptr, nr, int(bool(rows_are_packed)),
+                              y.ctypes.data, a.ctypes.data), "gemv")
+    return y, a
+
+
+def gemm(w, X64):
+    """Y[m] = W x_m for each activation row (FP64), with the matching absdot."""
+    X = np.atleast_2d(np.asarray(X64, dtype=np.float64))
+    ys, As = [], []
+    for m in range(X.shape[0]):
+        y, a = gemv(w, X[m])
+        ys.append(y)
+        As.append(a)
+    return np.stack(ys), np.stack(As)
+
+
+# -- whole pipelines from unquantized weights -----------------------------------
+
+def q8_0_reference(w, x):
+    """Quantize W (fp32 n x k) to Q8_0 and return (blocks, dequantized W,
+    y, absdot) for activation x (or rows of X)."""
+    w = _f32(w)
+    n, k = w.shape
+    blocks = q8_0_quantize(w)
+    deq = q8_0_dequant(blocks, n, k)
+    x = np.asarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        y, a = gemv(deq, x.astype(np.float64))
+    else:
+        y, a = gemm(deq, x.astype(np.float64))
+    return blocks, deq, y, a
+
+
+def pq2_0_reference(w, x):
+    """Rotate W blockwise (fp32), quantize to PQ2_0, rotate x in FP64 and
+    return (blocks, dequantized W', y, absdot)."""
+    w = _f32(w)
+    n, k = w.shape
+    _, w_rot = rotate_rows(w)
+    blocks = pq2_0_quantize(w_rot)
+    deq = pq2_0_dequant(blocks, n, k)
+    x = np.asarray(x, dtype=np.float32)
+    x_rot64, _ = rotate_rows(x)
+    if x.ndim == 1:
+        y, a = gemv(deq, x_rot64)
+    else:
+        y, a = gemm(deq, x_rot64)
+    return blocks, deq, y, a
+
+
+def reference(fmt, w, x):
+    if fmt == "q8_0":
+        return q8_0_reference(w, x)
+    if fmt == "pq2_0":
+        return pq2_0_reference(w, x)
+    raise OracleError(fmt)
+
+
+def within_bound(y, y_ref, absdot, tol=TOLERANCE):
+    """Per-row acceptance: |y - y_ref| <= tol * absdot.  Returns (ok, worst
+    ratio of error to bound)."""
+    err = np.abs(np.asarray(y, dtype=np.float64) - y_ref)
+    bound = tol * np.asarray(absdot, dtype=np.float64)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, err / np.where(bound > 0, bound, 1), np.where(err > 0, np.inf, 0.0))
+    return bool(np.all(err <= bound)), float(ratio.max()) if ratio.size else 0.0

@@ -1,0 +1,85 @@
+/*
+ * FP64 CPU oracle of the quantized weight-streaming GEMV.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU
+ * baseline leg of the benchmark may load this code; the product library never
+ * links, calls or falls back to it, and it shares no code with the product.
+ *
+ * It is a plain, slow restatement of the definitions on the pages:
+ *
+ *  - Q8_0 ("Kipp Architecture", section "Weight quantization"): blocks of 32
+ *    weights along K, an fp16 scale d and int8 codes q, value d*q; the
+ *    converter quantizes against the fp16-rounded scale.  Block = 2 B of d
+ *    (little endian) followed by 32 int8 codes (34 B; 136 B per 128-dim row
+ *    in "Kipp Benchmarks", Quantized KV cache bullet).
+ *  - PQ2_0 ("Bonsai 2 27B - ternary g128 + blockwise Hadamard", section 3.1):
+ *    128-weight blocks of 34 B, fp16 d first, then 32 bytes of 2-bit codes;
+ *    element j sits in byte j/4 at bit offset 2*(j%4); code q in {0,1,2}
+ *    has value (q-1)*d; the quantiser takes d = max|w| over the group and
+ *    q = round(w/d) + 1.
+ *  - The rotation (same page, sections 4.1 and 4.2): R = (1/sqrt(n)) * H_n,
+ *    H_n the natural-order Sylvester matrix H[r][c] = (-1)^popcount(r & c),
+ *    applied block-diagonally along K; the stored weight is W' = W R^T
+ *    (rotate, then quantize) and the activation gets x' = R x before the
+ *    product.  Signs are the identity here (S = I) and n = 128.
+ *
+ * Readings where the pages are silent:
+ *  - round() is round-half-away-from-zero (C round), decided on the FP64
+ *    ratio of two floats, which is exact enough to see every tie;
+ *  - the Q8_0 scale is the fp32 quotient amax/127, then rounded to fp16 with
+ *    round-to-nearest-even; codes are clamped to [-127, 127];
+ *  - a block whose fp16 scale is zero gets codes 0 (Q8_0) or 1 (PQ2_0);
+ *  - R w is evaluated as (1/sqrt(n)) * (H w): the sum in FP64, one FP64
+ *    multiply, then (for stored weights) one rounding to fp32.
+ *
+ * Every output of the GEMV is the FP64 value of the finite sum
+ * sum_j deq(W)_ij * x_j (x' for PQ2_0), summed in index order, together with
+ * sum_j |deq(W)_ij * x_j|, the scale of the acceptance bound.
+ */
+#ifndef KQ_ORACLE_H
+#define KQ_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_OK = 0, ORC_ERR_SHAPE = 1, ORC_ERR_NONFINITE = 2, ORC_ERR_RANGE = 3 };
+
+/* IEEE 754 binary16 <-> binary32, round to nearest even (overflow -> inf). */
+uint16_t orc_half_from_float(float f);
+float orc_float_from_half(uint16_t h);
+void orc_half_from_float_array(const float* in, int64_t n, uint16_t* out);
+void orc_float_from_half_array(const uint16_t* in, int64_t n, float* out);
+
+/* Q8_0: w is n x k row-major fp32, k % 32 == 0; blocks gets n*k/32 blocks of 34 B. */
+int orc_q8_0_quantize(const float* w, int64_t n, int64_t k, uint8_t* blocks);
+int orc_q8_0_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out);
+
+/* PQ2_0: w_rot is the already rotated n x k matrix, k % 128 == 0; n*k/128 blocks of 34 B. */
+int orc_pq2_0_quantize(const float* w_rot, int64_t n, int64_t k, uint8_t* blocks);
+int orc_pq2_0_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out);
+
+/* Unnormalised Sylvester Hadamard matrix, n x n row-major, entries +-1. */
+int orc_hadamard(int32_t n, double* h_out);
+
+/* Blockwise rotation of each row: out = (1/sqrt(n)) * (H_n block) per n-block
+ * of K.  out64 (may be NULL) gets the FP64 values, out32 (may be NULL) the
+ * same values rounded once to fp32. */
+int orc_rotate_rows(const float* in, int64_t rows, int64_t k, int32_t n, double* out64, float* out32);
+
+/* y_i = sum_j w_ij x_j and absdot_i = sum_j |w_ij x_j| in FP64 for the listed
+ * rows (rows == NULL: all n rows, in order); w holds the n x k matrix (or
+ * just the listed rows when rows_are_packed != 0). */
+int orc_gemv_f64(const float* w, int64_t n, int64_t k, const double* x, const int64_t* rows, int64_t nrows,
+                 int32_t rows_are_packed, double* y, double* absdot);
+
+/* Threads the row loops may use (OpenMP), for reporting. */
+int orc_max_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KQ_ORACLE_H */
