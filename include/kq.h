@@ -1,0 +1,204 @@
+/*
+ * kq.h -- C ABI of libkq, the quantized weight-streaming GEMV library for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What it computes.  Token decode of a large language model is bound by one
+ * operation: a matrix-vector product that streams every quantized weight from
+ * HBM once per token and dequantizes it inside the dot product.  Two block
+ * formats are supported:
+ *
+ *   Q8_0   32 weights per block along K: an fp16 scale d and 32 int8 codes q,
+ *          value d*q ("Kipp Architecture", section "Weight quantization";
+ *          34 bytes per block, i.e. 136 bytes per 128-dim row as printed in
+ *          "Kipp Benchmarks", Quantized KV cache bullet).
+ *
+ *   PQ2_0  128 weights per block: an fp16 scale d and 2-bit codes
+ *          q in {0,1,2}, element j in byte j/4 at bit offset 2*(j%4), value
+ *          (q-1)*d, d = max|w| and q = round(w/d)+1 ("Bonsai 2 27B - ternary
+ *          g128 + blockwise Hadamard", section 3.1).  The weights are stored
+ *          rotated, W' = W R^T with R = H_128/sqrt(128) applied block-diagonally
+ *          along K (same page, sections 4.1-4.2, with n = 128 and no sign
+ *          vector), so the activation gets x' = R x before the product; the
+ *          PQ2_0 GEMV takes the UNROTATED x and applies R itself.
+ *
+ * Conventions.
+ *  - Every function returns a kq_status (int); 0 is success.  On failure
+ *    nothing has been written to any output and no work was enqueued;
+ *    kq_last_error() gives a one-line reason (per calling thread).
+ *  - Device entry points are asynchronous: they validate their arguments on
+ *    the host, enqueue kernels on `stream` (a cudaStream_t passed as void*;
+ *    NULL means the legacy default stream) and return.  The caller
+ *    synchronises.  All pointers named d_* are device memory owned by the
+ *    caller; the library never frees them.
+ *  - GEMV/GEMM and decode-step calls allocate nothing.  Scratch memory they
+ *    need is the caller's workspace, sized by the *_workspace_bytes queries.
+ *  - Results are deterministic: the same inputs, shapes and split plan give
+ *    bitwise the same output on every call and for every grid size.
+ *  - Device pointers must be 16-byte aligned.  Sizes are int64_t elements.
+ *
+ * Device data layout of a quantized matrix (n rows, k columns, "planes"):
+ *  - codes  Q8_0: int8 [n][k], row stride k bytes.
+ *           PQ2_0: uint32 [n][k/16], row stride k/4 bytes; each 32-bit word
+ *           (little endian) holds elements 16i..16i+15 of its row at bits 2j,
+ *           which is the byte order of the block's qs[] read as words.
+ *  - scales fp16 [n][kq_scale_stride(fmt, k)]; entry [r][b] is the scale of
+ *           block b of row r; the padding entries of each row are zero.
+ */
+#ifndef KQ_H
+#define KQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KQ_OK = 0,
+  KQ_ERR_INVALID_ARG = 1, /* NULL pointer, unknown format, negative or zero size   */
+  KQ_ERR_SHAPE = 2,       /* k not a multiple of the block, n < 1, m out of range  */
+  KQ_ERR_ALIGNMENT = 3,   /* a device pointer is not 16-byte aligned               */
+  KQ_ERR_NONFINITE = 4,   /* NaN or Inf in the weights given to a quantizer        */
+  KQ_ERR_RANGE = 5,       /* a block scale does not fit fp16 (above 65504)         */
+  KQ_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than required               */
+  KQ_ERR_CUDA = 7,        /* a CUDA runtime call failed                            */
+  KQ_ERR_TIMEOUT = 8,     /* a bounded wait inside a kernel expired                */
+  KQ_ERR_UNSUPPORTED = 9  /* device or combination of arguments not supported      */
+} kq_status;
+
+typedef enum { KQ_Q8_0 = 0, KQ_PQ2_0 = 1 } kq_format;
+
+/* A quantized matrix resident in device memory (planes as described above).
+ * had_block is the Hadamard block of the fold: 128 for PQ2_0, 0 for Q8_0. */
+typedef struct {
+  int32_t fmt;
+  int32_t had_block;
+  int64_t n;
+  int64_t k;
+  const void* codes;
+  const void* scales;
+} kq_qmat;
+
+/* ---- status and layout ---------------------------------------------------- */
+
+const char* kq_status_string(int status);
+/* Reason of the last failing call on this thread ("" if none). */
+const char* kq_last_error(void);
+/* ABI version, bumped on incompatible change. */
+int kq_version(void);
+
+/* Weights per block: 32 (Q8_0) or 128 (PQ2_0); 0 for an unknown format. */
+int64_t kq_block_size(int fmt);
+/* Bytes of one 34-byte block times the number of blocks of an n x k matrix. */
+int64_t kq_blocks_bytes(int fmt, int64_t n, int64_t k);
+/* Row stride of the scales plane in fp16 elements: k/block rounded up to 8. */
+int64_t kq_scale_stride(int fmt, int64_t k);
+int64_t kq_codes_bytes(int fmt, int64_t n, int64_t k);
+int64_t kq_scales_bytes(int fmt, int64_t n, int64_t k);
+
+/* ---- host quantizers (offline weight preparation, deterministic) ----------- */
+
+/* Q8_0 per row and 32-block: d = fp16(amax/127) (fp32 quotient, then round to
+ * nearest even), q = round-half-away-from-zero(w / float(d)) clamped to
+ * [-127, 127]; a block whose fp16 scale is zero gets q = 0.  Output: n*k/32
+ * blocks of 34 bytes (d little endian, then 32 int8), row-major.
+ * Errors: KQ_ERR_SHAPE (k % 32), KQ_ERR_NONFINITE, KQ_ERR_RANGE. */
+int kq_quantize_q8_0(const float* w, int64_t n, int64_t k, void* blocks);
+
+/* PQ2_0 per row and 128-block of the ROTATED weights: d = fp16(max|w|), code =
+ * round-half-away-from-zero(w / float(d)) clamped to [-1, 1], plus 1; a block
+ * whose fp16 scale is zero gets code 1.  Output: n*k/128 blocks of 34 bytes.
+ * Errors: KQ_ERR_SHAPE (k % 128), KQ_ERR_NONFINITE, KQ_ERR_RANGE. */
+int kq_quantize_pq2_0(const float* w_rot, int64_t n, int64_t k, void* blocks);
+
+/* Blockwise normalised Walsh-Hadamard transform of each row, on the host:
+ * out[b*block + i] = (1/sqrt(block)) * sum_c H[i][c] in[b*block + c], with the
+ * sum taken in FP64, one FP64 multiply, one rounding to fp32.  block is a
+ * power of two dividing k.  in == out is allowed. */
+int kq_hadamard_blockwise_host(const float* in, float* out, int64_t rows, int64_t k, int32_t block);
+
+/* ---- device weight preparation ------------------------------------------- */
+
+/* Repack n*k/block AoS blocks (device memory, 34-byte blocks as produced by
+ * the host quantizers) into the codes and scales planes. */
+int kq_prepare(int fmt, const void* d_blocks, int64_t n, int64_t k, void* d_codes, void* d_scales, void* stream);
+
+/* Quantize an n x k fp32 matrix in device memory straight into planes, with
+ * the same rules and bit-identical results as the host quantizers.  On a
+ * NaN, Inf or fp16 overflow the call still returns KQ_OK (it is
+ * asynchronous); kq_device_status() then reports KQ_ERR_NONFINITE or
+ * KQ_ERR_RANGE. */
+int kq_quantize_q8_0_device(const float* d_w, int64_t n, int64_t k, void* d_codes, void* d_scales, void* stream);
+int kq_quantize_pq2_0_device(const float* d_w_rot, int64_t n, int64_t k, void* d_codes, void* d_scales,
+                             void* stream);
+
+/* Debug: write the dequantized n x k fp32 matrix (d*q or (q-1)*d, exact). */
+int kq_dequantize(const kq_qmat* W, float* d_out, void* stream);
+
+/* Blockwise normalised Walsh-Hadamard transform of each row on the device,
+ * same arithmetic as kq_hadamard_blockwise_host (FP64 butterflies, one FP64
+ * multiply, one rounding), bit-identical to it.  d_in == d_out is allowed. */
+int kq_hadamard_blockwise(const float* d_in, float* d_out, int64_t rows, int64_t k, int32_t block, void* stream);
+
+/* ---- GEMV / small-M GEMM --------------------------------------------------- */
+
+/* Workspace bytes needed by a GEMV / GEMM call on W with m activation rows
+ * (split-K partials; 0 when the call needs none). */
+size_t kq_gemv_workspace_bytes(const kq_qmat* W, int64_t m);
+
+/* y[n] = W x for a Q8_0 matrix: d_x fp32 [k], d_y fp32 [n]. */
+int kq_gemv_q8_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
+
+/* y[n] = W' (R x) for a PQ2_0 matrix: d_x is the UNROTATED fp32 activation
+ * [k]; the blockwise transform runs in the kernel's activation prologue. */
+int kq_gemv_pq2_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
+
+/* Y[m][n] = X[m][k] W^T (rotated per row for PQ2_0), X and Y row-major fp32,
+ * 1 <= m <= 64. */
+int kq_gemm_small_m(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, void* d_ws, size_t ws_bytes,
+                    void* stream);
+
+/* GEMV/GEMM with an explicit split-K factor (1 = no split; 0 = automatic).
+ * Splits are whole multiples of 1024 weights along K; the partial sums of
+ * each split are added in split order by a second pass, so a given split
+ * factor always gives bitwise the same result. */
+int kq_gemm_splitk(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int32_t splits, void* d_ws,
+                   size_t ws_bytes, void* stream);
+size_t kq_gemm_splitk_workspace_bytes(const kq_qmat* W, int64_t m, int32_t splits);
+
+/* ---- decode-step driver ---------------------------------------------------- */
+
+/* A plan for streaming a whole model's projection list once per step: count
+ * matrices of one format.  Creating it copies the descriptors and a
+ * per-SM schedule to device memory (the only allocation the plan makes);
+ * kq_decode_step then runs the whole list in one persistent kernel.
+ * Activations are packed: matrix i reads x at offset sum_{j<i} k_j floats of
+ * d_x_packed and writes y at offset sum_{j<i} n_j floats of d_y_packed. */
+typedef struct kq_plan kq_plan;
+int kq_decode_plan_create(const kq_qmat* mats, int64_t count, kq_plan** out);
+/* Total packed activation / output lengths in floats, and weight bytes. */
+int kq_decode_plan_sizes(const kq_plan* plan, int64_t* x_floats, int64_t* y_floats, int64_t* weight_bytes);
+size_t kq_decode_workspace_bytes(const kq_plan* plan);
+int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, void* d_ws, size_t ws_bytes,
+                   void* stream);
+void kq_decode_plan_destroy(kq_plan* plan);
+
+/* ---- device status --------------------------------------------------------- */
+
+/* binaryVersion (major*10 + minor) of the streaming kernel as loaded on the
+ * current device: 103 for the sm_103a code this library is built with.  A
+ * caller that records performance can refuse any other value. */
+int kq_kernel_binary_version(int* version);
+
+/* Synchronises the current device and returns the status word that kernels
+ * set when a bounded wait expired (KQ_ERR_TIMEOUT) or a device quantizer met
+ * a non-finite weight (KQ_ERR_NONFINITE) or an fp16 overflow (KQ_ERR_RANGE);
+ * KQ_OK if none.  clear != 0 resets the word. */
+int kq_device_status(int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KQ_H */

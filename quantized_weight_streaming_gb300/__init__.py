@@ -1,0 +1,313 @@
+"""Python binding of libkq, the quantized weight-streaming GEMV library for
+GB300 (sm_103a).
+
+Argument marshalling only: every function here checks nothing the C library
+does not check itself, turns torch tensors (device memory, owned by the
+caller) and streams into pointers, calls the entry point of the same name in
+libkq.so and raises KQError on a non-zero status.  All arithmetic runs in the
+library's CUDA kernels (or, for the offline host quantizers, in its C++ host
+code); there is no fallback of any kind.
+
+If the shared library has not been built, importing this package fails with
+an ImportError: build it with ``quantized_weight_streaming_gb300.build.build()``
+(or ``__graft_entry__.build()``).
+"""
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkq.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libkq.so is not built ({LIB_PATH} missing); run quantized_weight_streaming_gb300.build.build()")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+KQ_OK = 0
+KQ_ERR_INVALID_ARG = 1
+KQ_ERR_SHAPE = 2
+KQ_ERR_ALIGNMENT = 3
+KQ_ERR_NONFINITE = 4
+KQ_ERR_RANGE = 5
+KQ_ERR_WORKSPACE = 6
+KQ_ERR_CUDA = 7
+KQ_ERR_TIMEOUT = 8
+KQ_ERR_UNSUPPORTED = 9
+
+KQ_Q8_0 = 0
+KQ_PQ2_0 = 1
+FORMATS = {"q8_0": KQ_Q8_0, "pq2_0": KQ_PQ2_0}
+
+
+class KQError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = _lib.kq_last_error().decode()
+        super().__init__(f"{where}: {_lib.kq_status_string(status).decode()} ({status}): {msg}")
+
+
+class kq_qmat(ctypes.Structure):
+    _fields_ = [("fmt", ctypes.c_int32), ("had_block", ctypes.c_int32), ("n", ctypes.c_int64),
+                ("k", ctypes.c_int64), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+_QP = ctypes.POINTER(kq_qmat)
+
+# name -> (restype, argtypes); every symbol declared in include/kq.h
+SIGNATURES = {
+    "kq_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "kq_last_error": (ctypes.c_char_p, []),
+    "kq_version": (ctypes.c_int, []),
+    "kq_block_size": (_I64, [ctypes.c_int]),
+    "kq_blocks_bytes": (_I64, [ctypes.c_int, _I64, _I64]),
+    "kq_scale_stride": (_I64, [ctypes.c_int, _I64]),
+    "kq_codes_bytes": (_I64, [ctypes.c_int, _I64, _I64]),
+    "kq_scales_bytes": (_I64, [ctypes.c_int, _I64, _I64]),
+    "kq_quantize_q8_0": (ctypes.c_int, [_P, _I64, _I64, _P]),
+    "kq_quantize_pq2_0": (ctypes.c_int, [_P, _I64, _I64, _P]),
+    "kq_hadamard_blockwise_host": (ctypes.c_int, [_P, _P, _I64, _I64, _I32]),
+    "kq_prepare": (ctypes.c_int, [ctypes.c_int, _P, _I64, _I64, _P, _P, _P]),
+    "kq_quantize_q8_0_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+    "kq_quantize_pq2_0_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+    "kq_dequantize": (ctypes.c_int, [_QP, _P, _P]),
+    "kq_hadamard_blockwise": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _P]),
+    "kq_gemv_workspace_bytes": (_SZ, [_QP, _I64]),
+    "kq_gemv_q8_0": (ctypes.c_int, [_QP, _P, _P, _P, _SZ, _P]),
+    "kq_gemv_pq2_0": (ctypes.c_int, [_QP, _P, _P, _P, _SZ, _P]),
+    "kq_gemm_small_m": (ctypes.c_int, [_QP, _P, _I64, _P, _P, _SZ, _P]),
+    "kq_gemm_splitk": (ctypes.c_int, [_QP, _P, _I64, _P, _I32, _P, _SZ, _P]),
+    "kq_gemm_splitk_workspace_bytes": (_SZ, [_QP, _I64, _I32]),
+    "kq_decode_plan_create": (ctypes.c_int, [_QP, _I64, ctypes.POINTER(_P)]),
+    "kq_decode_plan_sizes": (ctypes.c_int, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    "kq_decode_workspace_bytes": (_SZ, [_P]),
+    "kq_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _SZ, _P]),
+    "kq_decode_plan_destroy": (None, [_P]),
+    "kq_device_status": (ctypes.c_int, [ctypes.c_int]),
+    "kq_kernel_binary_version": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
+}
+
+for _name, (_res, _args) in SIGNATURES.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+def lib():
+    return _lib
+
+
+def _check(status, where):
+    if status != KQ_OK:
+        raise KQError(status, where)
+
+
+def _ptr(t):
+    """Address of a torch tensor, a numpy array or an integer (None -> NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    if isinstance(t, np.ndarray):
+        return t.ctypes.data
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _fmt(fmt):
+    return FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+
+
+# ---- layout ------------------------------------------------------------------
+
+def kq_block_size(fmt):
+    return _lib.kq_block_size(_fmt(fmt))
+
+
+def kq_blocks_bytes(fmt, n, k):
+    return _lib.kq_blocks_bytes(_fmt(fmt), n, k)
+
+
+def kq_scale_stride(fmt, k):
+    return _lib.kq_scale_stride(_fmt(fmt), k)
+
+
+def kq_codes_bytes(fmt, n, k):
+    return _lib.kq_codes_bytes(_fmt(fmt), n, k)
+
+
+def kq_scales_bytes(fmt, n, k):
+    return _lib.kq_scales_bytes(_fmt(fmt), n, k)
+
+
+# ---- host quantizers (numpy in, numpy out) --------------------------------------
+
+def kq_quantize_q8_0(w):
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    out = np.zeros(max(kq_blocks_bytes("q8_0", n, k), 1), dtype=np.uint8)
+    _check(_lib.kq_quantize_q8_0(w.ctypes.data, n, k, out.ctypes.data), "kq_quantize_q8_0")
+    return out[: n * (k // 32) * 34].reshape(n, k // 32, 34)
+
+
+def kq_quantize_pq2_0(w_rot):
+    w = np.ascontiguousarray(w_rot, dtype=np.float32)
+    n, k = w.shape
+    out = np.zeros(max(kq_blocks_bytes("pq2_0", n, k), 1), dtype=np.uint8)
+    _check(_lib.kq_quantize_pq2_0(w.ctypes.data, n, k, out.ctypes.data), "kq_quantize_pq2_0")
+    return out[: n * (k // 128) * 34].reshape(n, k // 128, 34)
+
+
+def kq_hadamard_blockwise_host(x, block=128):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    x2 = x.reshape(-1, x.shape[-1])
+    out = np.empty_like(x2)
+    _check(_lib.kq_hadamard_blockwise_host(x2.ctypes.data, out.ctypes.data, x2.shape[0], x2.shape[1], block),
+           "kq_hadamard_blockwise_host")
+    return out.reshape(x.shape)
+
+
+# ---- device entry points (torch tensors) ------------------------------------------
+
+class QMatrix:
+    """A quantized matrix in device memory: torch tensors for the codes and
+    scales planes plus the kq_qmat descriptor that points at them."""
+
+    def __init__(self, fmt, n, k, device="cuda"):
+        import torch
+
+        self.fmt = _fmt(fmt)
+        self.n, self.k = int(n), int(k)
+        cb = kq_codes_bytes(self.fmt, n, k)
+        sb = kq_scales_bytes(self.fmt, n, k)
+        if cb <= 0 or sb <= 0:
+            raise KQError(KQ_ERR_SHAPE, f"QMatrix({fmt}, {n}, {k})")
+        self.codes = torch.empty(cb, dtype=torch.uint8, device=device)
+        self.scales = torch.empty(sb // 2, dtype=torch.int16, device=device)
+        self.desc = kq_qmat(self.fmt, 128 if self.fmt == KQ_PQ2_0 else 0, self.n, self.k, self.codes.data_ptr(),
+                            self.scales.data_ptr())
+
+    @property
+    def nbytes(self):
+        return self.codes.numel() + self.scales.numel() * 2
+
+    @property
+    def weight_bytes(self):
+        """Bytes of the format itself (codes plus one fp16 scale per block)."""
+        return self.codes.numel() + self.n * (self.k // kq_block_size(self.fmt)) * 2
+
+
+def kq_prepare(W, d_blocks, stream=None):
+    _check(_lib.kq_prepare(W.fmt, _ptr(d_blocks), W.n, W.k, W.codes.data_ptr(), W.scales.data_ptr(), _stream(stream)),
+           "kq_prepare")
+
+
+def kq_quantize_q8_0_device(W, d_w, stream=None):
+    _check(_lib.kq_quantize_q8_0_device(_ptr(d_w), W.n, W.k, W.codes.data_ptr(), W.scales.data_ptr(),
+                                        _stream(stream)), "kq_quantize_q8_0_device")
+
+
+def kq_quantize_pq2_0_device(W, d_w_rot, stream=None):
+    _check(_lib.kq_quantize_pq2_0_device(_ptr(d_w_rot), W.n, W.k, W.codes.data_ptr(), W.scales.data_ptr(),
+                                         _stream(stream)), "kq_quantize_pq2_0_device")
+
+
+def kq_dequantize(W, d_out, stream=None):
+    _check(_lib.kq_dequantize(ctypes.byref(W.desc), _ptr(d_out), _stream(stream)), "kq_dequantize")
+
+
+def kq_hadamard_blockwise(d_in, d_out, rows, k, block=128, stream=None):
+    _check(_lib.kq_hadamard_blockwise(_ptr(d_in), _ptr(d_out), rows, k, block, _stream(stream)),
+           "kq_hadamard_blockwise")
+
+
+def kq_gemv_workspace_bytes(W, m=1):
+    return _lib.kq_gemv_workspace_bytes(ctypes.byref(W.desc), m)
+
+
+def kq_gemm_splitk_workspace_bytes(W, m, splits):
+    return _lib.kq_gemm_splitk_workspace_bytes(ctypes.byref(W.desc), m, splits)
+
+
+def _ws(ws):
+    if ws is None:
+        return None, 0
+    return _ptr(ws), ws.numel() * ws.element_size()
+
+
+def kq_gemv_q8_0(W, d_x, d_y, ws=None, stream=None):
+    p, nb = _ws(ws)
+    _check(_lib.kq_gemv_q8_0(ctypes.byref(W.desc), _ptr(d_x), _ptr(d_y), p, nb, _stream(stream)), "kq_gemv_q8_0")
+
+
+def kq_gemv_pq2_0(W, d_x, d_y, ws=None, stream=None):
+    p, nb = _ws(ws)
+    _check(_lib.kq_gemv_pq2_0(ctypes.byref(W.desc), _ptr(d_x), _ptr(d_y), p, nb, _stream(stream)), "kq_gemv_pq2_0")
+
+
+def kq_gemm_small_m(W, d_X, m, d_Y, ws=None, stream=None):
+    p, nb = _ws(ws)
+    _check(_lib.kq_gemm_small_m(ctypes.byref(W.desc), _ptr(d_X), m, _ptr(d_Y), p, nb, _stream(stream)),
+           "kq_gemm_small_m")
+
+
+def kq_gemm_splitk(W, d_X, m, d_Y, splits, ws=None, stream=None):
+    p, nb = _ws(ws)
+    _check(_lib.kq_gemm_splitk(ctypes.byref(W.desc), _ptr(d_X), m, _ptr(d_Y), splits, p, nb, _stream(stream)),
+           "kq_gemm_splitk")
+
+
+def kq_kernel_binary_version():
+    v = ctypes.c_int()
+    _check(_lib.kq_kernel_binary_version(ctypes.byref(v)), "kq_kernel_binary_version")
+    return v.value
+
+
+def kq_device_status(clear=True):
+    return _lib.kq_device_status(1 if clear else 0)
+
+
+class DecodePlan:
+    """kq_decode_plan_create / kq_decode_step / kq_decode_plan_destroy."""
+
+    def __init__(self, mats):
+        self.mats = list(mats)
+        arr = (kq_qmat * len(self.mats))(*[m.desc for m in self.mats])
+        h = ctypes.c_void_p()
+        _check(_lib.kq_decode_plan_create(arr, len(self.mats), ctypes.byref(h)), "kq_decode_plan_create")
+        self.handle = h
+        xf, yf, wb = _I64(), _I64(), _I64()
+        _check(_lib.kq_decode_plan_sizes(h, ctypes.byref(xf), ctypes.byref(yf), ctypes.byref(wb)),
+               "kq_decode_plan_sizes")
+        self.x_floats, self.y_floats, self.weight_bytes = xf.value, yf.value, wb.value
+        self.workspace_bytes = _lib.kq_decode_workspace_bytes(h)
+
+    def step(self, d_x_packed, d_y_packed, ws=None, stream=None):
+        p, nb = _ws(ws)
+        _check(_lib.kq_decode_step(self.handle, _ptr(d_x_packed), _ptr(d_y_packed), p, nb, _stream(stream)),
+               "kq_decode_step")
+
+    def close(self):
+        if self.handle:
+            _lib.kq_decode_plan_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,228 @@
+// Host half of libkq: status strings, per-thread error text, layout queries,
+// the offline host quantizers and the host blockwise Hadamard transform.
+//
+// Formats: Q8_0 ("Kipp Architecture", "Weight quantization": 32-weight
+// blocks, fp16 d, int8 q, value d*q, quantized against the fp16-rounded
+// scale) and PQ2_0 ("Bonsai 2 27B - ternary g128 + blockwise Hadamard",
+// section 3.1: 128-weight 34-byte blocks, 2-bit codes at bit 2*(j%4), value
+// (q-1)*d, d = max|w|, q = round(w/d)+1).  Rounding of w/d is half away from
+// zero, decided on the FP64 quotient of the two floats.
+#include <cuda_fp16.h>
+
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kq_internal.h"
+
+namespace kq {
+
+static thread_local char g_last_error[512] = {0};
+
+int fail(int status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+void clear_error() { g_last_error[0] = 0; }
+
+int check_qmat(const kq_qmat* W, int expect_fmt) {
+  if (!W) return fail(KQ_ERR_INVALID_ARG, "W is NULL");
+  if (W->fmt != KQ_Q8_0 && W->fmt != KQ_PQ2_0) return fail(KQ_ERR_INVALID_ARG, "unknown format %d", W->fmt);
+  if (expect_fmt >= 0 && W->fmt != expect_fmt)
+    return fail(KQ_ERR_INVALID_ARG, "format %d given to an entry point for format %d", W->fmt, expect_fmt);
+  if (W->n < 1) return fail(KQ_ERR_SHAPE, "n = %lld < 1", (long long)W->n);
+  int64_t bs = block_of(W->fmt);
+  if (W->k < bs || W->k % bs != 0)
+    return fail(KQ_ERR_SHAPE, "k = %lld is not a positive multiple of %lld", (long long)W->k, (long long)bs);
+  int want_had = W->fmt == KQ_PQ2_0 ? 128 : 0;
+  if (W->had_block != want_had)
+    return fail(KQ_ERR_UNSUPPORTED, "had_block = %d (this format needs %d)", W->had_block, want_had);
+  if (!W->codes || !W->scales) return fail(KQ_ERR_INVALID_ARG, "NULL plane pointer");
+  if (!aligned16(W->codes) || !aligned16(W->scales)) return fail(KQ_ERR_ALIGNMENT, "plane not 16-byte aligned");
+  return KQ_OK;
+}
+
+}  // namespace kq
+
+using namespace kq;
+
+extern "C" {
+
+const char* kq_status_string(int s) {
+  switch (s) {
+    case KQ_OK: return "ok";
+    case KQ_ERR_INVALID_ARG: return "invalid argument";
+    case KQ_ERR_SHAPE: return "invalid shape";
+    case KQ_ERR_ALIGNMENT: return "misaligned pointer";
+    case KQ_ERR_NONFINITE: return "non-finite weight";
+    case KQ_ERR_RANGE: return "scale out of fp16 range";
+    case KQ_ERR_WORKSPACE: return "workspace missing or too small";
+    case KQ_ERR_CUDA: return "CUDA error";
+    case KQ_ERR_TIMEOUT: return "bounded device wait expired";
+    case KQ_ERR_UNSUPPORTED: return "unsupported";
+    default: return "unknown status";
+  }
+}
+
+const char* kq_last_error(void) { return g_last_error; }
+
+int kq_version(void) { return 1; }
+
+int64_t kq_block_size(int fmt) { return block_of(fmt); }
+
+int64_t kq_blocks_bytes(int fmt, int64_t n, int64_t k) {
+  int64_t bs = block_of(fmt);
+  if (!bs || n < 0 || k < 0 || k % bs) return 0;
+  return n * (k / bs) * 34;
+}
+
+int64_t kq_scale_stride(int fmt, int64_t k) {
+  int64_t bs = block_of(fmt);
+  if (!bs || k < 0 || k % bs) return 0;
+  return scale_stride(fmt, k);
+}
+
+int64_t kq_codes_bytes(int fmt, int64_t n, int64_t k) {
+  int64_t bs = block_of(fmt);
+  if (!bs || n < 0 || k < 0 || k % bs) return 0;
+  return n * code_row_bytes(fmt, k);
+}
+
+int64_t kq_scales_bytes(int fmt, int64_t n, int64_t k) {
+  int64_t bs = block_of(fmt);
+  if (!bs || n < 0 || k < 0 || k % bs) return 0;
+  return n * scale_stride(fmt, k) * 2;
+}
+
+// ---------------------------------------------------------------------------
+// Host quantizers
+// ---------------------------------------------------------------------------
+
+static inline uint16_t half_bits_rn(float v) { return __half_as_ushort(__float2half_rn(v)); }
+static inline float half_to_float(uint16_t h) { return __half2float(__ushort_as_half(h)); }
+
+static int check_host_weights(const float* w, int64_t n, int64_t k, int64_t bs, const void* out) {
+  if (!w || !out) return fail(KQ_ERR_INVALID_ARG, "NULL pointer");
+  if (n < 1 || k < bs || k % bs)
+    return fail(KQ_ERR_SHAPE, "n = %lld, k = %lld (k must be a positive multiple of %lld)", (long long)n,
+                (long long)k, (long long)bs);
+  for (int64_t i = 0; i < n * k; ++i)
+    if (!std::isfinite(w[i])) return fail(KQ_ERR_NONFINITE, "weight %lld is not finite", (long long)i);
+  return KQ_OK;
+}
+
+int kq_quantize_q8_0(const float* w, int64_t n, int64_t k, void* blocks) {
+  clear_error();
+  if (int s = check_host_weights(w, n, k, 32, blocks)) return s;
+  const int64_t nb = k / 32;
+  // First pass: scales only, so that a range error leaves the output untouched.
+  std::vector<uint16_t> dh(static_cast<size_t>(n * nb));
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* src = w + r * k + b * 32;
+      float amax = 0.f;
+      for (int j = 0; j < 32; ++j) amax = std::fmax(amax, std::fabs(src[j]));
+      uint16_t h = half_bits_rn(amax / 127.0f);
+      if ((h & 0x7C00u) == 0x7C00u)
+        return fail(KQ_ERR_RANGE, "row %lld block %lld: scale %g overflows fp16", (long long)r, (long long)b,
+                    (double)(amax / 127.0f));
+      dh[static_cast<size_t>(r * nb + b)] = h;
+    }
+  }
+  uint8_t* out = static_cast<uint8_t*>(blocks);
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* src = w + r * k + b * 32;
+      uint8_t* blk = out + (r * nb + b) * 34;
+      uint16_t h = dh[static_cast<size_t>(r * nb + b)];
+      double d = half_to_float(h);
+      blk[0] = static_cast<uint8_t>(h & 0xFF);
+      blk[1] = static_cast<uint8_t>(h >> 8);
+      for (int j = 0; j < 32; ++j) {
+        long q = 0;
+        if (d != 0.0) q = std::lround(static_cast<double>(src[j]) / d);
+        q = q > 127 ? 127 : (q < -127 ? -127 : q);
+        blk[2 + j] = static_cast<uint8_t>(static_cast<int8_t>(q));
+      }
+    }
+  }
+  return KQ_OK;
+}
+
+int kq_quantize_pq2_0(const float* w_rot, int64_t n, int64_t k, void* blocks) {
+  clear_error();
+  if (int s = check_host_weights(w_rot, n, k, 128, blocks)) return s;
+  const int64_t nb = k / 128;
+  std::vector<uint16_t> dh(static_cast<size_t>(n * nb));
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* src = w_rot + r * k + b * 128;
+      float amax = 0.f;
+      for (int j = 0; j < 128; ++j) amax = std::fmax(amax, std::fabs(src[j]));
+      uint16_t h = half_bits_rn(amax);
+      if ((h & 0x7C00u) == 0x7C00u)
+        return fail(KQ_ERR_RANGE, "row %lld block %lld: scale %g overflows fp16", (long long)r, (long long)b,
+                    (double)amax);
+      dh[static_cast<size_t>(r * nb + b)] = h;
+    }
+  }
+  uint8_t* out = static_cast<uint8_t*>(blocks);
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* src = w_rot + r * k + b * 128;
+      uint8_t* blk = out + (r * nb + b) * 34;
+      uint16_t h = dh[static_cast<size_t>(r * nb + b)];
+      double d = half_to_float(h);
+      blk[0] = static_cast<uint8_t>(h & 0xFF);
+      blk[1] = static_cast<uint8_t>(h >> 8);
+      std::memset(blk + 2, 0, 32);
+      for (int j = 0; j < 128; ++j) {
+        long t = 0;
+        if (d != 0.0) t = std::lround(static_cast<double>(src[j]) / d);
+        t = t > 1 ? 1 : (t < -1 ? -1 : t);
+        blk[2 + j / 4] |= static_cast<uint8_t>((t + 1) << (2 * (j % 4)));
+      }
+    }
+  }
+  return KQ_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Host blockwise Hadamard: in-place FP64 butterflies (natural Sylvester order),
+// then one FP64 multiply by 1/sqrt(block) and one rounding to fp32.
+// ---------------------------------------------------------------------------
+
+int kq_hadamard_blockwise_host(const float* in, float* out, int64_t rows, int64_t k, int32_t block) {
+  clear_error();
+  if (!in || !out) return fail(KQ_ERR_INVALID_ARG, "NULL pointer");
+  if (block < 1 || (block & (block - 1)) != 0) return fail(KQ_ERR_SHAPE, "block %d is not a power of two", block);
+  if (rows < 1 || k < block || k % block)
+    return fail(KQ_ERR_SHAPE, "rows = %lld, k = %lld, block = %d", (long long)rows, (long long)k, block);
+  const double scale = 1.0 / std::sqrt(static_cast<double>(block));
+  std::vector<double> v(static_cast<size_t>(block));
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t b0 = 0; b0 < k; b0 += block) {
+      const float* src = in + r * k + b0;
+      for (int32_t i = 0; i < block; ++i) v[i] = src[i];
+      for (int32_t h = 1; h < block; h <<= 1) {
+        for (int32_t i = 0; i < block; i += 2 * h) {
+          for (int32_t j = i; j < i + h; ++j) {
+            double a = v[j], c = v[j + h];
+            v[j] = a + c;
+            v[j + h] = a - c;
+          }
+        }
+      }
+      float* dst = out + r * k + b0;
+      for (int32_t i = 0; i < block; ++i) dst[i] = static_cast<float>(scale * v[i]);
+    }
+  }
+  return KQ_OK;
+}
+
+}  // extern "C"

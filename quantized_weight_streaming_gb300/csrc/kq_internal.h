@@ -1,0 +1,34 @@
+// Host-side helpers shared by the translation units of libkq.
+#pragma once
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+
+#include "kq.h"
+
+namespace kq {
+
+// Records a one-line reason for the calling thread and returns `status`.
+int fail(int status, const char* fmt, ...);
+// Clears the thread's last error (called on entry of every public function).
+void clear_error();
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+inline int64_t block_of(int fmt) { return fmt == KQ_Q8_0 ? 32 : (fmt == KQ_PQ2_0 ? 128 : 0); }
+inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
+inline int64_t scale_stride(int fmt, int64_t k) { return round_up(k / block_of(fmt), 8); }
+inline int64_t code_row_bytes(int fmt, int64_t k) { return fmt == KQ_Q8_0 ? k : k / 4; }
+
+// Checks a kq_qmat descriptor (format, shape, plane pointers and alignment).
+int check_qmat(const kq_qmat* W, int expect_fmt);
+
+}  // namespace kq
+
+#define KQ_CUDA_TRY(expr)                                                                           \
+  do {                                                                                              \
+    cudaError_t kq_err_ = (expr);                                                                   \
+    if (kq_err_ != cudaSuccess)                                                                     \
+      return ::kq::fail(KQ_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(kq_err_));                 \
+  } while (0)

@@ -1,0 +1,149 @@
+"""CPU checks of the C-ABI library: it loads, exports every symbol the header
+declares, its host quantizers produce the oracle's bytes, its host Hadamard
+matches the oracle, and invalid arguments are rejected on the host before
+any CUDA call."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def kq():
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import quantized_weight_streaming_gb300 as kq
+
+    return kq
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "kq.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_symbols_exported(kq):
+    names = _header_functions()
+    assert len(names) >= 25
+    lib = ctypes.CDLL(kq.LIB_PATH)
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(kq.SIGNATURES) == names
+
+
+def test_layout_queries(kq):
+    assert kq.kq_block_size("q8_0") == 32 and kq.kq_block_size("pq2_0") == 128
+    assert kq.kq_blocks_bytes("q8_0", 1, 128) == 136
+    assert kq.kq_blocks_bytes("pq2_0", 10240, 5120) == 13_926_400
+    assert kq.kq_scale_stride("q8_0", 2560) == 80
+    assert kq.kq_scale_stride("pq2_0", 384) == 8  # 3 blocks, padded to 8
+    assert kq.kq_codes_bytes("pq2_0", 2, 512) == 256
+    assert kq.kq_scales_bytes("q8_0", 3, 64) == 3 * 8 * 2
+    assert kq.kq_codes_bytes("q8_0", 1, 33) == 0  # not a multiple of the block
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_host_q8_0_quantizer_matches_oracle_bytes(kq, seed):
+    w = synth.fill_host("w", 96 * 2560, seed, synth.stream_id("test", 0, 200)).reshape(96, 2560)
+    assert np.array_equal(kq.kq_quantize_q8_0(w), oracle.q8_0_quantize(w))
+    rng = np.random.default_rng(seed)
+    wide = (rng.standard_normal((64, 512)) * rng.uniform(1e-6, 50, size=(64, 1))).astype(np.float32)
+    wide[3, :32] = 0
+    wide[5, 40] = 127 * 0.5  # ties against d = 0.5
+    assert np.array_equal(kq.kq_quantize_q8_0(wide), oracle.q8_0_quantize(wide))
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_host_pq2_0_quantizer_matches_oracle_bytes(kq, seed):
+    w = synth.fill_host("w", 40 * 5120, seed, synth.stream_id("test", 0, 201)).reshape(40, 5120)
+    _, w_rot = oracle.rotate_rows(w)
+    assert np.array_equal(kq.kq_quantize_pq2_0(w_rot), oracle.pq2_0_quantize(w_rot))
+    rng = np.random.default_rng(seed)
+    wide = (rng.standard_normal((16, 1024)) * rng.uniform(1e-6, 50, size=(16, 1))).astype(np.float32)
+    wide[2, :128] = 0
+    wide[4, :4] = [2.0, 1.0, -1.0, 0.99999994]  # ties at half the scale
+    assert np.array_equal(kq.kq_quantize_pq2_0(wide), oracle.pq2_0_quantize(wide))
+
+
+def test_host_hadamard_matches_oracle(kq):
+    # grid inputs: the block sums are exact, so the results are bit-identical
+    w = synth.fill_host("w", 8 * 1024, 0, synth.stream_id("test", 0, 202)).reshape(8, 1024)
+    _, ref32 = oracle.rotate_rows(w)
+    assert np.array_equal(kq.kq_hadamard_blockwise_host(w, 128), ref32)
+    # general inputs: within a few fp32 rounding steps
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((4, 4096)).astype(np.float32) * 3
+    ref64, _ = oracle.rotate_rows(x, 128)
+    got = kq.kq_hadamard_blockwise_host(x, 128)
+    assert np.max(np.abs(got - ref64)) <= 2 * np.finfo(np.float32).eps * np.max(np.abs(ref64))
+    for block in (1, 2, 64, 1024):
+        ref64, _ = oracle.rotate_rows(x, block)
+        assert np.max(np.abs(kq.kq_hadamard_blockwise_host(x, block) - ref64)) < 1e-4
+
+
+def test_host_errors_leave_output_untouched(kq):
+    lib = kq.lib()
+    out = np.full(34 * 4, 0xAB, dtype=np.uint8)
+    w = np.zeros((1, 48), dtype=np.float32)
+    assert lib.kq_quantize_q8_0(w.ctypes.data, 1, 48, out.ctypes.data) == kq.KQ_ERR_SHAPE
+    w = np.zeros((1, 128), dtype=np.float32)
+    w[0, 77] = np.inf
+    assert lib.kq_quantize_q8_0(w.ctypes.data, 1, 128, out.ctypes.data) == kq.KQ_ERR_NONFINITE
+    assert lib.kq_quantize_pq2_0(w.ctypes.data, 1, 128, out.ctypes.data) == kq.KQ_ERR_NONFINITE
+    w[0, 77] = 1e7
+    assert lib.kq_quantize_q8_0(w.ctypes.data, 1, 128, out.ctypes.data) == kq.KQ_ERR_RANGE
+    w[0, 77] = 7e4
+    assert lib.kq_quantize_pq2_0(w.ctypes.data, 1, 128, out.ctypes.data) == kq.KQ_ERR_RANGE
+    assert np.all(out == 0xAB)
+    assert "overflows fp16" in lib.kq_last_error().decode()
+    assert lib.kq_quantize_q8_0(None, 1, 32, out.ctypes.data) == kq.KQ_ERR_INVALID_ARG
+    x = np.zeros((1, 96), dtype=np.float32)
+    assert lib.kq_hadamard_blockwise_host(x.ctypes.data, x.ctypes.data, 1, 96, 64) == kq.KQ_ERR_SHAPE
+    assert lib.kq_hadamard_blockwise_host(x.ctypes.data, x.ctypes.data, 1, 96, 3) == kq.KQ_ERR_SHAPE
+
+
+def test_device_entry_points_validate_before_any_cuda_call(kq):
+    lib = kq.lib()
+    A = 1 << 20  # a 16-byte-aligned fake address; validation must fail before it is used
+    bad_k = kq.kq_qmat(kq.KQ_Q8_0, 0, 8, 48, A, A)
+    assert lib.kq_gemv_q8_0(ctypes.byref(bad_k), A, A, None, 0, None) == kq.KQ_ERR_SHAPE
+    wrong_fmt = kq.kq_qmat(kq.KQ_PQ2_0, 128, 8, 128, A, A)
+    assert lib.kq_gemv_q8_0(ctypes.byref(wrong_fmt), A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
+    no_had = kq.kq_qmat(kq.KQ_PQ2_0, 0, 8, 128, A, A)
+    assert lib.kq_gemv_pq2_0(ctypes.byref(no_had), A, A, None, 0, None) == kq.KQ_ERR_UNSUPPORTED
+    misaligned = kq.kq_qmat(kq.KQ_Q8_0, 0, 8, 64, A + 4, A)
+    assert lib.kq_gemv_q8_0(ctypes.byref(misaligned), A, A, None, 0, None) == kq.KQ_ERR_ALIGNMENT
+    good = kq.kq_qmat(kq.KQ_Q8_0, 0, 8, 64, A, A)
+    assert lib.kq_gemv_q8_0(ctypes.byref(good), A + 8, A, None, 0, None) == kq.KQ_ERR_ALIGNMENT
+    assert lib.kq_gemm_small_m(ctypes.byref(good), A, 65, A, None, 0, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_gemm_small_m(ctypes.byref(good), A, 0, A, None, 0, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_gemm_splitk(ctypes.byref(good), A, 1, A, -1, None, 0, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_gemv_q8_0(None, A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_dequantize(ctypes.byref(bad_k), A, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_hadamard_blockwise(A, A, 1, 100, 128, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_hadamard_blockwise(A, A, 1, 8192, 8192, None) == kq.KQ_ERR_UNSUPPORTED
+    assert lib.kq_prepare(5, A, 1, 32, A, A, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_quantize_pq2_0_device(A, 1, 64, A, A, None) == kq.KQ_ERR_SHAPE
+    h = ctypes.c_void_p()
+    mixed = (kq.kq_qmat * 2)(good, kq.kq_qmat(kq.KQ_PQ2_0, 128, 8, 128, A, A))
+    assert lib.kq_decode_plan_create(mixed, 2, ctypes.byref(h)) in (kq.KQ_ERR_UNSUPPORTED, kq.KQ_ERR_CUDA)
+    assert lib.kq_decode_plan_create(mixed, 0, ctypes.byref(h)) == kq.KQ_ERR_SHAPE
+    assert lib.kq_decode_step(None, A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_gemv_workspace_bytes(ctypes.byref(bad_k), 1) == 0
+
+
+def test_status_strings(kq):
+    lib = kq.lib()
+    for s in range(10):
+        assert lib.kq_status_string(s)
+    assert lib.kq_status_string(99) == b"unknown status"
+    assert lib.kq_version() == 1

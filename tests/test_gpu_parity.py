@@ -1,0 +1,354 @@
+"""GPU parity of the CUDA path against the FP64 oracle, through the C ABI.
+
+Bars: integer and byte work (codes, scales, dequantized values, the
+generator, the FP64 weight rotation) bit-exact; floating-point outputs within
+|y - y_oracle| <= 1e-4 * sum_j |w_ij x_j| per row; integer-valued cases at
+tolerance 0."""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module")
+def kq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import quantized_weight_streaming_gb300 as kq
+
+    torch.cuda.set_device(0)
+    kq.kq_device_status(True)
+    yield kq
+    assert kq.kq_device_status(True) == kq.KQ_OK
+
+
+@pytest.fixture(scope="module")
+def wl(kq):
+    import workloads
+
+    return workloads
+
+
+def _sync_ok(kq):
+    torch.cuda.synchronize()
+    assert kq.kq_device_status(True) == kq.KQ_OK
+
+
+def _planes_as_blocks(kq, W):
+    """Device planes -> AoS 34-byte blocks (host), for byte comparison."""
+    bs = kq.kq_block_size(W.fmt)
+    nb = W.k // bs
+    codes = W.codes.cpu().numpy().reshape(W.n, nb, 32)
+    ss = kq.kq_scale_stride(W.fmt, W.k)
+    scales = W.scales.cpu().numpy().view(np.uint16).reshape(W.n, ss)
+    assert not scales[:, nb:].any()  # padding is zero
+    out = np.empty((W.n, nb, 34), dtype=np.uint8)
+    out[:, :, 0] = scales[:, :nb] & 0xFF
+    out[:, :, 1] = scales[:, :nb] >> 8
+    out[:, :, 2:] = codes
+    return out
+
+
+def _run_gemv(kq, W, x, splits=0, m=1):
+    y = torch.empty(m * W.n, dtype=torch.float32, device="cuda")
+    nbytes = kq.kq_gemm_splitk_workspace_bytes(W, m, splits)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
+    if splits == 0 and m == 1:
+        (kq.kq_gemv_pq2_0 if W.fmt == kq.KQ_PQ2_0 else kq.kq_gemv_q8_0)(W, x, y, ws)
+    else:
+        kq.kq_gemm_splitk(W, x, m, y, splits, ws)
+    _sync_ok(kq)
+    return y.cpu().numpy().reshape(m, W.n) if m > 1 else y.cpu().numpy()
+
+
+# ----------------------------------------------------------------------------
+# generator, rotation, quantizers
+# ----------------------------------------------------------------------------
+
+def test_device_generator_matches_host(kq):
+    for kind, n, first in (("w", 1_000_003, 0), ("x", 77_777, 12345)):
+        s = synth.stream_id("test", 0, 300)
+        d = torch.empty(n, dtype=torch.float32, device="cuda")
+        synth.fill_device(d.data_ptr(), kind, n, 5, s, first)
+        torch.cuda.synchronize()
+        assert np.array_equal(d.cpu().numpy(), synth.fill_host(kind, n, 5, s, first))
+
+
+def test_device_hadamard_bit_identical_to_host_and_oracle(kq):
+    w = synth.fill_host("w", 64 * 1024, 1, synth.stream_id("test", 0, 301)).reshape(64, 1024)
+    d = torch.from_numpy(w).cuda()
+    out = torch.empty_like(d)
+    kq.kq_hadamard_blockwise(d, out, 64, 1024, 128)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert np.array_equal(got, kq.kq_hadamard_blockwise_host(w, 128))
+    assert np.array_equal(got, oracle.rotate_rows(w)[1])  # grid inputs: exact sums
+    rng = np.random.default_rng(0)
+    g = (rng.standard_normal((8, 2048)) * 10).astype(np.float32)
+    dg = torch.from_numpy(g).cuda()
+    for block in (2, 64, 128, 256, 2048):
+        o = torch.empty_like(dg)
+        kq.kq_hadamard_blockwise(dg, o, 8, 2048, block)
+        torch.cuda.synchronize()
+        assert np.array_equal(o.cpu().numpy(), kq.kq_hadamard_blockwise_host(g, block)), block
+    kq.kq_hadamard_blockwise(dg, dg, 8, 2048, 128)  # in place
+    torch.cuda.synchronize()
+    assert np.array_equal(dg.cpu().numpy(), kq.kq_hadamard_blockwise_host(g, 128))
+
+
+@pytest.mark.parametrize("fmt,n,k", [("q8_0", 1024, 2560), ("pq2_0", 10240, 5120), ("q8_0", 33, 96),
+                                     ("pq2_0", 17, 384)])
+def test_device_quantizer_and_prepare_bit_exact(kq, wl, fmt, n, k):
+    s = synth.stream_id("test", 0, 302)
+    W = wl.build_matrix(fmt, n, k, 3, s)
+    _sync_ok(kq)
+    w = synth.fill_host("w", n * k, 3, s).reshape(n, k)
+    ref = oracle.q8_0_quantize(w) if fmt == "q8_0" else oracle.pq2_0_quantize(oracle.rotate_rows(w)[1])
+    assert np.array_equal(_planes_as_blocks(kq, W), ref)
+    # debug dequantizer is bit-exact against the oracle's dequantizer
+    deq = torch.empty(n * k, dtype=torch.float32, device="cuda")
+    kq.kq_dequantize(W, deq)
+    _sync_ok(kq)
+    ref_deq = (oracle.q8_0_dequant if fmt == "q8_0" else oracle.pq2_0_dequant)(ref, n, k)
+    assert np.array_equal(deq.cpu().numpy().reshape(n, k), ref_deq)
+    # AoS blocks from the host quantizer, repacked on the device, give the same planes
+    W2 = kq.QMatrix(fmt, n, k)
+    blocks = torch.from_numpy(np.ascontiguousarray(ref).reshape(-1)).cuda()
+    kq.kq_prepare(W2, blocks)
+    _sync_ok(kq)
+    assert torch.equal(W2.codes, W.codes) and torch.equal(W2.scales, W.scales)
+
+
+def test_device_quantizer_flags_nonfinite_and_range(kq):
+    W = kq.QMatrix("q8_0", 2, 64)
+    w = torch.zeros(128, dtype=torch.float32, device="cuda")
+    w[5] = float("nan")
+    kq.kq_quantize_q8_0_device(W, w)
+    assert kq.kq_device_status(True) == kq.KQ_ERR_NONFINITE
+    w[5] = 1e7
+    kq.kq_quantize_q8_0_device(W, w)
+    assert kq.kq_device_status(True) == kq.KQ_ERR_RANGE
+    assert kq.kq_device_status(True) == kq.KQ_OK
+
+
+# ----------------------------------------------------------------------------
+# GEMV parity
+# ----------------------------------------------------------------------------
+
+SHAPES = [
+    ("q8_0", 1024, 2560),    # Q8_0 GEMV workload, full size
+    ("pq2_0", 10240, 5120),  # PQ2_0 GEMV workload, full size
+    ("q8_0", 1, 32), ("q8_0", 17, 96), ("q8_0", 72, 2592), ("q8_0", 33, 9728), ("q8_0", 5, 4096),
+    ("pq2_0", 1, 128), ("pq2_0", 15, 384), ("pq2_0", 72, 5248), ("pq2_0", 31, 17408), ("pq2_0", 48, 6144),
+]
+
+
+@pytest.mark.parametrize("fmt,n,k", SHAPES)
+def test_gemv_matches_oracle(kq, wl, fmt, n, k):
+    sw, sx = synth.stream_id("test", 0, 310), synth.stream_id("test", 1, 310)
+    W = wl.build_matrix(fmt, n, k, 0, sw)
+    x = wl.build_activation(k, 0, sx)
+    y = _run_gemv(kq, W, x)
+    w = synth.fill_host("w", n * k, 0, sw).reshape(n, k)
+    xh = synth.fill_host("x", k, 0, sx)
+    _, _, y_ref, absdot = oracle.reference(fmt, w, xh)
+    ok, worst = oracle.within_bound(y, y_ref, absdot, TOL)
+    assert ok, f"worst error/bound {worst}"
+    # deterministic: a second call gives the same bits
+    assert np.array_equal(_run_gemv(kq, W, x), y)
+
+
+def test_q8_0_exact_integer_case_tolerance_zero(kq):
+    # integer codes, power-of-two scales, small integer activations: every
+    # partial sum is an exact fp32 value, so the result must match exactly
+    rng = np.random.default_rng(11)
+    n, k = 72, 2816  # ragged rows and a K that is not a multiple of the chunk
+    q = rng.integers(-127, 128, size=(n, k))
+    q[:, ::32] = 127
+    w = (q * 2.0**-5).astype(np.float32)
+    x = rng.integers(-8, 9, size=k).astype(np.float32)
+    blocks, _, y_ref, _ = oracle.q8_0_reference(w, x)
+    W = kq.QMatrix("q8_0", n, k)
+    kq.kq_prepare(W, torch.from_numpy(blocks.reshape(-1)).cuda())
+    y = _run_gemv(kq, W, torch.from_numpy(x).cuda())
+    assert np.array_equal(y.astype(np.float64), y_ref)
+    assert np.array_equal(y_ref, (q @ x.astype(np.int64)) * 2.0**-5)
+
+
+def test_pq2_0_nonzero_mean_activation(kq, wl):
+    n, k = 96, 5120
+    sw = synth.stream_id("test", 0, 311)
+    W = wl.build_matrix("pq2_0", n, k, 0, sw)
+    xh = synth.fill_host("x", k, 0, synth.stream_id("test", 1, 311)) + np.float32(4.0)
+    y = _run_gemv(kq, W, torch.from_numpy(xh).cuda())
+    w = synth.fill_host("w", n * k, 0, sw).reshape(n, k)
+    _, _, y_ref, absdot = oracle.pq2_0_reference(w, xh)
+    ok, worst = oracle.within_bound(y, y_ref, absdot, TOL)
+    assert ok, worst
+
+
+def test_pq2_0_activation_scale_extremes(kq, wl):
+    # per-block exponent normalisation: tiny and huge activations keep precision
+    n, k = 32, 1024
+    sw = synth.stream_id("test", 0, 312)
+    W = wl.build_matrix("pq2_0", n, k, 0, sw)
+    w = synth.fill_host("w", n * k, 0, sw).reshape(n, k)
+    base = synth.fill_host("x", k, 0, synth.stream_id("test", 1, 312))
+    for scale in (2.0**-60, 2.0**-20, 1.0, 2.0**40):
+        xh = (base * np.float32(scale)).astype(np.float32)
+        xh[:128] *= np.float32(2.0**10)  # blocks of very different magnitude
+        y = _run_gemv(kq, W, torch.from_numpy(xh).cuda())
+        _, _, y_ref, absdot = oracle.pq2_0_reference(w, xh)
+        ok, worst = oracle.within_bound(y, y_ref, absdot, TOL)
+        assert ok, (scale, worst)
+
+
+@pytest.mark.parametrize("fmt,n,k", [("q8_0", 200, 9728), ("pq2_0", 120, 20480), ("pq2_0", 64, 5120)])
+def test_split_k(kq, wl, fmt, n, k):
+    sw, sx = synth.stream_id("test", 0, 320), synth.stream_id("test", 1, 320)
+    W = wl.build_matrix(fmt, n, k, 1, sw)
+    x = wl.build_activation(k, 1, sx)
+    w = synth.fill_host("w", n * k, 1, sw).reshape(n, k)
+    _, _, y_ref, absdot = oracle.reference(fmt, w, synth.fill_host("x", k, 1, sx))
+    outs = {}
+    for splits in (1, 2, 3, 0):
+        if splits == 1 and k > 18432:
+            continue
+        y = _run_gemv(kq, W, x, splits=splits)
+        ok, worst = oracle.within_bound(y, y_ref, absdot, TOL)
+        assert ok, (splits, worst)
+        assert np.array_equal(_run_gemv(kq, W, x, splits=splits), y)  # same plan, same bits
+        outs[splits] = y
+
+
+def test_workspace_too_small_is_rejected(kq, wl):
+    W = wl.build_matrix("pq2_0", 16, 20480, 0, synth.stream_id("test", 0, 321))
+    x = wl.build_activation(20480, 0, synth.stream_id("test", 1, 321))
+    y = torch.full((16,), 7.0, device="cuda")
+    need = kq.kq_gemv_workspace_bytes(W)
+    assert need > 0
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kq.KQError) as e:
+        kq.kq_gemv_pq2_0(W, x, y, ws)
+    assert e.value.status == kq.KQ_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(y == 7.0)
+
+
+# ----------------------------------------------------------------------------
+# small-M GEMM
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,n,k", [("q8_0", 9728, 2560), ("pq2_0", 17408, 5120), ("q8_0", 40, 288),
+                                     ("pq2_0", 24, 1152)])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 16, 64])
+def test_small_m_matches_oracle(kq, wl, fmt, n, k, m):
+    if n * k > 50_000_000 and m not in (1, 4, 16, 64):
+        pytest.skip("full-size matrices run only at the workload's M values")
+    sw, sx = synth.stream_id("test", 0, 330), synth.stream_id("test", 1, 330 + m)
+    W = wl.build_matrix(fmt, n, k, 2, sw)
+    X = wl.build_activation(k, 2, sx, rows=m)
+    Y = torch.empty(m * n, dtype=torch.float32, device="cuda")
+    kq.kq_gemm_small_m(W, X, m, Y)
+    _sync_ok(kq)
+    Y = Y.cpu().numpy().reshape(m, n)
+    rows = np.arange(n) if n * k <= 50_000_000 else np.unique(np.r_[0, n - 1, np.arange(7, n, 997)])
+    w = synth.matrix_rows_host(n, k, rows, 2, sw)
+    Xh = synth.fill_host("x", m * k, 2, sx).reshape(m, k)
+    if fmt == "pq2_0":
+        deq = oracle.pq2_0_dequant(oracle.pq2_0_quantize(oracle.rotate_rows(w)[1]), rows.size, k)
+        X64 = oracle.rotate_rows(Xh)[0]
+    else:
+        deq = oracle.q8_0_dequant(oracle.q8_0_quantize(w), rows.size, k)
+        X64 = Xh.astype(np.float64)
+    for i in range(m):
+        y_ref, absdot = oracle.gemv(deq, X64[i])
+        ok, worst = oracle.within_bound(Y[i, rows], y_ref, absdot, TOL)
+        assert ok, (i, worst)
+
+
+# ----------------------------------------------------------------------------
+# decode-step driver
+# ----------------------------------------------------------------------------
+
+def test_decode_plan_small_mixed_shapes(kq, wl):
+    spec = [(16, 256), (33, 1024), (1, 5120), (300, 2048), (17, 17408), (64, 128)]
+    for fmt in ("q8_0", "pq2_0"):
+        mats, xs, host = [], [], []
+        for i, (n, k) in enumerate(spec):
+            if fmt == "q8_0" and k % 32:
+                continue
+            sw, sx = synth.stream_id("test", 0, 340 + i), synth.stream_id("test", 1, 340 + i)
+            mats.append(wl.build_matrix(fmt, n, k, 4, sw))
+            xs.append(synth.fill_host("x", k, 4, sx))
+            host.append(synth.fill_host("w", n * k, 4, sw).reshape(n, k))
+        plan = kq.DecodePlan(mats)
+        x = torch.from_numpy(np.concatenate(xs)).cuda()
+        y = torch.empty(plan.y_floats, dtype=torch.float32, device="cuda")
+        plan.step(x, y)
+        _sync_ok(kq)
+        yh = y.cpu().numpy()
+        off = 0
+        for W, w, xh in zip(mats, host, xs):
+            _, _, y_ref, absdot = oracle.reference(fmt, w, xh)
+            ok, worst = oracle.within_bound(yh[off:off + W.n], y_ref, absdot, TOL)
+            assert ok, (fmt, W.n, W.k, worst)
+            # same tile geometry as the single GEMV, so the same bits
+            assert np.array_equal(yh[off:off + W.n], _run_gemv(kq, W, torch.from_numpy(xh).cuda()))
+            off += W.n
+        y2 = torch.empty_like(y)
+        plan.step(x, y2)
+        _sync_ok(kq)
+        assert torch.equal(y, y2)
+        plan.close()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("config", ["qwen3_4b_q8_0_step", "bonsai_27b_pq2_0_step"])
+def test_decode_step_full_size_sampled_rows(kq, wl, config):
+    W = wl.DecodeWorkload(config, seed=0)
+    W.step()
+    _sync_ok(kq)
+    y = W.y.cpu().numpy()
+    rng = np.random.default_rng(0)
+    worst_all = 0.0
+    for i, (_, fmt, n, k) in enumerate(W.mats_spec):
+        if i % 7 and i != len(W.mats_spec) - 1:
+            continue  # every 7th projection and the head
+        rows = np.unique(np.r_[0, n - 1, rng.integers(0, n, size=6)])
+        w, xh = W.host_rows(i, rows)
+        if fmt == "pq2_0":
+            blocks = oracle.pq2_0_quantize(oracle.rotate_rows(w)[1])
+            deq = oracle.pq2_0_dequant(blocks, rows.size, k)
+            x64 = oracle.rotate_rows(xh)[0]
+        else:
+            blocks = oracle.q8_0_quantize(w)
+            deq = oracle.q8_0_dequant(blocks, rows.size, k)
+            x64 = xh.astype(np.float64)
+        # the device planes of these rows hold the oracle's bytes
+        Wm = W.mats[i]
+        nb = k // kq.kq_block_size(fmt)
+        rb = kq.kq_codes_bytes(fmt, 1, k)
+        ss = kq.kq_scale_stride(fmt, k)
+        for t, r in enumerate(rows):
+            codes = Wm.codes[int(r) * rb:(int(r) + 1) * rb].cpu().numpy()
+            scales = Wm.scales[int(r) * ss:int(r) * ss + nb].cpu().numpy().view(np.uint16)
+            assert np.array_equal(codes, blocks[t, :, 2:].reshape(-1))
+            assert np.array_equal(scales, blocks[t, :, 0].astype(np.uint16) | (blocks[t, :, 1].astype(np.uint16) << 8))
+        y_ref, absdot = oracle.gemv(deq, x64)
+        off = int(W.y_offsets[i])
+        ok, worst = oracle.within_bound(y[off + rows], y_ref, absdot, TOL)
+        assert ok, (config, i, worst)
+        worst_all = max(worst_all, worst)
+    W.close()
+    print(f"{config}: worst error/bound over sampled rows {worst_all:.3g}")

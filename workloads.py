@@ -1,0 +1,87 @@
+"""Device-resident synthetic workloads, built through the library's public API.
+
+Values come from the seeded generator (``synth``, identical on host and
+device); weight preparation is the library's own: blockwise Walsh-Hadamard
+rotation (PQ2_0 only, rotate then quantize) and the device quantizers.  Used
+by the GPU tests and the benchmark; the oracle rebuilds any row of these
+matrices on the host from the same seeds.
+"""
+import numpy as np
+import torch
+
+import quantized_weight_streaming_gb300 as kq
+import synth
+
+
+def _fmt_name(fmt):
+    return fmt if isinstance(fmt, str) else ("q8_0" if fmt == kq.KQ_Q8_0 else "pq2_0")
+
+
+def build_matrix(fmt, n, k, seed, stream, tmp=None, device="cuda"):
+    """Quantized n x k matrix from generator stream (seed, stream).  tmp, if
+    given, is a float32 device tensor with at least n*k elements used as the
+    fp32 staging buffer."""
+    W = kq.QMatrix(fmt, n, k, device=device)
+    if tmp is None or tmp.numel() < n * k:
+        tmp = torch.empty(n * k, dtype=torch.float32, device=device)
+    w = tmp[: n * k]
+    synth.fill_device(w.data_ptr(), "w", n * k, seed, stream, cuda_stream=torch.cuda.current_stream().cuda_stream)
+    if _fmt_name(fmt) == "pq2_0":
+        kq.kq_hadamard_blockwise(w, w, n, k, 128)
+        kq.kq_quantize_pq2_0_device(W, w)
+    else:
+        kq.kq_quantize_q8_0_device(W, w)
+    return W
+
+
+def build_activation(k, seed, stream, rows=1, device="cuda"):
+    x = torch.empty(rows * k, dtype=torch.float32, device=device)
+    synth.fill_device(x.data_ptr(), "x", rows * k, seed, stream, cuda_stream=torch.cuda.current_stream().cuda_stream)
+    return x
+
+
+class DecodeWorkload:
+    """A decode-step workload: every projection quantized on the device, one
+    activation vector per projection packed into x, outputs packed into y."""
+
+    def __init__(self, config, seed=0, device="cuda"):
+        self.config = config
+        self.seed = seed
+        self.mats_spec = synth.workload(config)
+        big = max(n * k for _, _, n, k in self.mats_spec)
+        tmp = torch.empty(big, dtype=torch.float32, device=device)
+        self.mats = []
+        for i, (_, fmt, n, k) in enumerate(self.mats_spec):
+            self.mats.append(build_matrix(fmt, n, k, seed, synth.stream_id(config, synth.ROLE_W, i), tmp, device))
+        del tmp
+        self.x_offsets = np.cumsum([0] + [k for _, _, _, k in self.mats_spec])
+        self.y_offsets = np.cumsum([0] + [n for _, _, n, _ in self.mats_spec])
+        self.x = torch.empty(int(self.x_offsets[-1]), dtype=torch.float32, device=device)
+        for i, (_, _, _, k) in enumerate(self.mats_spec):
+            off = int(self.x_offsets[i])
+            synth.fill_device(self.x[off:].data_ptr(), "x", k, seed, synth.stream_id(config, synth.ROLE_X, i),
+                              cuda_stream=torch.cuda.current_stream().cuda_stream)
+        self.y = torch.empty(int(self.y_offsets[-1]), dtype=torch.float32, device=device)
+        self.plan = kq.DecodePlan(self.mats)
+        assert self.plan.x_floats == self.x.numel() and self.plan.y_floats == self.y.numel()
+
+    @property
+    def weight_bytes(self):
+        return self.plan.weight_bytes
+
+    @property
+    def activation_bytes(self):
+        return 4 * (self.x.numel() + self.y.numel())
+
+    def step(self, stream=None):
+        self.plan.step(self.x, self.y, stream=stream)
+
+    def host_rows(self, i, rows):
+        """(W rows fp32, x fp32) of projection i regenerated on the host."""
+        _, _, n, k = self.mats_spec[i]
+        w = synth.matrix_rows_host(n, k, rows, self.seed, synth.stream_id(self.config, synth.ROLE_W, i))
+        x = synth.fill_host("x", k, self.seed, synth.stream_id(self.config, synth.ROLE_X, i))
+        return w, x
+
+    def close(self):
+        self.plan.close()
