@@ -82,3 +82,24 @@ __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t count) {
 }
 
 }  // namespace kq
+
+namespace kq {
+
+// 2-D tiled TMA load (cp.async.bulk.tensor) of the box at element coordinates
+// (x, y) of the tensor map at `tmap` (a CUtensorMap in param or global memory)
+// into this CTA's shared memory, completing on `bar`.  x is the innermost
+// coordinate; callers keep x * element size a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+}  // namespace kq

@@ -2,39 +2,49 @@
 // decode-step driver, for the Q8_0 and PQ2_0 block formats.
 //
 // Decode is bound by streaming every weight once per token ("Kipp
-// Benchmarks", "Decode is weight-bandwidth-bound"); the kernel therefore does
-// nothing but keep HBM busy and dequantize in registers:
+// Benchmarks", "Decode is weight-bandwidth-bound"); the kernel does nothing
+// but keep HBM busy and dequantize in registers:
 //
-//  * One persistent CTA per SM: warp 0 is the producer, eight consumer warps
-//    compute.  The producer copies tiles of 16 weight rows (codes plane plus
-//    scales plane) into a ring of shared-memory stages with 1-D bulk copies
-//    (cp.async.bulk, completion counted on an mbarrier, L2 evict-first since
-//    every weight byte is read exactly once).
-//  * Work is a list of items (matrix, 16-row group, K split).  Each CTA owns a
-//    contiguous run of items, so it changes matrices rarely; every item walks
-//    its K range in chunks (one chunk per stage).
-//  * When a CTA starts an item of a new (matrix, split), its consumer warps
-//    stage the activation slice in shared memory.  For PQ2_0 this prologue
-//    applies the blockwise normalised Walsh-Hadamard transform (x' = R x,
-//    "Bonsai 2 27B - ternary g128 + blockwise Hadamard", section 4.2) in
-//    registers and warp shuffles, fused into the load.
+//  * One persistent CTA per SM: warp 0 is the producer, sixteen consumer
+//    warps compute.  A tile is 128 weight rows x 256 bytes of codes (256
+//    Q8_0 weights or 1024 PQ2_0 weights per row) plus the matching 128 x 8
+//    fp16 scales.  The producer brings each tile into a ring of four
+//    shared-memory stages with two 2-D TMA loads (cp.async.bulk.tensor over
+//    tensor maps of the row-major planes; rows past n and columns past k come
+//    back as zeros), completion counted on an mbarrier, L2 evict-first since
+//    every weight byte is read exactly once.
+//  * Work is a list of items (matrix, 128-row block, K split).  Each CTA owns
+//    a contiguous run of items, so it changes matrices rarely; an item walks
+//    its K range one 256-byte chunk (one tile) at a time.
+//  * Consumer warp w owns rows 8w..8w+7 of every tile and lane l the l-th
+//    8-byte granule of each row (8 Q8_0 or 32 PQ2_0 weights): eight
+//    independent FMA chains per lane, the granule's activations loaded once
+//    (conflict-free 16-byte loads from a swizzled layout) and reused by the
+//    eight rows, per-row sums kept in registers across the item's tiles.
+//  * When a CTA starts an item of a new (matrix, split), its consumers stage
+//    the activation slice in shared memory.  For PQ2_0 this prologue applies
+//    the blockwise normalised Walsh-Hadamard transform (x' = R x, "Bonsai 2
+//    27B - ternary g128 + blockwise Hadamard", section 4.2) in registers and
+//    warp shuffles, fused into the load.
 //  * Q8_0 dot: sum_b d_b sum_j q_j x_j with the int8 code turned into an fp32
 //    integer by a byte permute into the mantissa of 2^23 and one subtract.
 //  * PQ2_0 dot: sum_b d_b (sum_j c_j x'_j - sum_j x'_j) with c in {0,1,2}
-//    (the ternary value is c-1; the -1 is folded into a precomputed activation
-//    sum, an idea the Bonsai page, section 8.5, uses on Metal).  A 2-bit code
-//    masked in place inside its 32-bit word IS an fp32 denormal c * 4^j *
-//    2^-149, so one AND per code produces the FMA operand; the activation is
-//    pre-scaled by the matching power of two in the prologue, which keeps the
-//    arithmetic exact up to fp32 rounding of the sums.
-//  * Each output row is reduced across lanes with shuffles in a fixed order;
-//    with K splits, partials land in the workspace and a second pass adds them
-//    in split order.  Results never depend on the grid size.
+//    (the ternary value is c-1; the -1 is folded into a precomputed
+//    activation sum, as the Bonsai page, section 8.5, does on Metal).  A 2-bit
+//    code masked in place inside its 32-bit word IS an fp32 denormal
+//    c * 4^j * 2^-149, so one AND per code produces the FMA operand; the
+//    activation is pre-scaled by the matching power of two in the prologue.
+//  * Each output is reduced across lanes with shuffles in a fixed order; with
+//    K splits, partials land in the workspace and a second pass adds them in
+//    split order.  Results never depend on the grid size.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <vector>
 
 #include "kq_device.cuh"
@@ -43,47 +53,50 @@
 namespace kq {
 
 // ---- geometry ---------------------------------------------------------------
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kTileRows = 16;                            // rows per tile
-constexpr int kRowsPerWarp = kTileRows / kConsumerWarps;  // 2
-constexpr int kStageCodeBytes = 24576;                   // codes bytes per stage (1536 per row)
-constexpr int kStageScaleBytes = kTileRows * 96;          // up to 48 scales per row
-constexpr int kStageBytes = kStageCodeBytes + kStageScaleBytes;
-constexpr int kStages = 5;
-constexpr int kXMax = 18432;                             // activation floats staged per item (all m)
-constexpr int kGranMax = kXMax / 32;                     // PQ2_0 per-granule side arrays
-constexpr size_t kSmemBytes =
-    (size_t)kStages * kStageBytes + (size_t)kXMax * 4 + 2 * (size_t)kGranMax * 4 + 2 * kStages * 8 + 16;
+constexpr int kRowsPerWarp = 8;
+constexpr int kTileRows = kConsumerWarps * kRowsPerWarp;  // 128
+constexpr int kChunkBytes = 256;                          // code bytes per row per tile (32 lanes x 8 B)
+constexpr int kTileCodeBytes = kTileRows * kChunkBytes;    // 32 KB
+constexpr int kTileScaleBytes = kTileRows * 16;            // 8 fp16 scales per row per tile
+constexpr int kStageBytes = kTileCodeBytes + kTileScaleBytes;
+constexpr int kStages = 4;
+constexpr int kXMax = 18432;          // activation floats (or B-fragment words) staged per item (all m)
+constexpr int kBlkMax = kXMax / 128;  // PQ2_0 per-block side arrays
+constexpr int kScratchFloats = 128;   // per-warp scratch (one Hadamard block)
+constexpr int kCombineFloats = 8 * 64;  // K-half partials handed between paired warps
+constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kXMax * 4 + 2 * (size_t)kBlkMax * 4 +
+                              (size_t)kConsumerWarps * kScratchFloats * 4 + (size_t)kCombineFloats * 4 +
+                              2 * kStages * 8 + 16;
 
 __device__ unsigned int g_stream_status = 0;
 __device__ __forceinline__ void stream_flag(int status) { atomicOr(&g_stream_status, 1u << status); }
 
 // One matrix of the work list.
 struct Job {
-  const uint8_t* codes;
-  const uint16_t* scales;
   const float* x;  // m rows, row stride k
   float* y;        // m rows, row stride ldy (splits == 1)
   float* ws;       // [splits][m][n] partials (splits > 1)
   int64_t n, k, ldy;
   int64_t x_off, y_off;  // offsets into the packed activation / output (decode plan)
   int64_t item_begin;    // first global item of this job
-  int64_t items;       // row_groups * splits
-  int32_t sstride;     // scales row stride (halves)
-  int32_t row_groups;
+  int64_t items;         // row_blocks * splits
+  int32_t row_blocks;
   int32_t splits;
-  int32_t split_k;  // weights per split (multiple of the alignment unit)
-  int32_t chunk_k;  // weights per tile (multiple of the alignment unit)
+  int32_t split_k;  // weights per split (multiple of the chunk)
+  int32_t pad;
 };
 
 struct Params {
-  Job job0;                // used when jobs == nullptr
-  const Job* jobs;         // device table (decode plan)
-  const float* x_base;     // packed activations (decode plan)
-  float* y_base;           // packed outputs (decode plan)
-  const int64_t* bounds;   // per-CTA item ranges [bounds[c], bounds[c+1]) (plan), or nullptr
-  int32_t njobs;
+  CUtensorMap map_codes0;  // single GEMV / GEMM: maps of the one matrix
+  CUtensorMap map_scales0;
+  Job job0;
+  const Job* jobs;          // decode plan: device table of jobs ...
+  const CUtensorMap* maps;  // ... and their maps, [2 * j] codes, [2 * j + 1] scales
+  const float* x_base;      // packed activations (decode plan)
+  float* y_base;            // packed outputs (decode plan)
+  const int64_t* bounds;    // per-CTA item ranges [bounds[c], bounds[c+1]) (plan), or nullptr
   int64_t total_items;
 };
 
@@ -93,25 +106,31 @@ template <>
 struct Fmt<KQ_Q8_0> {
   static constexpr int kBlock = 32;
   static constexpr int kCodesPerByte = 1;
-  static constexpr int kAlign = 256;    // split / chunk unit: 32 granules of 8 codes, 8 scales
-  static constexpr int kCodesPerGran = 8;
+  static constexpr int kChunk = kChunkBytes;  // 256 weights per tile row
+  static constexpr int kGran = 8;             // weights per lane per tile row
 };
 template <>
 struct Fmt<KQ_PQ2_0> {
   static constexpr int kBlock = 128;
   static constexpr int kCodesPerByte = 4;
-  static constexpr int kAlign = 1024;   // 32 granules of 32 codes, 8 scales
-  static constexpr int kCodesPerGran = 32;
+  static constexpr int kChunk = kChunkBytes * 4;  // 1024 weights per tile row
+  static constexpr int kGran = 32;
 };
 
-// Item -> (job, row group, split).  Items of a job are split-major.
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+// Item -> (job, row block, split).  Items of a job are split-major.
 struct ItemCursor {
   int32_t j = -1;
   Job job;
+  const CUtensorMap* mc = nullptr;
+  const CUtensorMap* ms = nullptr;
   __device__ void seek(const Params& p, int64_t item) {
     if (p.jobs == nullptr) {
       if (j < 0) {
         job = p.job0;
+        mc = &p.map_codes0;
+        ms = &p.map_scales0;
         j = 0;
       }
       return;
@@ -133,6 +152,8 @@ struct ItemCursor {
     job = p.jobs[j];
     job.x = p.x_base + job.x_off;
     job.y = p.y_base + job.y_off;
+    mc = p.maps + 2 * j;
+    ms = p.maps + 2 * j + 1;
   }
 };
 
@@ -146,32 +167,97 @@ __device__ __forceinline__ void cta_range(const Params& p, int64_t& b, int64_t& 
   }
 }
 
-__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
-
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }  // e in [-126, 127]
 
-// Position of code j (0..15) of a 32-bit word in the masked-denormal view:
-// codes 0..11 are masked in place (bits 2j), codes 12..15 after a shift by 24.
-__device__ __forceinline__ int code_bitpos(int j) { return j < 12 ? 2 * j : 2 * (j - 12); }
+// Q8_0 swizzled activation layout: the 8 activations of lane l in tile chunk
+// t are read as two 16-byte pieces c = 0, 1 at [t][c][l], so the 32 lanes of
+// a warp read 512 contiguous bytes per load.  Index of the float4 holding
+// positions p..p+3 (p % 4 == 0) of the staged slice.
+__device__ __forceinline__ int q8_swz4(int p) {
+  const int t = p / 256, r = p % 256;
+  return t * 64 + ((r % 8) / 4) * 32 + r / 8;
+}
+
+// ---------------------------------------------------------------------------
+// PQ2_0 on the tensor cores: mma.sync.m16n8k16, f16 x f16 -> f32.
+//
+// A (16 weight rows x 16 codes).  A 2-bit code masked in place inside a
+// 16-bit half is an exact fp16 denormal c * 2^(s-24) while its bit position
+// s <= 10; one AND with 0x00030003 << s therefore turns the two codes at bits
+// s and 16+s of a 32-bit code word (word elements s/2 and 8+s/2) into one
+// half2 A register, and one shift right by 4 brings the pairs at 12 and 14
+// down to 8 and 10.  Thread (g = lane/4, t = lane%4) owns word t of every
+// group of four words of rows g and g+8 and feeds all 16 of its codes to the
+// four MMAs of that group: MMA j takes the pairs at s = 4j and 4j+2 (after
+// the shift for j = 3), i.e. logical k (2t, 2t+1) <- word elements
+// (2j, 2j+8) and (2t+8, 2t+9) <- (2j+1, 2j+9).  Per 16 codes: one shift and
+// eight ANDs with immediates.
+//
+// B (16 codes x 8 columns): column 2m holds the high fp16 part and 2m+1 the
+// low part of activation row m, x' * 2^-E (|.| < 2) scaled by 2^(14-s) to
+// match its code's denormal scale; every product is c * x' * 2^(-10-E)
+// exactly.  A block of 128 codes is 8 MMAs, then its scale d is applied:
+//     y += d * (2^(10+E) * (C_hi + C_lo) - sum_j x'_j)
+//
+// The codes of a tile arrive as two 128-byte-wide TMA boxes with the 128-byte
+// swizzle (16-byte chunk c of box row r stored at chunk c ^ (r % 8)), so the
+// 32 lanes of a word load touch 32 distinct banks.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                          uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// denormal bit position (after the shift for j = 3) of the pair of register
+// `reg` (0: elements 2j, 2j+8; 1: elements 2j+1, 2j+9) of MMA j
+__host__ __device__ __forceinline__ int pair_bit(int j, int reg) { return j < 3 ? 4 * j + 2 * reg : 8 + 2 * reg; }
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
+}
+
+// Byte offset, inside a stage, of code byte `col` (0..255) of tile row `row`
+// for the two 128-byte swizzled half boxes.
+__device__ __forceinline__ int swz_code_offset(int row, int col) {
+  const int half = col >> 7, o = col & 127;
+  return half * (kTileRows * 128) + row * 128 + ((((o >> 4) ^ (row & 7))) << 4) + (o & 15);
+}
+
+// B table entry (uint2) of (block b of the slice, word group q, MMA j,
+// column n < 2M, thread t): 64 M entries of 8 bytes per block of 128
+// positions, i.e. 4 M bytes per position, the size of M fp32 activations.
+template <int M>
+__device__ __forceinline__ int btab_index(int b, int q, int j, int n, int t) {
+  return (((b * 2 + q) * 4 + j) * (2 * M) + n) * 4 + t;
+}
 
 // ---------------------------------------------------------------------------
 // Activation prologue: stage x[m][kbeg, kend) of the current job.
+//  Q8_0: fp32 activations in the swizzled layout.
+//  PQ2_0: blockwise Walsh-Hadamard transform, then the B table of every
+//  block, plus per block the factor 2^(10+E) and the sum of x'.
 // ---------------------------------------------------------------------------
 template <int FMT, int M>
-__device__ void stage_activation(const Job& job, int64_t kbeg, int64_t kend, float* xbuf, float* fx, float* sx,
-                                 int cw, int lane) {
+__device__ void stage_activation(const Job& job, int64_t kbeg, int64_t kend, int xlen_pad, float* xbuf, float* fx,
+                                 float* sx, float* scratch, int cw, int lane) {
   const int len = (int)(kend - kbeg);
+  constexpr int kT = 32 * kConsumerWarps;
   if (FMT == KQ_Q8_0) {
+    float4* xb4 = reinterpret_cast<float4*>(xbuf);
     for (int m = 0; m < M; ++m) {
       const float4* src = reinterpret_cast<const float4*>(job.x + (int64_t)m * job.k + kbeg);
-      float4* dst = reinterpret_cast<float4*>(xbuf + m * len);
-      for (int i = cw * 32 + lane; i < len / 4; i += kConsumerWarps * 32) dst[i] = src[i];
+      for (int i = cw * 32 + lane; i < len / 4; i += kT) xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] = src[i];
     }
   } else {
     const int nblk = len / 128;
+    uint2* btab = reinterpret_cast<uint2*>(xbuf);
     const float inv_sqrt128 = 0.08838834764831845f;
-    for (int t = cw; t < M * nblk; t += kConsumerWarps) {
-      const int m = t / nblk, b = t % nblk;
+    for (int tt = cw; tt < M * nblk; tt += kConsumerWarps) {
+      const int m = tt / nblk, b = tt % nblk;
       float4 f = *reinterpret_cast<const float4*>(job.x + (int64_t)m * job.k + kbeg + b * 128 + 4 * lane);
       float v[4] = {f.x, f.y, f.z, f.w};
       // fast Walsh-Hadamard transform, natural (Sylvester) order: strides 1, 2 in registers ...
@@ -204,129 +290,119 @@ __device__ void stage_activation(const Job& job, int64_t kbeg, int64_t kend, flo
       const float unscale = pow2f(-e);
       float s = v[0] + v[1] + v[2] + v[3];
 #pragma unroll
-      for (int mk = 1; mk < 8; mk <<= 1) s += __shfl_xor_sync(0xffffffffu, s, mk);
-      float4 o;
-      float* op = &o.x;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int j = (4 * lane + i) & 15;  // code index inside its 32-bit word
-        op[i] = (v[i] * unscale) * pow2f(126 - code_bitpos(j));
-      }
-      *reinterpret_cast<float4*>(xbuf + m * len + b * 128 + 4 * lane) = o;
-      if ((lane & 7) == 0) {
-        const int g = m * (len / 32) + b * 4 + lane / 8;
-        sx[g] = s;
-        fx[g] = pow2f(23 + e);
+      for (int mk = 16; mk; mk >>= 1) s += __shfl_xor_sync(0xffffffffu, s, mk);
+      // the normalised block goes through the warp's scratch; lane (q, j, t)
+      // then builds the high and low B entries of word 4q+t for MMA j
+      __syncwarp();
+      *reinterpret_cast<float4*>(scratch + 4 * lane) =
+          make_float4(v[0] * unscale, v[1] * unscale, v[2] * unscale, v[3] * unscale);
+      __syncwarp();
+      const int t = lane & 3, j = (lane >> 2) & 3, q = lane >> 4;
+      const float* xw = scratch + 16 * (4 * q + t);
+      const float s0 = pow2f(14 - pair_bit(j, 0)), s1 = pow2f(14 - pair_bit(j, 1));
+      const float u0 = xw[2 * j] * s0, u1 = xw[2 * j + 8] * s0, u2 = xw[2 * j + 1] * s1, u3 = xw[2 * j + 9] * s1;
+      const float h0 = __half2float(__float2half_rn(u0)), h1 = __half2float(__float2half_rn(u1));
+      const float h2 = __half2float(__float2half_rn(u2)), h3 = __half2float(__float2half_rn(u3));
+      btab[btab_index<M>(b, q, j, 2 * m, t)] = make_uint2(pack_half2(h0, h1), pack_half2(h2, h3));
+      btab[btab_index<M>(b, q, j, 2 * m + 1, t)] =
+          make_uint2(pack_half2(u0 - h0, u1 - h1), pack_half2(u2 - h2, u3 - h3));
+      if (lane == 0) {
+        const int gb = m * (xlen_pad / 128) + b;
+        sx[gb] = s;
+        fx[gb] = pow2f(10 + e);
       }
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Consumer math for one stage.
+// Q8_0 consumer math for one tile: rows 8w..8w+7, granule `lane` of chunk `ci`.
 // ---------------------------------------------------------------------------
 template <int M>
-__device__ __forceinline__ void q8_0_tile(const uint8_t* st_codes, const uint16_t* st_scales, int kc, int sp,
-                                          int rows, int xoff, int xlen, const float* xbuf, int cw, int lane,
+__device__ __forceinline__ void q8_0_tile(const uint8_t* st_codes, const uint16_t* st_scales, int rows, int ci,
+                                          int xlen_pad, const float* xbuf, int cw, int lane,
                                           float (&acc)[kRowsPerWarp][M]) {
-  const int G = kc / 8;
-  for (int g = lane; g < G; g += 32) {
-    float4 xa[M], xb[M];
+  float4 xa[M], xb[M];
+#pragma unroll
+  for (int m = 0; m < M; ++m) {
+    const float4* xp = reinterpret_cast<const float4*>(xbuf + m * xlen_pad) + ci * 64 + lane;
+    xa[m] = xp[0];
+    xb[m] = xp[32];
+  }
+#pragma unroll
+  for (int r = 0; r < kRowsPerWarp; ++r) {
+    const int row = cw * kRowsPerWarp + r;
+    if (row >= rows) break;
+    const uint2 c = *reinterpret_cast<const uint2*>(st_codes + row * kChunkBytes + lane * 8);
+    const float d = __half2float(__ushort_as_half(st_scales[row * 8 + lane / 4]));
+    const uint32_t u0 = c.x ^ 0x80808080u, u1 = c.y ^ 0x80808080u;
+    constexpr float kMagic = 8388736.0f;  // 2^23 + 128
+    float q[8];
+    q[0] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7540)) - kMagic;
+    q[1] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7541)) - kMagic;
+    q[2] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7542)) - kMagic;
+    q[3] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7543)) - kMagic;
+    q[4] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7540)) - kMagic;
+    q[5] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7541)) - kMagic;
+    q[6] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7542)) - kMagic;
+    q[7] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7543)) - kMagic;
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      const float4* xp = reinterpret_cast<const float4*>(xbuf + m * xlen + xoff + g * 8);
-      xa[m] = xp[0];
-      xb[m] = xp[1];
-    }
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const int row = cw * kRowsPerWarp + r;
-      if (row >= rows) break;
-      const uint2 c = *reinterpret_cast<const uint2*>(st_codes + row * kc + g * 8);
-      const float d = __half2float(__ushort_as_half(st_scales[row * sp + g / 4]));
-      const uint32_t u0 = c.x ^ 0x80808080u, u1 = c.y ^ 0x80808080u;
-      constexpr float kMagic = 8388736.0f;  // 2^23 + 128
-      float q[8];
-      q[0] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7540)) - kMagic;
-      q[1] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7541)) - kMagic;
-      q[2] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7542)) - kMagic;
-      q[3] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7543)) - kMagic;
-      q[4] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7540)) - kMagic;
-      q[5] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7541)) - kMagic;
-      q[6] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7542)) - kMagic;
-      q[7] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7543)) - kMagic;
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        float p = q[0] * xa[m].x;
-        p = fmaf(q[1], xa[m].y, p);
-        p = fmaf(q[2], xa[m].z, p);
-        p = fmaf(q[3], xa[m].w, p);
-        p = fmaf(q[4], xb[m].x, p);
-        p = fmaf(q[5], xb[m].y, p);
-        p = fmaf(q[6], xb[m].z, p);
-        p = fmaf(q[7], xb[m].w, p);
-        acc[r][m] = fmaf(d, p, acc[r][m]);
-      }
+      float p = q[0] * xa[m].x;
+      p = fmaf(q[1], xa[m].y, p);
+      p = fmaf(q[2], xa[m].z, p);
+      p = fmaf(q[3], xa[m].w, p);
+      p = fmaf(q[4], xb[m].x, p);
+      p = fmaf(q[5], xb[m].y, p);
+      p = fmaf(q[6], xb[m].z, p);
+      p = fmaf(q[7], xb[m].w, p);
+      acc[r][m] = fmaf(d, p, acc[r][m]);
     }
   }
 }
 
-// 16 codes of one word against 16 pre-scaled activations.
-__device__ __forceinline__ float ternary_word(uint32_t w, const float* xt, float a) {
-#pragma unroll
-  for (int j = 0; j < 12; ++j) a = fmaf(__uint_as_float(w & (3u << (2 * j))), xt[j], a);
-  const uint32_t h = w >> 24;
-#pragma unroll
-  for (int j = 12; j < 16; ++j) a = fmaf(__uint_as_float(h & (3u << (2 * (j - 12)))), xt[j], a);
-  return a;
-}
-
+// ---------------------------------------------------------------------------
+// PQ2_0 consumer math for one tile: warp cw takes the 16-row slab cw % 8 and
+// the K half cw / 8 (4 blocks, 512 codes per row).  acc[0] / acc[1] are the
+// partial outputs of rows g and g+8 for activation row m = t.
+// ---------------------------------------------------------------------------
 template <int M>
-__device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16_t* st_scales, int kc, int sp,
-                                           int rows, int xoff, int xlen, const float* xbuf, const float* fx,
-                                           const float* sx, int cw, int lane, float (&acc)[kRowsPerWarp][M]) {
-  const int G = kc / 32;       // granules of 32 codes (two words, 8 bytes) per row
-  const int pitch = kc / 4;    // code bytes per row in the stage
-  const int gl = xlen / 32;    // granules per activation row in the side arrays
-  for (int g = lane; g < G; g += 32) {
-    uint2 c[kRowsPerWarp];
-    float d[kRowsPerWarp];
+__device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16_t* st_scales, int rows, int ci,
+                                           int nblk_valid, int xlen_pad, const float* xbuf, const float* fx,
+                                           const float* sx, int cw, int lane, float (&acc)[2]) {
+  const int slab = cw & 7, kh = cw >> 3;
+  if (slab * 16 >= rows) return;
+  const int g = lane >> 2, t = lane & 3;
+  const int rA = slab * 16 + g, rB = rA + 8;
+  const uint2* btab = reinterpret_cast<const uint2*>(xbuf);
+  const bool has_b = g < 2 * M;
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-      const int row = cw * kRowsPerWarp + r;
-      const int rr = row < rows ? row : 0;
-      c[r] = *reinterpret_cast<const uint2*>(st_codes + rr * pitch + g * 8);
-      d[r] = __half2float(__ushort_as_half(st_scales[rr * sp + g / 4]));
-    }
-    float a[kRowsPerWarp][M];
+  for (int blk = 0; blk < 4; ++blk) {
+    const int bt = kh * 4 + blk;  // block inside the tile row
+    if (bt >= nblk_valid) break;
+    const int b = ci * 8 + bt;  // block inside the staged slice
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r)
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t wa = *reinterpret_cast<const uint32_t*>(st_codes + swz_code_offset(rA, bt * 32 + 16 * q + 4 * t));
+      const uint32_t wb = *reinterpret_cast<const uint32_t*>(st_codes + swz_code_offset(rB, bt * 32 + 16 * q + 4 * t));
+      const uint32_t ha = wa >> 4, hb = wb >> 4;
 #pragma unroll
-      for (int m = 0; m < M; ++m) a[r][m] = 0.f;
-#pragma unroll
-    for (int wi = 0; wi < 2; ++wi) {
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        float xt[16];
-        const float4* xp = reinterpret_cast<const float4*>(xbuf + m * xlen + xoff + g * 32 + wi * 16);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 t = xp[i];
-          xt[4 * i] = t.x;
-          xt[4 * i + 1] = t.y;
-          xt[4 * i + 2] = t.z;
-          xt[4 * i + 3] = t.w;
-        }
-#pragma unroll
-        for (int r = 0; r < kRowsPerWarp; ++r) a[r][m] = ternary_word(wi ? c[r].y : c[r].x, xt, a[r][m]);
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t m0 = 0x00030003u << pair_bit(j, 0), m1 = 0x00030003u << pair_bit(j, 1);
+        const uint32_t xa = j < 3 ? wa : ha, xb = j < 3 ? wb : hb;
+        uint2 bf = make_uint2(0u, 0u);
+        if (has_b) bf = btab[btab_index<M>(b, q, j, g, t)];
+        mma_16816(c, xa & m0, xb & m0, xa & m1, xb & m1, bf.x, bf.y);
       }
     }
-    const int gi = (xoff / 32) + g;
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-      const float f = fx[m * gl + gi], s = sx[m * gl + gi];
-#pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) acc[r][m] = fmaf(d[r], fmaf(f, a[r][m], -s), acc[r][m]);
+    const float dA = __half2float(__ushort_as_half(st_scales[rA * 8 + bt]));
+    const float dB = __half2float(__ushort_as_half(st_scales[rB * 8 + bt]));
+    if (t < M) {
+      const int gb = t * (xlen_pad / 128) + b;
+      const float F = fx[gb], S = sx[gb];
+      acc[0] = fmaf(dA, fmaf(F, c[0] + c[1], -S), acc[0]);
+      acc[1] = fmaf(dB, fmaf(F, c[2] + c[3], -S), acc[1]);
     }
   }
 }
@@ -337,12 +413,14 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
 template <int FMT, int M>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ Params p) {
   using F = Fmt<FMT>;
-  extern __shared__ __align__(128) uint8_t smem[];
+  extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
   float* fx = xbuf + kXMax;
-  float* sx = fx + kGranMax;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sx + kGranMax);
+  float* sx = fx + kBlkMax;
+  float* scratch_all = sx + kBlkMax;
+  float* combine = scratch_all + kConsumerWarps * kScratchFloats;
+  uint64_t* full = reinterpret_cast<uint64_t*>(combine + kCombineFloats);
   uint64_t* empty = full + kStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
 
@@ -367,21 +445,21 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       ItemCursor cur;
       int64_t tile = 0;
       bool ok = true;
+      int32_t last_j = -1;
       for (int64_t item = ib; item < ie && ok; ++item) {
         cur.seek(p, item);
+        if (cur.j != last_j) {
+          prefetch_tmap(cur.mc);
+          prefetch_tmap(cur.ms);
+          last_j = cur.j;
+        }
         const Job& job = cur.job;
         const int64_t local = item - job.item_begin;
-        const int split = (int)(local / job.row_groups);
-        const int rg = (int)(local % job.row_groups);
-        const int64_t row0 = (int64_t)rg * kTileRows;
-        const int rows = (int)min64(kTileRows, job.n - row0);
+        const int split = (int)(local / job.row_blocks);
+        const int rb = (int)(local % job.row_blocks);
         const int64_t kbeg = (int64_t)split * job.split_k;
         const int64_t kend = min64(job.k, kbeg + job.split_k);
-        const int64_t rowbytes = job.k / F::kCodesPerByte;
-        for (int64_t k0 = kbeg; k0 < kend; k0 += job.chunk_k, ++tile) {
-          const int kc = (int)min64(job.chunk_k, kend - k0);
-          const int cbytes = kc / F::kCodesPerByte;
-          const int sp = ((kc / F::kBlock) + 7) & ~7;
+        for (int64_t k0 = kbeg; k0 < kend; k0 += F::kChunk, ++tile) {
           const int s = (int)(tile % kStages);
           const uint32_t par = (uint32_t)((tile / kStages) & 1);
           if (*abort_flag || !mbar_wait_bounded(&empty[s], par ^ 1u)) {
@@ -391,19 +469,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
             break;
           }
           uint8_t* st = stages + (size_t)s * kStageBytes;
-          uint8_t* st_scales = st + rows * cbytes;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)(rows * (cbytes + 2 * sp)));
-          if (kc == job.k) {
-            bulk_g2s(st, job.codes + row0 * rowbytes, (uint32_t)(rows * cbytes), &full[s], policy);
-            bulk_g2s(st_scales, job.scales + row0 * job.sstride, (uint32_t)(rows * 2 * sp), &full[s], policy);
-          } else {
-            for (int r = 0; r < rows; ++r) {
-              bulk_g2s(st + r * cbytes, job.codes + (row0 + r) * rowbytes + k0 / F::kCodesPerByte, (uint32_t)cbytes,
-                       &full[s], policy);
-              bulk_g2s(st_scales + r * 2 * sp, job.scales + (row0 + r) * job.sstride + k0 / F::kBlock,
-                       (uint32_t)(2 * sp), &full[s], policy);
-            }
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
+          // codes: u32 elements, x = k0 code bytes / 4; scales: u32 elements (2 fp16), x = k0 / block / 2
+          const int32_t xc = (int32_t)(k0 / F::kCodesPerByte / 4);
+          if (FMT == KQ_Q8_0) {
+            tma_load_2d(st, cur.mc, xc, rb * kTileRows, &full[s], policy);
+          } else {  // two 128-byte swizzled half boxes
+            tma_load_2d(st, cur.mc, xc, rb * kTileRows, &full[s], policy);
+            tma_load_2d(st + kTileRows * 128, cur.mc, xc + 32, rb * kTileRows, &full[s], policy);
           }
+          tma_load_2d(st + kTileCodeBytes, cur.ms, (int32_t)(k0 / F::kBlock / 2), rb * kTileRows, &full[s], policy);
         }
       }
       // Never leave the CTA with copies in flight: wait for the last stages issued.
@@ -415,39 +490,40 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 
   // -------------------------------- consumers --------------------------------
   const int cw = warp - 1;
+  float* scratch = scratch_all + cw * kScratchFloats;
   ItemCursor cur;
   int32_t cached_job = -1, cached_split = -1;
   int64_t tile = 0;
+  int xlen_pad = 0;
   for (int64_t item = ib; item < ie; ++item) {
     cur.seek(p, item);
     const Job& job = cur.job;
     const int64_t local = item - job.item_begin;
-    const int split = (int)(local / job.row_groups);
-    const int rg = (int)(local % job.row_groups);
-    const int64_t row0 = (int64_t)rg * kTileRows;
+    const int split = (int)(local / job.row_blocks);
+    const int rb = (int)(local % job.row_blocks);
+    const int64_t row0 = (int64_t)rb * kTileRows;
     const int rows = (int)min64(kTileRows, job.n - row0);
     const int64_t kbeg = (int64_t)split * job.split_k;
     const int64_t kend = min64(job.k, kbeg + job.split_k);
-    const int xlen = (int)(kend - kbeg);
     if (cur.j != cached_job || split != cached_split) {
+      xlen_pad = (int)(((kend - kbeg) + F::kChunk - 1) / F::kChunk * F::kChunk);
       named_barrier(1, kConsumerWarps * 32);  // everyone is done with the previous slice
-      stage_activation<FMT, M>(job, kbeg, kend, xbuf, fx, sx, cw, lane);
+      stage_activation<FMT, M>(job, kbeg, kend, xlen_pad, xbuf, fx, sx, scratch, cw, lane);
       named_barrier(1, kConsumerWarps * 32);
       cached_job = cur.j;
       cached_split = split;
     }
-    float acc[kRowsPerWarp][M];
+    float acc8[FMT == KQ_Q8_0 ? kRowsPerWarp : 1][M];
+    float acc2[2] = {0.f, 0.f};
 #pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r)
+    for (int r = 0; r < (FMT == KQ_Q8_0 ? kRowsPerWarp : 1); ++r)
 #pragma unroll
-      for (int m = 0; m < M; ++m) acc[r][m] = 0.f;
+      for (int m = 0; m < M; ++m) acc8[r][m] = 0.f;
 
     // After an abort every warp keeps walking the item list (so the named
-    // barriers above stay matched) but waits for and computes nothing.
-    for (int64_t k0 = kbeg; k0 < kend; k0 += job.chunk_k, ++tile) {
-      const int kc = (int)min64(job.chunk_k, kend - k0);
-      const int cbytes = kc / F::kCodesPerByte;
-      const int sp = ((kc / F::kBlock) + 7) & ~7;
+    // barriers stay matched) but waits for and computes nothing.
+    int ci = 0;
+    for (int64_t k0 = kbeg; k0 < kend; k0 += F::kChunk, ++tile, ++ci) {
       const int s = (int)(tile % kStages);
       const uint32_t par = (uint32_t)((tile / kStages) & 1);
       if (*abort_flag) continue;
@@ -457,42 +533,77 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         continue;
       }
       const uint8_t* st = stages + (size_t)s * kStageBytes;
-      const uint16_t* st_scales = reinterpret_cast<const uint16_t*>(st + rows * cbytes);
-      const int xoff = (int)(k0 - kbeg);
-      if (FMT == KQ_Q8_0)
-        q8_0_tile<M>(st, st_scales, kc, sp, rows, xoff, xlen, xbuf, cw, lane, acc);
-      else
-        pq2_0_tile<M>(st, st_scales, kc, sp, rows, xoff, xlen, xbuf, fx, sx, cw, lane, acc);
+      const uint16_t* st_scales = reinterpret_cast<const uint16_t*>(st + kTileCodeBytes);
+      if constexpr (FMT == KQ_Q8_0) {
+        // lanes whose granule lies past k have nothing to do in this chunk
+        if (k0 + (int64_t)(lane + 1) * F::kGran <= kend)
+          q8_0_tile<M>(st, st_scales, rows, ci, xlen_pad, xbuf, cw, lane, acc8);
+      } else {
+        const int nblk_valid = (int)min64(8, (kend - k0) / 128);
+        pq2_0_tile<M>(st, st_scales, rows, ci, nblk_valid, xlen_pad, xbuf, fx, sx, cw, lane, acc2);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
     }
-    if (*abort_flag) continue;
 
-    // fixed-order lane reduction, then one write per (row, m)
-#pragma unroll
-    for (int r = 0; r < kRowsPerWarp; ++r) {
-#pragma unroll
-      for (int m = 0; m < M; ++m) {
-        float v = acc[r][m];
-#pragma unroll
-        for (int mk = 16; mk; mk >>= 1) v += __shfl_xor_sync(0xffffffffu, v, mk);
-        acc[r][m] = v;
-      }
-    }
-    if (lane == 0) {
+    if constexpr (FMT == KQ_Q8_0) {
+      if (*abort_flag) continue;
+      // fixed-order lane reduction, then one write per (row, m)
 #pragma unroll
       for (int r = 0; r < kRowsPerWarp; ++r) {
-        const int row = cw * kRowsPerWarp + r;
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+          float v = acc8[r][m];
+#pragma unroll
+          for (int mk = 16; mk; mk >>= 1) v += __shfl_xor_sync(0xffffffffu, v, mk);
+          acc8[r][m] = v;
+        }
+      }
+      if (lane < kRowsPerWarp) {
+        const int row = cw * kRowsPerWarp + lane;
         if (row < rows) {
+          float v[M];
+#pragma unroll
+          for (int m = 0; m < M; ++m) {
+            v[m] = acc8[0][m];
+#pragma unroll
+            for (int r = 1; r < kRowsPerWarp; ++r)
+              if (lane == r) v[m] = acc8[r][m];
+          }
 #pragma unroll
           for (int m = 0; m < M; ++m) {
             if (job.splits == 1)
-              job.y[(int64_t)m * job.ldy + row0 + row] = acc[r][m];
+              job.y[(int64_t)m * job.ldy + row0 + row] = v[m];
             else
-              job.ws[((int64_t)split * M + m) * job.n + row0 + row] = acc[r][m];
+              job.ws[((int64_t)split * M + m) * job.n + row0 + row] = v[m];
           }
         }
       }
+    } else {
+      // warps cw and cw + 8 hold the two K halves of the same 16 rows: the
+      // second hands its partials over, the first adds them in a fixed order
+      const int slab = cw & 7, kh = cw >> 3;
+      float* cb = combine + slab * 64;
+      if (kh == 1) {
+        cb[2 * lane] = acc2[0];
+        cb[2 * lane + 1] = acc2[1];
+      }
+      named_barrier(2 + slab, 64);
+      if (kh == 0 && !*abort_flag) {
+        const int g = lane >> 2, t = lane & 3;
+        const float yA = acc2[0] + cb[2 * lane], yB = acc2[1] + cb[2 * lane + 1];
+        const int rA = slab * 16 + g, rB = rA + 8;
+        if (t < M) {
+          if (job.splits == 1) {
+            if (rA < rows) job.y[(int64_t)t * job.ldy + row0 + rA] = yA;
+            if (rB < rows) job.y[(int64_t)t * job.ldy + row0 + rB] = yB;
+          } else {
+            if (rA < rows) job.ws[((int64_t)split * M + t) * job.n + row0 + rA] = yA;
+            if (rB < rows) job.ws[((int64_t)split * M + t) * job.n + row0 + rB] = yB;
+          }
+        }
+      }
+      named_barrier(2 + slab, 64);
     }
   }
 }
@@ -513,31 +624,91 @@ __global__ void reduce_splits_kernel(const float* __restrict__ ws, float* __rest
 // Host side
 // ---------------------------------------------------------------------------
 
+static int64_t chunk_of(int fmt) { return fmt == KQ_Q8_0 ? Fmt<KQ_Q8_0>::kChunk : Fmt<KQ_PQ2_0>::kChunk; }
+
 struct Geometry {
-  int32_t splits, split_k, chunk_k, row_groups;
+  int32_t splits, split_k, row_blocks;
 };
 
-static int64_t align_unit(int fmt) { return fmt == KQ_Q8_0 ? Fmt<KQ_Q8_0>::kAlign : Fmt<KQ_PQ2_0>::kAlign; }
-static int64_t chunk_max(int fmt) { return fmt == KQ_Q8_0 ? kStageCodeBytes / kTileRows : kStageCodeBytes / kTileRows * 4; }
-
-// Splits and chunks of one matrix for m activation rows.  requested = 0 means
-// as few splits as the activation staging allows.
-static Geometry make_geometry(int fmt, int64_t n, int64_t k, int64_t m, int requested) {
+// Splits of one matrix for m activation rows.  requested > 0 asks for that
+// many splits (more if the activation staging needs them); requested = 0
+// picks the count that minimises an estimate of the kernel time on `sms`
+// CTAs: tiles of the busiest CTA times the time of a tile, plus the second
+// pass when there is more than one split.
+static Geometry make_geometry(int fmt, int64_t n, int64_t k, int64_t m, int requested, int sms = 0) {
   Geometry g;
-  const int64_t unit = align_unit(fmt);
-  int64_t max_split = std::max<int64_t>(unit, (kXMax / m) / unit * unit);
-  int64_t splits = std::max<int64_t>(requested > 0 ? requested : 1, (k + max_split - 1) / max_split);
-  int64_t split_k = round_up((k + splits - 1) / splits, unit);
-  split_k = std::min(split_k, max_split);
+  const int64_t unit = chunk_of(fmt);
+  const int64_t max_split = std::max<int64_t>(unit, (kXMax / m) / unit * unit);
+  const int64_t min_splits = (k + max_split - 1) / max_split;
+  const int64_t row_blocks = (n + kTileRows - 1) / kTileRows;
+  int64_t splits = std::max<int64_t>(requested > 0 ? requested : 1, min_splits);
+  if (requested == 0 && sms > 0) {
+    const int64_t chunks = (k + unit - 1) / unit;
+    constexpr double kTileUs = 0.75, kReduceUs = 2.5;
+    double best = 1e30;
+    for (int64_t s = min_splits; s <= chunks; ++s) {
+      const int64_t sk = round_up((k + s - 1) / s, unit);
+      if (sk > max_split) continue;
+      const int64_t real = (k + sk - 1) / sk;
+      const int64_t items = row_blocks * real;
+      const double t = (double)((items + sms - 1) / sms) * (double)((sk + unit - 1) / unit) * kTileUs +
+                       (real > 1 ? kReduceUs : 0.0);
+      if (t < best - 1e-9) {
+        best = t;
+        splits = real;
+      }
+    }
+  }
+  int64_t split_k = std::min(round_up((k + splits - 1) / splits, unit), max_split);
   splits = (k + split_k - 1) / split_k;
-  int64_t nchunks = (split_k + chunk_max(fmt) - 1) / chunk_max(fmt);
-  int64_t chunk_k = round_up((split_k + nchunks - 1) / nchunks, unit);
-  chunk_k = std::min(chunk_k, chunk_max(fmt));
   g.splits = (int32_t)splits;
   g.split_k = (int32_t)split_k;
-  g.chunk_k = (int32_t)chunk_k;
-  g.row_groups = (int32_t)((n + kTileRows - 1) / kTileRows);
+  g.row_blocks = (int32_t)row_blocks;
   return g;
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Tensor maps of a matrix's planes, both viewed as 2-D arrays of 32-bit
+// elements: codes [n][k*bits/32], box 64 x 128 (256 bytes of 128 rows) or,
+// for PQ2_0, 32 x 128 with the 128-byte swizzle; scales [n][stride/2], box
+// 4 x 128 (8 fp16 scales of 128 rows).
+static int make_maps(const kq_qmat* W, CUtensorMap* mc, CUtensorMap* ms) {
+  auto fn = encode_fn();
+  if (!fn) return fail(KQ_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is not available from the driver");
+  const int64_t rowbytes = code_row_bytes(W->fmt, W->k);
+  const int64_t sst = scale_stride(W->fmt, W->k);
+  cuuint64_t gdim[2] = {(cuuint64_t)(rowbytes / 4), (cuuint64_t)W->n};
+  cuuint64_t gstride[1] = {(cuuint64_t)rowbytes};
+  // Q8_0: one 256-byte box per tile row; PQ2_0: two 128-byte boxes with the
+  // 128-byte swizzle (the tensor-core consumer reads columns of 8 rows)
+  const bool swz = W->fmt == KQ_PQ2_0;
+  cuuint32_t box[2] = {swz ? 32u : (cuuint32_t)(kChunkBytes / 4), kTileRows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(W->codes), gdim, gstride, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KQ_ERR_CUDA, "tensor map of the codes plane: CUresult %d", (int)r);
+  cuuint64_t sdim[2] = {(cuuint64_t)(sst / 2), (cuuint64_t)W->n};
+  cuuint64_t sstr[1] = {(cuuint64_t)(sst * 2)};
+  cuuint32_t sbox[2] = {4, kTileRows};
+  r = fn(ms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(W->scales), sdim, sstr, sbox, es,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(KQ_ERR_CUDA, "tensor map of the scales plane: CUresult %d", (int)r);
+  return KQ_OK;
 }
 
 static int device_sms(int* sms) {
@@ -550,13 +721,13 @@ static int device_sms(int* sms) {
 
 template <int FMT, int M>
 static int launch_stream(const Params& p, int grid, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(stream_kernel<FMT, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return fail(KQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-    configured = true;
-  }
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(stream_kernel<FMT, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return fail(KQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
   stream_kernel<FMT, M><<<grid, kThreads, kSmemBytes, st>>>(p);
   KQ_CUDA_TRY(cudaGetLastError());
   return KQ_OK;
@@ -584,9 +755,18 @@ static int launch_any(int fmt, int m, const Params& p, int grid, cudaStream_t st
 constexpr int kMaxRowsPerLaunch = 4;
 constexpr int64_t kMaxM = 64;
 
+static int sms_or_default() {
+  int sms = 0;
+  if (device_sms(&sms) != KQ_OK) {
+    clear_error();
+    return 0;
+  }
+  return sms;
+}
+
 static size_t splitk_ws_bytes(const kq_qmat* W, int64_t m, int splits) {
-  int64_t mm = min64(m, kMaxRowsPerLaunch);
-  Geometry g = make_geometry(W->fmt, W->n, W->k, mm, splits);
+  int64_t mm = std::min<int64_t>(m, kMaxRowsPerLaunch);
+  Geometry g = make_geometry(W->fmt, W->n, W->k, mm, splits, splits == 0 ? sms_or_default() : 0);
   return g.splits > 1 ? (size_t)g.splits * (size_t)mm * (size_t)W->n * sizeof(float) : 0;
 }
 
@@ -603,14 +783,17 @@ static int gemm_impl(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, 
   if (need > 0 && !aligned16(d_ws)) return fail(KQ_ERR_ALIGNMENT, "workspace not 16-byte aligned");
   int sms = 0;
   if (int s = device_sms(&sms)) return s;
+  Params p{};
+  if (int s = make_maps(W, &p.map_codes0, &p.map_scales0)) return s;
   cudaStream_t st = (cudaStream_t)stream;
   for (int64_t m0 = 0; m0 < m; m0 += kMaxRowsPerLaunch) {
-    const int mm = (int)min64(kMaxRowsPerLaunch, m - m0);
-    Geometry g = make_geometry(W->fmt, W->n, W->k, mm, splits);
-    Params p{};
+    const int mm = (int)std::min<int64_t>(kMaxRowsPerLaunch, m - m0);
+    Geometry g = make_geometry(W->fmt, W->n, W->k, mm, splits, splits == 0 ? sms : 0);
+    // the staged activation slice (or its B table, 4 bytes per position and
+    // row for PQ2_0) must fit the shared-memory buffer
+    if ((int64_t)mm * g.split_k > kXMax)
+      return fail(KQ_ERR_UNSUPPORTED, "internal: split of %d weights x %d rows exceeds the staging buffer", g.split_k, mm);
     Job& j = p.job0;
-    j.codes = (const uint8_t*)W->codes;
-    j.scales = (const uint16_t*)W->scales;
     j.x = d_X + m0 * W->k;
     j.y = d_Y + m0 * W->n;
     j.ws = (float*)d_ws;
@@ -618,21 +801,19 @@ static int gemm_impl(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, 
     j.k = W->k;
     j.ldy = W->n;
     j.item_begin = 0;
-    j.items = (int64_t)g.row_groups * g.splits;
-    j.sstride = (int32_t)scale_stride(W->fmt, W->k);
-    j.row_groups = g.row_groups;
+    j.items = (int64_t)g.row_blocks * g.splits;
+    j.row_blocks = g.row_blocks;
     j.splits = g.splits;
     j.split_k = g.split_k;
-    j.chunk_k = g.chunk_k;
     p.jobs = nullptr;
+    p.maps = nullptr;
     p.bounds = nullptr;
-    p.njobs = 1;
     p.total_items = j.items;
-    const int grid = (int)min64(j.items, sms);
+    const int grid = (int)std::min<int64_t>(j.items, sms);
     if (int s = launch_any(W->fmt, mm, p, grid, st)) return s;
     if (g.splits > 1) {
       const int64_t tot = (int64_t)mm * W->n;
-      const int rgrid = (int)min64((tot + 255) / 256, (int64_t)sms * 8);
+      const int rgrid = (int)std::min<int64_t>((tot + 255) / 256, (int64_t)sms * 8);
       reduce_splits_kernel<<<rgrid, 256, 0, st>>>((const float*)d_ws, d_Y + m0 * W->n, W->n, W->n, mm, g.splits);
       KQ_CUDA_TRY(cudaGetLastError());
     }
@@ -664,8 +845,8 @@ struct kq_plan {
   int64_t x_floats = 0, y_floats = 0, weight_bytes = 0;
   int grid = 0;
   int64_t total_items = 0;
-  std::vector<kq::Job> host_jobs;
-  kq::Job* d_jobs = nullptr;  // device copy of host_jobs
+  kq::Job* d_jobs = nullptr;
+  CUtensorMap* d_maps = nullptr;
   int64_t* d_bounds = nullptr;
 };
 
@@ -714,50 +895,49 @@ int kq_decode_plan_create(const kq_qmat* mats, int64_t count, kq_plan** out) {
   for (int64_t i = 0; i < count; ++i) {
     if (int s = check_qmat(&mats[i], -1)) return fail(s, "matrix %lld: %s", (long long)i, kq_last_error());
     if (mats[i].fmt != fmt) return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: mixed formats in one plan", (long long)i);
-    if (mats[i].k > kXMax) return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: k = %lld > %d", (long long)i,
-                                       (long long)mats[i].k, kXMax);
+    if (mats[i].k > kXMax)
+      return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: k = %lld > %d", (long long)i, (long long)mats[i].k, kXMax);
   }
   int sms = 0;
   if (int s = device_sms(&sms)) return s;
-  kq_plan* p = new kq_plan();
-  p->fmt = fmt;
-  p->count = count;
+  std::vector<Job> jobs((size_t)count);
+  std::vector<CUtensorMap> maps((size_t)(2 * count));
   std::vector<double> item_bytes;
-  int64_t items = 0;
+  int64_t items = 0, xf = 0, yf = 0, wb = 0;
   for (int64_t i = 0; i < count; ++i) {
     const kq_qmat& W = mats[i];
+    if (int s = make_maps(&W, &maps[(size_t)(2 * i)], &maps[(size_t)(2 * i + 1)])) return s;
     Geometry g = make_geometry(fmt, W.n, W.k, 1, 1);
-    Job j{};
-    j.codes = (const uint8_t*)W.codes;
-    j.scales = (const uint16_t*)W.scales;
-    j.x = nullptr;
-    j.y = nullptr;
-    j.x_off = p->x_floats;
-    j.y_off = p->y_floats;
-    j.ws = nullptr;
+    Job& j = jobs[(size_t)i];
+    j = Job{};
+    j.x_off = xf;
+    j.y_off = yf;
     j.n = W.n;
     j.k = W.k;
     j.ldy = W.n;
     j.item_begin = items;
-    j.items = g.row_groups;
-    j.sstride = (int32_t)scale_stride(fmt, W.k);
-    j.row_groups = g.row_groups;
+    j.items = g.row_blocks;
+    j.row_blocks = g.row_blocks;
     j.splits = 1;
     j.split_k = (int32_t)W.k;
-    j.chunk_k = g.chunk_k;
-    p->host_jobs.push_back(j);
-    const double rb = (double)code_row_bytes(fmt, W.k) + 2.0 * j.sstride;
-    for (int32_t r = 0; r < g.row_groups; ++r)
-      item_bytes.push_back(rb * (double)min64(kTileRows, W.n - (int64_t)r * kTileRows));
-    items += g.row_groups;
-    p->x_floats += W.k;
-    p->y_floats += W.n;
-    p->weight_bytes += kq_codes_bytes(fmt, W.n, W.k) + W.n * (W.k / block_of(fmt)) * 2;
+    const double rb = (double)code_row_bytes(fmt, W.k) + 2.0 * (W.k / block_of(fmt));
+    for (int32_t r = 0; r < g.row_blocks; ++r)
+      item_bytes.push_back(rb * (double)std::min<int64_t>(kTileRows, W.n - (int64_t)r * kTileRows));
+    items += g.row_blocks;
+    xf += W.k;
+    yf += W.n;
+    wb += kq_codes_bytes(fmt, W.n, W.k) + W.n * (W.k / block_of(fmt)) * 2;
   }
+  kq_plan* p = new kq_plan();
+  p->fmt = fmt;
+  p->count = count;
+  p->x_floats = xf;
+  p->y_floats = yf;
+  p->weight_bytes = wb;
   p->total_items = items;
-  p->grid = (int)min64(items, sms);
+  p->grid = (int)std::min<int64_t>(items, sms);
   // byte-balanced contiguous item ranges, one per CTA
-  std::vector<int64_t> bounds(p->grid + 1, items);
+  std::vector<int64_t> bounds((size_t)p->grid + 1, items);
   double total = 0;
   for (double b : item_bytes) total += b;
   bounds[0] = 0;
@@ -765,18 +945,21 @@ int kq_decode_plan_create(const kq_qmat* mats, int64_t count, kq_plan** out) {
   int c = 1;
   for (int64_t it = 0; it < items && c < p->grid; ++it) {
     accum += item_bytes[(size_t)it];
-    while (c < p->grid && accum >= total * c / p->grid) bounds[c++] = it + 1;
+    while (c < p->grid && accum >= total * c / p->grid) bounds[(size_t)c++] = it + 1;
   }
-  for (; c < p->grid; ++c) bounds[c] = items;
-  bounds[p->grid] = items;
+  for (; c < p->grid; ++c) bounds[(size_t)c] = items;
+  bounds[(size_t)p->grid] = items;
   cudaError_t e = cudaMalloc(&p->d_jobs, sizeof(Job) * (size_t)count);
+  if (e == cudaSuccess) e = cudaMalloc(&p->d_maps, sizeof(CUtensorMap) * (size_t)(2 * count));
   if (e == cudaSuccess) e = cudaMalloc(&p->d_bounds, sizeof(int64_t) * (size_t)(p->grid + 1));
+  if (e == cudaSuccess) e = cudaMemcpy(p->d_jobs, jobs.data(), sizeof(Job) * (size_t)count, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(p->d_maps, maps.data(), sizeof(CUtensorMap) * (size_t)(2 * count), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemcpy(p->d_bounds, bounds.data(), sizeof(int64_t) * (size_t)(p->grid + 1), cudaMemcpyHostToDevice);
-  if (e == cudaSuccess)
-    e = cudaMemcpy(p->d_jobs, p->host_jobs.data(), sizeof(Job) * (size_t)count, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) {
     cudaFree(p->d_jobs);
+    cudaFree(p->d_maps);
     cudaFree(p->d_bounds);
     delete p;
     return fail(KQ_ERR_CUDA, "plan allocation: %s", cudaGetErrorString(e));
@@ -807,21 +990,21 @@ int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, vo
   if (!plan) return fail(KQ_ERR_INVALID_ARG, "NULL plan");
   if (!d_x_packed || !d_y_packed) return fail(KQ_ERR_INVALID_ARG, "NULL activation or output");
   if (!aligned16(d_x_packed) || !aligned16(d_y_packed)) return fail(KQ_ERR_ALIGNMENT, "x or y not 16-byte aligned");
-  cudaStream_t st = (cudaStream_t)stream;
   Params p{};
   p.jobs = plan->d_jobs;
+  p.maps = plan->d_maps;
   p.x_base = d_x_packed;
   p.y_base = d_y_packed;
   p.bounds = plan->d_bounds;
-  p.njobs = (int32_t)plan->count;
   p.total_items = plan->total_items;
-  if (plan->fmt == KQ_Q8_0) return launch_stream<KQ_Q8_0, 1>(p, plan->grid, st);
-  return launch_stream<KQ_PQ2_0, 1>(p, plan->grid, st);
+  if (plan->fmt == KQ_Q8_0) return launch_stream<KQ_Q8_0, 1>(p, plan->grid, (cudaStream_t)stream);
+  return launch_stream<KQ_PQ2_0, 1>(p, plan->grid, (cudaStream_t)stream);
 }
 
 void kq_decode_plan_destroy(kq_plan* plan) {
   if (!plan) return;
   cudaFree(plan->d_jobs);
+  cudaFree(plan->d_maps);
   cudaFree(plan->d_bounds);
   delete plan;
 }

@@ -259,7 +259,9 @@ def test_small_m_matches_oracle(kq, wl, fmt, n, k, m):
     W = wl.build_matrix(fmt, n, k, 2, sw)
     X = wl.build_activation(k, 2, sx, rows=m)
     Y = torch.empty(m * n, dtype=torch.float32, device="cuda")
-    kq.kq_gemm_small_m(W, X, m, Y)
+    nbytes = kq.kq_gemv_workspace_bytes(W, m)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
+    kq.kq_gemm_small_m(W, X, m, Y, ws)
     _sync_ok(kq)
     Y = Y.cpu().numpy().reshape(m, n)
     rows = np.arange(n) if n * k <= 50_000_000 else np.unique(np.r_[0, n - 1, np.arange(7, n, 997)])
@@ -303,8 +305,8 @@ def test_decode_plan_small_mixed_shapes(kq, wl):
             _, _, y_ref, absdot = oracle.reference(fmt, w, xh)
             ok, worst = oracle.within_bound(yh[off:off + W.n], y_ref, absdot, TOL)
             assert ok, (fmt, W.n, W.k, worst)
-            # same tile geometry as the single GEMV, so the same bits
-            assert np.array_equal(yh[off:off + W.n], _run_gemv(kq, W, torch.from_numpy(xh).cuda()))
+            # same tiles and one split, as the single GEMV with one split: the same bits
+            assert np.array_equal(yh[off:off + W.n], _run_gemv(kq, W, torch.from_numpy(xh).cuda(), splits=1))
             off += W.n
         y2 = torch.empty_like(y)
         plan.step(x, y2)

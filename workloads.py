@@ -44,10 +44,12 @@ class DecodeWorkload:
     """A decode-step workload: every projection quantized on the device, one
     activation vector per projection packed into x, outputs packed into y."""
 
-    def __init__(self, config, seed=0, device="cuda"):
+    def __init__(self, config, seed=0, device="cuda", limit=None):
         self.config = config
         self.seed = seed
         self.mats_spec = synth.workload(config)
+        if limit:
+            self.mats_spec = self.mats_spec[:limit]
         big = max(n * k for _, _, n, k in self.mats_spec)
         tmp = torch.empty(big, dtype=torch.float32, device=device)
         self.mats = []
