@@ -167,6 +167,28 @@ int kq_gemm_splitk(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, in
                    size_t ws_bytes, void* stream);
 size_t kq_gemm_splitk_workspace_bytes(const kq_qmat* W, int64_t m, int32_t splits);
 
+/* Allocation-free variant of kq_gemm_splitk (no counterpart on the pages; an
+ * addition of this library).  For callers that cannot allocate device
+ * memory where they run the product (allocation-free serving loops, fixed
+ * memory arenas, code that only receives device pointers): the split-K
+ * partial sums go to a scratch array of kq_gemm_splitk_noalloc_max_bytes()
+ * bytes (2 MiB) that the library reserves in device global memory on every
+ * GPU that loads it and keeps until the process exits.  The call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).
+ *  - Same arguments, results and bit-exactness as kq_gemm_splitk with the
+ *    same split count; the caller still passes X and Y.
+ *  - A split plan whose partials need more than the scratch is rejected with
+ *    KQ_ERR_WORKSPACE before anything is enqueued.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture on the device.
+ *  - Every call on a device shares the one array and leaves its partials in
+ *    it; nothing in it has to start at zero (each call writes every partial
+ *    it reads).  Calls that overlap on the GPU (different streams without
+ *    ordering) race on the array: order them on one stream or with events. */
+int kq_gemm_splitk_noalloc(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int32_t splits, void* stream);
+size_t kq_gemm_splitk_noalloc_max_bytes(void);
+
 /* ---- decode-step driver ---------------------------------------------------- */
 
 /* A plan for streaming a whole model's projection list once per step: count

@@ -83,6 +83,8 @@ SIGNATURES = {
     "kq_gemm_small_m": (ctypes.c_int, [_QP, _P, _I64, _P, _P, _SZ, _P]),
     "kq_gemm_splitk": (ctypes.c_int, [_QP, _P, _I64, _P, _I32, _P, _SZ, _P]),
     "kq_gemm_splitk_workspace_bytes": (_SZ, [_QP, _I64, _I32]),
+    "kq_gemm_splitk_noalloc": (ctypes.c_int, [_QP, _P, _I64, _P, _I32, _P]),
+    "kq_gemm_splitk_noalloc_max_bytes": (_SZ, []),
     "kq_decode_plan_create": (ctypes.c_int, [_QP, _I64, ctypes.POINTER(_P)]),
     "kq_decode_plan_sizes": (ctypes.c_int, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "kq_decode_workspace_bytes": (_SZ, [_P]),
@@ -275,6 +277,17 @@ def kq_kernel_binary_version():
     v = ctypes.c_int()
     _check(_lib.kq_kernel_binary_version(ctypes.byref(v)), "kq_kernel_binary_version")
     return v.value
+
+
+def kq_gemm_splitk_noalloc(W, d_X, m, d_Y, splits, stream=None):
+    """Split-K GEMM whose partial sums use the library's static device scratch
+    (no workspace argument, no allocation)."""
+    _check(_lib.kq_gemm_splitk_noalloc(ctypes.byref(W.desc), _ptr(d_X), m, _ptr(d_Y), splits, _stream(stream)),
+           "kq_gemm_splitk_noalloc")
+
+
+def kq_gemm_splitk_noalloc_max_bytes():
+    return _lib.kq_gemm_splitk_noalloc_max_bytes()
 
 
 def kq_device_status(clear=True):

@@ -1009,6 +1009,57 @@ void kq_decode_plan_destroy(kq_plan* plan) {
   delete plan;
 }
 
+// ---------------------------------------------------------------------------
+// Allocation-free split-K GEMM.
+//
+// Some callers cannot call cudaMalloc at the point where they run the
+// product: code that must not allocate after start-up (a real-time serving
+// loop, memory pools that forbid allocations outside their own arena, or
+// callers that only hold device pointers handed to them).  For them the
+// split-K partial sums live in one library-owned array in device global
+// memory, reserved when the library is loaded on a device and kept until the
+// process exits.
+// ---------------------------------------------------------------------------
+static constexpr size_t kNoAllocScratchBytes = 2u << 20;  // 2 MiB per device
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+static std::mutex g_noalloc_mutex;
+static std::vector<void*> g_noalloc_ptr;  // device address of the array, per device (host stand-in resolved once)
+
+static int noalloc_scratch(void** out) {
+  int dev = 0;
+  KQ_CUDA_TRY(cudaGetDevice(&dev));
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if ((int)g_noalloc_ptr.size() <= dev) g_noalloc_ptr.resize((size_t)dev + 1, nullptr);
+  if (g_noalloc_ptr[(size_t)dev] == nullptr) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || ptr == nullptr)
+      return fail(KQ_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
+    g_noalloc_ptr[(size_t)dev] = ptr;
+  }
+  *out = g_noalloc_ptr[(size_t)dev];
+  return KQ_OK;
+}
+
+size_t kq_gemm_splitk_noalloc_max_bytes(void) { return kNoAllocScratchBytes; }
+
+int kq_gemm_splitk_noalloc(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int32_t splits, void* stream) {
+  clear_error();
+  if (int s = check_qmat(W, -1)) return s;
+  if (m < 1 || m > kMaxM) return fail(KQ_ERR_SHAPE, "m = %lld outside [1, %lld]", (long long)m, (long long)kMaxM);
+  if (splits < 0) return fail(KQ_ERR_INVALID_ARG, "splits = %d", splits);
+  const size_t need = splitk_ws_bytes(W, m, splits);
+  if (need > kNoAllocScratchBytes)
+    return fail(KQ_ERR_WORKSPACE,
+                "this split plan needs %zu bytes of scratch; the allocation-free variant has %zu (use kq_gemm_splitk "
+                "with a workspace, or fewer splits)",
+                need, kNoAllocScratchBytes);
+  void* ws = nullptr;
+  if (int s = noalloc_scratch(&ws)) return s;
+  return gemm_impl(W, d_X, m, d_Y, splits, ws, kNoAllocScratchBytes, stream, -1);
+}
+
 int kq_kernel_binary_version(int* version) {
   clear_error();
   if (!version) return fail(KQ_ERR_INVALID_ARG, "NULL pointer");
