@@ -44,6 +44,28 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _traffic(workload):
+    """DRAM bytes per launch of the stream kernel from the committed ncu summary,
+    or None when the kernel source changed since those counters were taken."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", "stream_kernel_traffic.txt")
+    src = os.path.join(ROOT, "quantized_weight_streaming_gb300", "csrc", "kq_stream.cu")
+    try:
+        kv = {}
+        for line in open(path):
+            line = line.split("#", 1)[0].strip()
+            if "=" in line:
+                k, v = (t.strip() for t in line.split("=", 1))
+                kv[k] = v
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if kv.get("source_sha256") != sha:
+            return None
+        return float(kv[workload + ".dram_read_bytes"]) + float(kv[workload + ".dram_write_bytes"])
+    except Exception:
+        return None
+
+
 def _dist():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -127,6 +149,26 @@ def _time_steps(fn, steps, stream):
     return start.elapsed_time(end) / 1e3  # seconds
 
 
+def max_over_ranks(value, device=None):
+    """Largest `value` over all ranks of the default process group (the value
+    itself without one).  Used for the timed seconds: the job is as slow as its
+    slowest replica."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbs(bytes_per_step, steps, seconds_max, world):
+    """Whole-job throughput: every replica streams bytes_per_step per step, the
+    job takes as long as its slowest rank."""
+    return bytes_per_step * steps * world / seconds_max / 1e9
+
+
 def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None, world=1, limit=None):
     import torch
 
@@ -149,11 +191,7 @@ def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None,
     else:
         secs = _time_steps(lambda: W.step(stream), steps, stream)
     if world > 1:
-        import torch.distributed as dist
-
-        t = torch.tensor([secs], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        secs = float(t.item())
+        secs = max_over_ranks(secs, device="cuda")
     if kq.kq_device_status(True) != kq.KQ_OK:
         raise RuntimeError("device status not ok after the timed region")
     per_step = secs / steps
@@ -287,7 +325,7 @@ def run_kq(args):
             gemv.append({key: (round(v, 3) if isinstance(v, float) else v) for key, v in r.items()})
         extras["gemv_graph"] = gemv
     per_gpu_gbs = head["gbs"]
-    value = per_gpu_gbs * world
+    value = aggregate_gbs(head["bytes_per_step"], args.steps, head["seconds"], world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
@@ -313,7 +351,8 @@ def run_kq(args):
         "frac_of_measured_hbm": round(per_gpu_gbs / peak, 4),
         "frac_of_nominal_8tbs": round(per_gpu_gbs / 8000.0, 4),
         "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(per_gpu_gbs / peak, 4), "traffic": args.traffic,
+                     "frac": round(per_gpu_gbs / peak, 4),
+                     "traffic": args.traffic if args.traffic is not None else _traffic(args.workload),
                      "peak_kind": peak_kind, "kernel": "kq::stream_kernel<PQ2_0,1> (one launch per step)"},
         "e2e": {"value": round(head["e2e_gbs"] * world, 2), "unit": "GB/s", "h2d_bytes_per_step": head["h2d_bytes"],
                 "d2h_bytes_per_step": head["d2h_bytes"], "us_per_step": round(head["e2e_per_step_s"] * 1e6, 2)},

@@ -374,35 +374,48 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
   if (slab * 16 >= rows) return;
   const int g = lane >> 2, t = lane & 3;
   const int rA = slab * 16 + g, rB = rA + 8;
-  const uint2* btab = reinterpret_cast<const uint2*>(xbuf);
+  // Rows rA and rB share rA % 8 = g, so the swizzled offset of word t of
+  // chunk c is base + ((c ^ g) << 4): one XOR per chunk serves both rows.
+  const uint8_t* baseA = st_codes + kh * (kTileRows * 128) + rA * 128 + 4 * t;
+  const uint8_t* baseB = baseA + 8 * 128;
+  const int g16 = g << 4;
   const bool has_b = g < 2 * M;
+  // B entries of this thread: block b, group q, MMA j at
+  // btab + ((b * 2 + q) * 4 + j) * (2M * 4) + g * 4 + t
+  const uint2* bthread = reinterpret_cast<const uint2*>(xbuf) + (has_b ? g : 0) * 4 + t;
+  const float* fxm = fx + t * (xlen_pad / 128);
+  const float* sxm = sx + t * (xlen_pad / 128);
 #pragma unroll
   for (int blk = 0; blk < 4; ++blk) {
     const int bt = kh * 4 + blk;  // block inside the tile row
     if (bt >= nblk_valid) break;
     const int b = ci * 8 + bt;  // block inside the staged slice
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
+    const uint2* bb = bthread + b * (2 * 4 * 2 * M * 4);
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const uint32_t wa = *reinterpret_cast<const uint32_t*>(st_codes + swz_code_offset(rA, bt * 32 + 16 * q + 4 * t));
-      const uint32_t wb = *reinterpret_cast<const uint32_t*>(st_codes + swz_code_offset(rB, bt * 32 + 16 * q + 4 * t));
+      const int off = (((2 * blk + q) << 4) ^ g16);
+      const uint32_t wa = *reinterpret_cast<const uint32_t*>(baseA + off);
+      const uint32_t wb = *reinterpret_cast<const uint32_t*>(baseB + off);
       const uint32_t ha = wa >> 4, hb = wb >> 4;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const uint32_t m0 = 0x00030003u << pair_bit(j, 0), m1 = 0x00030003u << pair_bit(j, 1);
         const uint32_t xa = j < 3 ? wa : ha, xb = j < 3 ? wb : hb;
         uint2 bf = make_uint2(0u, 0u);
-        if (has_b) bf = btab[btab_index<M>(b, q, j, g, t)];
-        mma_16816(c, xa & m0, xb & m0, xa & m1, xb & m1, bf.x, bf.y);
+        if (has_b) bf = bb[(q * 4 + j) * (2 * M * 4)];
+        if (q == 0)
+          mma_16816(c0, xa & m0, xb & m0, xa & m1, xb & m1, bf.x, bf.y);
+        else
+          mma_16816(c1, xa & m0, xb & m0, xa & m1, xb & m1, bf.x, bf.y);
       }
     }
     const float dA = __half2float(__ushort_as_half(st_scales[rA * 8 + bt]));
     const float dB = __half2float(__ushort_as_half(st_scales[rB * 8 + bt]));
     if (t < M) {
-      const int gb = t * (xlen_pad / 128) + b;
-      const float F = fx[gb], S = sx[gb];
-      acc[0] = fmaf(dA, fmaf(F, c[0] + c[1], -S), acc[0]);
-      acc[1] = fmaf(dB, fmaf(F, c[2] + c[3], -S), acc[1]);
+      const float F = fxm[b], S = sxm[b];
+      acc[0] = fmaf(dA, fmaf(F, (c0[0] + c0[1]) + (c1[0] + c1[1]), -S), acc[0]);
+      acc[1] = fmaf(dB, fmaf(F, (c0[2] + c0[3]) + (c1[2] + c1[3]), -S), acc[1]);
     }
   }
 }
