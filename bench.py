@@ -278,8 +278,13 @@ def _gemv_graph_measure(kq, wl_mod, fmt, n, k, m, stream, replays=20):
     torch.cuda.synchronize()
     per_launch = start.elapsed_time(end) / 1e3 / (replays * len(mats))
     nbytes = W0.weight_bytes + 4 * m * (k + n)
-    out = {"fmt": fmt, "n": n, "k": k, "m": m, "us_per_call": per_launch * 1e6, "gbs": nbytes / per_launch / 1e9,
-           "copies": copies, "launches_per_call": 1 + (1 if nb else 0)}
+    if m >= 16:  # kq_gemm_small_m runs the tensor-core GEMM: prologue, GEMM, split second pass
+        split = kq.kq_gemm_tc_workspace_bytes(W0, m, 0) > kq.kq_gemm_tc_workspace_bytes(W0, m, 1)
+        path, launches = "tcgen05", 2 + (1 if split else 0)
+    else:
+        path, launches = "stream", ((m + 3) // 4) * (1 + (1 if nb else 0))
+    out = {"fmt": fmt, "n": n, "k": k, "m": m, "path": path, "us_per_call": per_launch * 1e6,
+           "gbs": nbytes / per_launch / 1e9, "copies": copies, "launches_per_call": launches}
     if m > 1:
         out["tflops"] = 2.0 * m * n * k / per_launch / 1e12
     del g, mats

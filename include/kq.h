@@ -155,9 +155,35 @@ int kq_gemv_q8_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, siz
 int kq_gemv_pq2_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
 
 /* Y[m][n] = X[m][k] W^T (rotated per row for PQ2_0), X and Y row-major fp32,
- * 1 <= m <= 64. */
+ * 1 <= m <= 64.  From m = 16 on (and k <= 32768) this is kq_gemm_tc with an
+ * automatic split; below, the streaming kernel applies each weight tile to
+ * up to 4 activation rows per pass.  kq_gemv_workspace_bytes(W, m) sizes the
+ * workspace of either. */
 int kq_gemm_small_m(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, void* d_ws, size_t ws_bytes,
                     void* stream);
+
+/* Small-batch GEMM on the tensor cores (tcgen05), the batched path of
+ * "Kipp Benchmarks" (tensor matmul section: each K block dequantized into a
+ * 16-bit tile, then multiplied): Y[m][n] = X[m][k] W^T, X rotated per
+ * 128-block for PQ2_0 (unrotated X in, as for kq_gemv_pq2_0).
+ *  - 1 <= m <= 64, k <= 32768; X, Y row-major fp32, 16-byte aligned.
+ *  - Weights enter the tensor core as fp16 tiles: (c-1)*d exactly for PQ2_0;
+ *    for Q8_0 as fp16(q*d) plus the residual q*d - fp16(q*d) (exact but for
+ *    fp16 subnormals: absolute error <= 2^-25 per weight).  Each activation
+ *    row enters as two fp16 rows, high and low part of x * 2^-e (e its
+ *    largest exponent), so x keeps ~22 bits; fp32 accumulation.  A Q8_0
+ *    scale above 65504/127 (q*d not a finite fp16) sets KQ_ERR_RANGE.
+ *  - splits: K splits (0 = automatic); with splits > 1 the partial sums are
+ *    added in split order by a second pass (deterministic).
+ *  - Workspace (kq_gemm_tc_workspace_bytes, 16-byte aligned): the fp16
+ *    activation matrix (4 * round16(m) * k bytes), per-row exponents and the
+ *    split partials; everything in it is written before it is read.
+ *  - Errors: KQ_ERR_SHAPE (m or k out of range), KQ_ERR_WORKSPACE,
+ *    KQ_ERR_ALIGNMENT, KQ_ERR_CUDA; a bounded device wait that expires sets
+ *    KQ_ERR_TIMEOUT for kq_device_status. */
+int kq_gemm_tc(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int32_t splits, void* d_ws,
+               size_t ws_bytes, void* stream);
+size_t kq_gemm_tc_workspace_bytes(const kq_qmat* W, int64_t m, int32_t splits);
 
 /* GEMV/GEMM with an explicit split-K factor (1 = no split; 0 = automatic).
  * Splits are whole multiples of 1024 weights along K; the partial sums of

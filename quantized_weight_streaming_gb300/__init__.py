@@ -81,6 +81,8 @@ SIGNATURES = {
     "kq_gemv_q8_0": (ctypes.c_int, [_QP, _P, _P, _P, _SZ, _P]),
     "kq_gemv_pq2_0": (ctypes.c_int, [_QP, _P, _P, _P, _SZ, _P]),
     "kq_gemm_small_m": (ctypes.c_int, [_QP, _P, _I64, _P, _P, _SZ, _P]),
+    "kq_gemm_tc": (ctypes.c_int, [_QP, _P, _I64, _P, _I32, _P, _SZ, _P]),
+    "kq_gemm_tc_workspace_bytes": (_SZ, [_QP, _I64, _I32]),
     "kq_gemm_splitk": (ctypes.c_int, [_QP, _P, _I64, _P, _I32, _P, _SZ, _P]),
     "kq_gemm_splitk_workspace_bytes": (_SZ, [_QP, _I64, _I32]),
     "kq_gemm_splitk_noalloc": (ctypes.c_int, [_QP, _P, _I64, _P, _I32, _P]),
@@ -265,6 +267,17 @@ def kq_gemm_small_m(W, d_X, m, d_Y, ws=None, stream=None):
     p, nb = _ws(ws)
     _check(_lib.kq_gemm_small_m(ctypes.byref(W.desc), _ptr(d_X), m, _ptr(d_Y), p, nb, _stream(stream)),
            "kq_gemm_small_m")
+
+
+def kq_gemm_tc_workspace_bytes(W, m, splits=0):
+    return _lib.kq_gemm_tc_workspace_bytes(ctypes.byref(W.desc), m, splits)
+
+
+def kq_gemm_tc(W, d_X, m, d_Y, splits=0, ws=None, stream=None):
+    """Small-batch GEMM on the tensor cores (tcgen05)."""
+    p, nb = _ws(ws)
+    _check(_lib.kq_gemm_tc(ctypes.byref(W.desc), _ptr(d_X), m, _ptr(d_Y), splits, p, nb, _stream(stream)),
+           "kq_gemm_tc")
 
 
 def kq_gemm_splitk(W, d_X, m, d_Y, splits, ws=None, stream=None):

@@ -49,6 +49,7 @@
 
 #include "kq_device.cuh"
 #include "kq_internal.h"
+#include "kq_tc.h"
 
 namespace kq {
 
@@ -867,8 +868,13 @@ using namespace kq;
 
 extern "C" {
 
+// kq_gemm_small_m runs on the tensor cores from kTcMinM activation rows on
+// (when k fits the tensor-core prologue), else on the streaming kernel.
+static bool small_m_uses_tc(const kq_qmat* W, int64_t m) { return m >= kTcMinM && m <= kTcMaxM && W->k <= kTcMaxK; }
+
 size_t kq_gemv_workspace_bytes(const kq_qmat* W, int64_t m) {
   if (check_qmat(W, -1) != KQ_OK || m < 1) return 0;
+  if (small_m_uses_tc(W, m)) return tc_workspace_bytes(W, m, 0);
   return splitk_ws_bytes(W, m, 0);
 }
 
@@ -890,7 +896,25 @@ int kq_gemv_pq2_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, si
 int kq_gemm_small_m(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, void* d_ws, size_t ws_bytes,
                     void* stream) {
   clear_error();
+  if (int s = check_qmat(W, -1)) return s;
+  if (small_m_uses_tc(W, m)) return tc_gemm(W, d_X, m, d_Y, 0, d_ws, ws_bytes, stream);
   return gemm_impl(W, d_X, m, d_Y, 0, d_ws, ws_bytes, stream, -1);
+}
+
+size_t kq_gemm_tc_workspace_bytes(const kq_qmat* W, int64_t m, int32_t splits) {
+  if (check_qmat(W, -1) != KQ_OK || splits < 0 || tc_check(W, m) != KQ_OK) {
+    clear_error();
+    return 0;
+  }
+  return tc_workspace_bytes(W, m, splits);
+}
+
+int kq_gemm_tc(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int32_t splits, void* d_ws,
+               size_t ws_bytes, void* stream) {
+  clear_error();
+  if (int s = check_qmat(W, -1)) return s;
+  if (splits < 0) return fail(KQ_ERR_INVALID_ARG, "splits = %d", splits);
+  return tc_gemm(W, d_X, m, d_Y, splits, d_ws, ws_bytes, stream);
 }
 
 int kq_gemm_splitk(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int32_t splits, void* d_ws,
@@ -1085,9 +1109,9 @@ int kq_kernel_binary_version(int* version) {
 int kq_device_status(int clear) {
   clear_error();
   KQ_CUDA_TRY(cudaDeviceSynchronize());
-  int a = read_stream_status(clear), b = read_prep_status(clear);
-  if (a < 0 || b < 0) return fail(KQ_ERR_CUDA, "reading the device status word failed");
-  const unsigned v = (unsigned)a | (unsigned)b;
+  int a = read_stream_status(clear), b = read_prep_status(clear), c = read_tc_status(clear);
+  if (a < 0 || b < 0 || c < 0) return fail(KQ_ERR_CUDA, "reading the device status word failed");
+  const unsigned v = (unsigned)a | (unsigned)b | (unsigned)c;
   if (v & (1u << KQ_ERR_TIMEOUT)) return fail(KQ_ERR_TIMEOUT, "a bounded device wait expired");
   if (v & (1u << KQ_ERR_NONFINITE)) return fail(KQ_ERR_NONFINITE, "non-finite weight met on the device");
   if (v & (1u << KQ_ERR_RANGE)) return fail(KQ_ERR_RANGE, "scale overflowed fp16 on the device");

@@ -127,6 +127,15 @@ def test_device_entry_points_validate_before_any_cuda_call(kq):
     assert lib.kq_gemm_small_m(ctypes.byref(good), A, 65, A, None, 0, None) == kq.KQ_ERR_SHAPE
     assert lib.kq_gemm_small_m(ctypes.byref(good), A, 0, A, None, 0, None) == kq.KQ_ERR_SHAPE
     assert lib.kq_gemm_splitk(ctypes.byref(good), A, 1, A, -1, None, 0, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_gemm_tc(ctypes.byref(good), A, 65, A, 0, None, 0, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_gemm_tc(ctypes.byref(good), A, 0, A, 0, None, 0, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_gemm_tc(ctypes.byref(good), A, 16, A, -1, None, 0, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_gemm_tc(ctypes.byref(good), None, 16, A, 0, None, 0, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_gemm_tc(ctypes.byref(good), A + 4, 16, A, 0, None, 0, None) == kq.KQ_ERR_ALIGNMENT
+    wide = kq.kq_qmat(kq.KQ_Q8_0, 0, 8, 32800, A, A)
+    assert lib.kq_gemm_tc(ctypes.byref(wide), A, 16, A, 0, None, 0, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_gemm_tc(ctypes.byref(bad_k), A, 16, A, 0, None, 0, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_gemm_tc_workspace_bytes(ctypes.byref(good), 65, 0) == 0
     assert lib.kq_gemv_q8_0(None, A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
     assert lib.kq_dequantize(ctypes.byref(bad_k), A, None) == kq.KQ_ERR_SHAPE
     assert lib.kq_hadamard_blockwise(A, A, 1, 100, 128, None) == kq.KQ_ERR_SHAPE

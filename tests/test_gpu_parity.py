@@ -280,6 +280,117 @@ def test_small_m_matches_oracle(kq, wl, fmt, n, k, m):
 
 
 # ----------------------------------------------------------------------------
+# small-M GEMM on the tensor cores (tcgen05)
+# ----------------------------------------------------------------------------
+
+def _small_m_reference(fmt, n, k, m, seed, sw, sx, rows):
+    """Oracle dequantized rows and (rotated for PQ2_0) FP64 activations."""
+    w = synth.matrix_rows_host(n, k, rows, seed, sw)
+    Xh = synth.fill_host("x", m * k, seed, sx).reshape(m, k)
+    if fmt == "pq2_0":
+        deq = oracle.pq2_0_dequant(oracle.pq2_0_quantize(oracle.rotate_rows(w)[1]), rows.size, k)
+        X64 = oracle.rotate_rows(Xh)[0]
+    else:
+        deq = oracle.q8_0_dequant(oracle.q8_0_quantize(w), rows.size, k)
+        X64 = Xh.astype(np.float64)
+    return deq, X64
+
+
+def _run_tc(kq, W, X, m, splits):
+    Y = torch.full((m * W.n,), 7.0, dtype=torch.float32, device="cuda")
+    nbytes = kq.kq_gemm_tc_workspace_bytes(W, m, splits)
+    assert nbytes > 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    kq.kq_gemm_tc(W, X, m, Y, splits, ws)
+    _sync_ok(kq)
+    return Y.cpu().numpy().reshape(m, W.n)
+
+
+@pytest.mark.parametrize("fmt,n,k", [("q8_0", 300, 2080), ("pq2_0", 200, 1152), ("q8_0", 128, 128),
+                                     ("pq2_0", 1, 128), ("q8_0", 1000, 4096), ("pq2_0", 520, 5120)])
+@pytest.mark.parametrize("m", [1, 5, 16, 33, 64])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_tc_gemm_matches_oracle(kq, wl, fmt, n, k, m, splits):
+    # ragged row tiles (n % 128), a ragged last K chunk (Q8_0 k = 2080), M not a
+    # multiple of 8, forced and automatic K splits
+    sw, sx = synth.stream_id("test", 0, 340), synth.stream_id("test", 1, 340 + m)
+    W = wl.build_matrix(fmt, n, k, 4, sw)
+    X = wl.build_activation(k, 4, sx, rows=m)
+    Y = _run_tc(kq, W, X, m, splits)
+    rows = np.arange(n)
+    deq, X64 = _small_m_reference(fmt, n, k, m, 4, sw, sx, rows)
+    for i in range(m):
+        y_ref, absdot = oracle.gemv(deq, X64[i])
+        ok, worst = oracle.within_bound(Y[i], y_ref, absdot, TOL)
+        assert ok, (i, worst)
+    # same plan, same bits
+    assert np.array_equal(_run_tc(kq, W, X, m, splits), Y)
+
+
+def test_tc_q8_0_exact_integer_case_tolerance_zero(kq):
+    # power-of-two scales make fp16(q*d) exact, small integer activations make
+    # the high part exact and the low part zero, and every partial sum is an
+    # exact fp32 value: the tensor-core result must equal the exact product,
+    # which pins the tile layouts (any transposed, permuted or shifted operand
+    # changes it)
+    rng = np.random.default_rng(12)
+    n, k, m = 200, 2848, 16
+    q = rng.integers(-127, 128, size=(n, k))
+    q[:, ::32] = 127
+    w = (q * 2.0**-5).astype(np.float32)
+    X = rng.integers(-8, 9, size=(m, k)).astype(np.float32)
+    X[3] = 0.0  # an all-zero activation row
+    blocks = oracle.q8_0_quantize(w)
+    W = kq.QMatrix("q8_0", n, k)
+    kq.kq_prepare(W, torch.from_numpy(blocks.reshape(-1)).cuda())
+    for splits in (1, 0, 5):
+        Y = _run_tc(kq, W, torch.from_numpy(X.reshape(-1)).cuda(), m, splits)
+        assert np.array_equal(Y.astype(np.float64), (X.astype(np.int64) @ q.T) * 2.0**-5), splits
+
+
+def test_tc_pq2_0_single_weight_rows_pin_the_pairing(kq):
+    # row r holds one nonzero ternary weight, at column r (all other codes 1,
+    # value 0): y[r] = +-d x'[r], so a wrong code pairing, B permutation or
+    # positional scale moves or rescales the weight and fails.  The rotated
+    # activations x' are integers of magnitude 16..64 (x = R x' in FP64,
+    # rounded to fp32), so no x'[r] is near zero.
+    n, k, m = 128, 256, 16
+    d = 2.0**-3
+    blocks = np.zeros((n, k // 128, 34), dtype=np.uint8)
+    dbits = np.array([d], dtype=np.float16).view(np.uint16)[0]
+    blocks[:, :, 0] = dbits & 0xFF
+    blocks[:, :, 1] = dbits >> 8
+    codes = np.ones((n, k), dtype=np.uint8)
+    for r in range(n):
+        codes[r, r] = 2 if r % 3 else 0
+    for j in range(k):
+        blocks[:, j // 128, 2 + (j % 128) // 4] |= (codes[:, j] << (2 * (j % 4))).astype(np.uint8)
+    W = kq.QMatrix("pq2_0", n, k)
+    kq.kq_prepare(W, torch.from_numpy(blocks.reshape(-1)).cuda())
+    rng = np.random.default_rng(13)
+    xr = (rng.integers(16, 65, size=(m, k)) * rng.choice([-1, 1], size=(m, k))).astype(np.float32)
+    X = oracle.rotate_rows(xr)[1]  # R is its own inverse
+    Y = _run_tc(kq, W, torch.from_numpy(X.reshape(-1)).cuda(), m, 1)
+    Xr = oracle.rotate_rows(X)[0]
+    sign = codes[np.arange(n), np.arange(n)].astype(np.float64) - 1
+    expect = Xr[:, :n] * d * sign
+    assert np.all(np.abs(Y - expect) <= TOL * np.abs(expect))
+
+
+def test_tc_workspace_too_small_is_rejected(kq, wl):
+    W = wl.build_matrix("q8_0", 256, 1024, 0, synth.stream_id("test", 0, 341))
+    X = wl.build_activation(1024, 0, synth.stream_id("test", 1, 341), rows=16)
+    Y = torch.full((16 * 256,), 7.0, dtype=torch.float32, device="cuda")
+    need = kq.kq_gemm_tc_workspace_bytes(W, 16, 2)
+    ws = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kq.KQError) as e:
+        kq.kq_gemm_tc(W, X, 16, Y, 2, ws)
+    assert e.value.status == kq.KQ_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.all(Y == 7.0)
+
+
+# ----------------------------------------------------------------------------
 # decode-step driver
 # ----------------------------------------------------------------------------
 
