@@ -44,11 +44,18 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def _traffic(workload):
-    """DRAM bytes per launch of the stream kernel from the committed ncu summary,
-    or None when the kernel source changed since those counters were taken."""
+def source_code_sha256(path):
+    """sha256 of a source file's code: every line, stripped, except empty
+    lines and whole-line // comments, so that comment edits keep it."""
     import hashlib
 
+    keep = [ln.strip() for ln in open(path, encoding="utf-8") if ln.strip() and not ln.strip().startswith("//")]
+    return hashlib.sha256("\n".join(keep).encode()).hexdigest()
+
+
+def _traffic(workload):
+    """DRAM bytes per launch of the stream kernel from the committed ncu summary,
+    or None when the kernel code changed since those counters were taken."""
     path = os.path.join(ROOT, "profiles", "stream_kernel_traffic.txt")
     src = os.path.join(ROOT, "quantized_weight_streaming_gb300", "csrc", "kq_stream.cu")
     try:
@@ -58,8 +65,7 @@ def _traffic(workload):
             if "=" in line:
                 k, v = (t.strip() for t in line.split("=", 1))
                 kv[k] = v
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if kv.get("source_sha256") != sha:
+        if kv.get("source_code_sha256") != source_code_sha256(src):
             return None
         return float(kv[workload + ".dram_read_bytes"]) + float(kv[workload + ".dram_write_bytes"])
     except Exception:

@@ -16,24 +16,26 @@
 //  * Work is a list of items (matrix, 128-row block, K split).  Each CTA owns
 //    a contiguous run of items, so it changes matrices rarely; an item walks
 //    its K range one 256-byte chunk (one tile) at a time.
-//  * Consumer warp w owns rows 8w..8w+7 of every tile and lane l the l-th
-//    8-byte granule of each row (8 Q8_0 or 32 PQ2_0 weights): eight
-//    independent FMA chains per lane, the granule's activations loaded once
-//    (conflict-free 16-byte loads from a swizzled layout) and reused by the
-//    eight rows, per-row sums kept in registers across the item's tiles.
+//  * Q8_0 consumers: warp w owns rows 8w..8w+7 of every tile and lane l the
+//    l-th 8-byte granule of each row (8 weights), the granule's activations
+//    loaded once (conflict-free 16-byte loads from a swizzled layout) and
+//    reused by the eight rows.  The int8 code becomes an fp32 integer by a
+//    byte permute into the mantissa of 2^23 and one subtract; rows go in
+//    pairs through the fp32 pair instructions (FADD2 / FFMA2), so one
+//    instruction converts or multiplies the codes of two rows.
 //  * When a CTA starts an item of a new (matrix, split), its consumers stage
 //    the activation slice in shared memory.  For PQ2_0 this prologue applies
 //    the blockwise normalised Walsh-Hadamard transform (x' = R x, "Bonsai 2
 //    27B - ternary g128 + blockwise Hadamard", section 4.2) in registers and
 //    warp shuffles, fused into the load.
-//  * Q8_0 dot: sum_b d_b sum_j q_j x_j with the int8 code turned into an fp32
-//    integer by a byte permute into the mantissa of 2^23 and one subtract.
-//  * PQ2_0 dot: sum_b d_b (sum_j c_j x'_j - sum_j x'_j) with c in {0,1,2}
-//    (the ternary value is c-1; the -1 is folded into a precomputed
-//    activation sum, as the Bonsai page, section 8.5, does on Metal).  A 2-bit
-//    code masked in place inside its 32-bit word IS an fp32 denormal
-//    c * 4^j * 2^-149, so one AND per code produces the FMA operand; the
-//    activation is pre-scaled by the matching power of two in the prologue.
+//  * PQ2_0 consumers run on the tensor cores (mma.sync m16n8k16, fp16 in,
+//    fp32 accumulate): warp w owns 32 rows (two 16-row slabs) and a quarter
+//    of the tile's K, so each B fragment it loads serves both slabs.  A
+//    2-bit code masked in place inside its 32-bit word is the exact fp16
+//    subnormal c * 2^(s-24): one AND per two codes builds an A register.  B
+//    holds x' as an fp16 high/low pair scaled per block by 2^(14-s-E); the
+//    ternary -1 is folded into a precomputed per-block activation sum, as
+//    the Bonsai page, section 8.5, does on Metal: y += d (2^(10+E) C - sum x').
 //  * Each output is reduced across lanes with shuffles in a fixed order; with
 //    K splits, partials land in the workspace and a second pass adds them in
 //    split order.  Results never depend on the grid size.
@@ -66,7 +68,7 @@ constexpr int kStages = 4;
 constexpr int kXMax = 18432;          // activation floats (or B-fragment words) staged per item (all m)
 constexpr int kBlkMax = kXMax / 128;  // PQ2_0 per-block side arrays
 constexpr int kScratchFloats = 128;   // per-warp scratch (one Hadamard block)
-constexpr int kCombineFloats = 8 * 64;  // K-half partials handed between paired warps
+constexpr int kCombineFloats = 4 * 3 * 32 * 4;  // K-quarter partials handed to the first warp of each slab pair
 constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kXMax * 4 + 2 * (size_t)kBlkMax * 4 +
                               (size_t)kConsumerWarps * kScratchFloats * 4 + (size_t)kCombineFloats * 4 +
                               2 * kStages * 8 + 16;
@@ -330,93 +332,117 @@ __device__ __forceinline__ void q8_0_tile(const uint8_t* st_codes, const uint16_
     xa[m] = xp[0];
     xb[m] = xp[32];
   }
+  // rows in pairs: the fp32 pair instructions (FADD2 / FFMA2) convert and
+  // multiply the codes of two rows against the same activations at once
 #pragma unroll
-  for (int r = 0; r < kRowsPerWarp; ++r) {
+  for (int r = 0; r < kRowsPerWarp; r += 2) {
     const int row = cw * kRowsPerWarp + r;
     if (row >= rows) break;
-    const uint2 c = *reinterpret_cast<const uint2*>(st_codes + row * kChunkBytes + lane * 8);
-    const float d = __half2float(__ushort_as_half(st_scales[row * 8 + lane / 4]));
-    const uint32_t u0 = c.x ^ 0x80808080u, u1 = c.y ^ 0x80808080u;
-    constexpr float kMagic = 8388736.0f;  // 2^23 + 128
-    float q[8];
-    q[0] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7540)) - kMagic;
-    q[1] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7541)) - kMagic;
-    q[2] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7542)) - kMagic;
-    q[3] = __int_as_float(__byte_perm(u0, 0x4B000000u, 0x7543)) - kMagic;
-    q[4] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7540)) - kMagic;
-    q[5] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7541)) - kMagic;
-    q[6] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7542)) - kMagic;
-    q[7] = __int_as_float(__byte_perm(u1, 0x4B000000u, 0x7543)) - kMagic;
+    const uint2 c0 = *reinterpret_cast<const uint2*>(st_codes + row * kChunkBytes + lane * 8);
+    const uint2 c1 = *reinterpret_cast<const uint2*>(st_codes + (row + 1) * kChunkBytes + lane * 8);
+    const float2 d2 = make_float2(__half2float(__ushort_as_half(st_scales[row * 8 + lane / 4])),
+                                  __half2float(__ushort_as_half(st_scales[(row + 1) * 8 + lane / 4])));
+    const uint32_t u[2][2] = {{c0.x ^ 0x80808080u, c0.y ^ 0x80808080u}, {c1.x ^ 0x80808080u, c1.y ^ 0x80808080u}};
+    const float2 kMagic2 = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+    float2 q[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const uint32_t sel = 0x7540u + (uint32_t)(e & 3);
+      q[e] = __fadd2_rn(make_float2(__int_as_float(__byte_perm(u[0][e >> 2], 0x4B000000u, sel)),
+                                    __int_as_float(__byte_perm(u[1][e >> 2], 0x4B000000u, sel))),
+                        kMagic2);
+    }
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-      float p = q[0] * xa[m].x;
-      p = fmaf(q[1], xa[m].y, p);
-      p = fmaf(q[2], xa[m].z, p);
-      p = fmaf(q[3], xa[m].w, p);
-      p = fmaf(q[4], xb[m].x, p);
-      p = fmaf(q[5], xb[m].y, p);
-      p = fmaf(q[6], xb[m].z, p);
-      p = fmaf(q[7], xb[m].w, p);
-      acc[r][m] = fmaf(d, p, acc[r][m]);
+      const float xv[8] = {xa[m].x, xa[m].y, xa[m].z, xa[m].w, xb[m].x, xb[m].y, xb[m].z, xb[m].w};
+      float2 p = __fmul2_rn(q[0], make_float2(xv[0], xv[0]));
+#pragma unroll
+      for (int e = 1; e < 8; ++e) p = __ffma2_rn(q[e], make_float2(xv[e], xv[e]), p);
+      const float2 a = __ffma2_rn(d2, p, make_float2(acc[r][m], acc[r + 1][m]));
+      acc[r][m] = a.x;
+      acc[r + 1][m] = a.y;
     }
   }
 }
 
 // ---------------------------------------------------------------------------
-// PQ2_0 consumer math for one tile: warp cw takes the 16-row slab cw % 8 and
-// the K half cw / 8 (4 blocks, 512 codes per row).  acc[0] / acc[1] are the
-// partial outputs of rows g and g+8 for activation row m = t.
+// PQ2_0 consumer math for one tile: warp cw takes the 32 rows of slab pair
+// cw % 4 (two 16-row slabs) and the K quarter cw / 4 (2 blocks, 256 codes
+// per row), so every B fragment it loads serves both slabs and its 16 MMAs
+// per block form four independent chains.  acc[s][0] / acc[s][1] are the
+// partial outputs of rows g and g+8 of slab s for activation row m = t.
 // ---------------------------------------------------------------------------
 template <int M>
 __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16_t* st_scales, int rows, int ci,
-                                           int nblk_valid, int xlen_pad, const float* xbuf, const float* fx,
-                                           const float* sx, int cw, int lane, float (&acc)[2]) {
-  const int slab = cw & 7, kh = cw >> 3;
-  if (slab * 16 >= rows) return;
+                                           int nblk_valid, const float* xbuf, const float* fx, const float* sx,
+                                           int xlen_pad, int cw, int lane, float (&acc)[2][2]) {
+  const int sp = cw & 3, kq = cw >> 2;
+  if (sp * 32 >= rows) return;
   const int g = lane >> 2, t = lane & 3;
-  const int rA = slab * 16 + g, rB = rA + 8;
-  // Rows rA and rB share rA % 8 = g, so the swizzled offset of word t of
-  // chunk c is base + ((c ^ g) << 4): one XOR per chunk serves both rows.
-  const uint8_t* baseA = st_codes + kh * (kTileRows * 128) + rA * 128 + 4 * t;
-  const uint8_t* baseB = baseA + 8 * 128;
+  const int kh = kq >> 1;  // 128-byte half box holding this quarter
+  // Rows g, g+8 of both slabs share r % 8 = g, so the swizzled offset of word
+  // t of chunk c is base + ((c ^ g) << 4) for all four rows.
+  const uint8_t* base = st_codes + kh * (kTileRows * 128) + (sp * 32 + g) * 128 + 4 * t;
   const int g16 = g << 4;
   const bool has_b = g < 2 * M;
-  // B entries of this thread: block b, group q, MMA j at
-  // btab + ((b * 2 + q) * 4 + j) * (2M * 4) + g * 4 + t
   const uint2* bthread = reinterpret_cast<const uint2*>(xbuf) + (has_b ? g : 0) * 4 + t;
-  const float* fxm = fx + t * (xlen_pad / 128);
-  const float* sxm = sx + t * (xlen_pad / 128);
+  // the tile's two block scales of the four rows (fp16 pairs), and the two
+  // blocks' activation factors and sums
+  const int bt0 = 2 * kq;  // first block of the quarter inside the tile row
+  uint32_t dpair[2][2];
 #pragma unroll
-  for (int blk = 0; blk < 4; ++blk) {
-    const int bt = kh * 4 + blk;  // block inside the tile row
-    if (bt >= nblk_valid) break;
-    const int b = ci * 8 + bt;  // block inside the staged slice
-    const uint2* bb = bthread + b * (2 * 4 * 2 * M * 4);
-    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int s2 = 0; s2 < 2; ++s2) {
+    const int rA = sp * 32 + s2 * 16 + g;
+    dpair[s2][0] = *reinterpret_cast<const uint32_t*>(st_scales + rA * 8 + bt0);
+    dpair[s2][1] = *reinterpret_cast<const uint32_t*>(st_scales + (rA + 8) * 8 + bt0);
+  }
+  const int b0 = ci * 8 + bt0;  // first block inside the staged slice
+  const int tm = t < M ? t : 0;  // lanes t >= M hold no activation row
+  const float2 F2 = *reinterpret_cast<const float2*>(fx + tm * (xlen_pad / 128) + b0);
+  const float2 S2 = *reinterpret_cast<const float2*>(sx + tm * (xlen_pad / 128) + b0);
+#pragma unroll
+  for (int bl = 0; bl < 2; ++bl) {
+    if (bt0 + bl >= nblk_valid) break;
+    const uint2* bb = bthread + (b0 + bl) * (2 * 4 * 2 * M * 4);
+    float c[2][2][4];
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2)
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) c[s2][q][e] = 0.f;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const int off = (((2 * blk + q) << 4) ^ g16);
-      const uint32_t wa = *reinterpret_cast<const uint32_t*>(baseA + off);
-      const uint32_t wb = *reinterpret_cast<const uint32_t*>(baseB + off);
-      const uint32_t ha = wa >> 4, hb = wb >> 4;
+      const int off = ((((kq & 1) * 4 + 2 * bl + q) << 4) ^ g16);
+      uint32_t w[2][2];
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        w[s2][0] = *reinterpret_cast<const uint32_t*>(base + s2 * (16 * 128) + off);
+        w[s2][1] = *reinterpret_cast<const uint32_t*>(base + s2 * (16 * 128) + 8 * 128 + off);
+      }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const uint32_t m0 = 0x00030003u << pair_bit(j, 0), m1 = 0x00030003u << pair_bit(j, 1);
-        const uint32_t xa = j < 3 ? wa : ha, xb = j < 3 ? wb : hb;
         uint2 bf = make_uint2(0u, 0u);
         if (has_b) bf = bb[(q * 4 + j) * (2 * M * 4)];
-        if (q == 0)
-          mma_16816(c0, xa & m0, xb & m0, xa & m1, xb & m1, bf.x, bf.y);
-        else
-          mma_16816(c1, xa & m0, xb & m0, xa & m1, xb & m1, bf.x, bf.y);
+        const uint32_t m0 = 0x00030003u << pair_bit(j, 0), m1 = 0x00030003u << pair_bit(j, 1);
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          const uint32_t xa = j < 3 ? w[s2][0] : w[s2][0] >> 4, xb = j < 3 ? w[s2][1] : w[s2][1] >> 4;
+          mma_16816(c[s2][q], xa & m0, xb & m0, xa & m1, xb & m1, bf.x, bf.y);
+        }
       }
     }
-    const float dA = __half2float(__ushort_as_half(st_scales[rA * 8 + bt]));
-    const float dB = __half2float(__ushort_as_half(st_scales[rB * 8 + bt]));
     if (t < M) {
-      const float F = fxm[b], S = sxm[b];
-      acc[0] = fmaf(dA, fmaf(F, (c0[0] + c0[1]) + (c1[0] + c1[1]), -S), acc[0]);
-      acc[1] = fmaf(dB, fmaf(F, (c0[2] + c0[3]) + (c1[2] + c1[3]), -S), acc[1]);
+      const float F = bl ? F2.y : F2.x, S = bl ? S2.y : S2.x;
+#pragma unroll
+      for (int s2 = 0; s2 < 2; ++s2) {
+        const float dA = bl ? __high2float(*reinterpret_cast<const __half2*>(&dpair[s2][0]))
+                            : __low2float(*reinterpret_cast<const __half2*>(&dpair[s2][0]));
+        const float dB = bl ? __high2float(*reinterpret_cast<const __half2*>(&dpair[s2][1]))
+                            : __low2float(*reinterpret_cast<const __half2*>(&dpair[s2][1]));
+        acc[s2][0] = fmaf(dA, fmaf(F, (c[s2][0][0] + c[s2][0][1]) + (c[s2][1][0] + c[s2][1][1]), -S), acc[s2][0]);
+        acc[s2][1] = fmaf(dB, fmaf(F, (c[s2][0][2] + c[s2][0][3]) + (c[s2][1][2] + c[s2][1][3]), -S), acc[s2][1]);
+      }
     }
   }
 }
@@ -528,7 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       cached_split = split;
     }
     float acc8[FMT == KQ_Q8_0 ? kRowsPerWarp : 1][M];
-    float acc2[2] = {0.f, 0.f};
+    float acc4[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
     for (int r = 0; r < (FMT == KQ_Q8_0 ? kRowsPerWarp : 1); ++r)
 #pragma unroll
@@ -554,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
           q8_0_tile<M>(st, st_scales, rows, ci, xlen_pad, xbuf, cw, lane, acc8);
       } else {
         const int nblk_valid = (int)min64(8, (kend - k0) / 128);
-        pq2_0_tile<M>(st, st_scales, rows, ci, nblk_valid, xlen_pad, xbuf, fx, sx, cw, lane, acc2);
+        pq2_0_tile<M>(st, st_scales, rows, ci, nblk_valid, xbuf, fx, sx, xlen_pad, cw, lane, acc4);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
@@ -594,30 +620,41 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         }
       }
     } else {
-      // warps cw and cw + 8 hold the two K halves of the same 16 rows: the
-      // second hands its partials over, the first adds them in a fixed order
-      const int slab = cw & 7, kh = cw >> 3;
-      float* cb = combine + slab * 64;
-      if (kh == 1) {
-        cb[2 * lane] = acc2[0];
-        cb[2 * lane + 1] = acc2[1];
+      // warps cw, cw + 4, cw + 8, cw + 12 hold the four K quarters of the
+      // same 32 rows: the last three hand their partials over, the first
+      // adds them in quarter order
+      const int sp = cw & 3, kq = cw >> 2;
+      float* cb = combine + sp * (3 * 32 * 4);
+      if (kq > 0) {
+        float4 v = make_float4(acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]);
+        *reinterpret_cast<float4*>(cb + ((kq - 1) * 32 + lane) * 4) = v;
       }
-      named_barrier(2 + slab, 64);
-      if (kh == 0 && !*abort_flag) {
+      named_barrier(2 + sp, 128);
+      if (kq == 0 && !*abort_flag) {
         const int g = lane >> 2, t = lane & 3;
-        const float yA = acc2[0] + cb[2 * lane], yB = acc2[1] + cb[2 * lane + 1];
-        const int rA = slab * 16 + g, rB = rA + 8;
+        float y4[4] = {acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]};
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const float4 v = *reinterpret_cast<const float4*>(cb + (q * 32 + lane) * 4);
+          y4[0] += v.x;
+          y4[1] += v.y;
+          y4[2] += v.z;
+          y4[3] += v.w;
+        }
         if (t < M) {
-          if (job.splits == 1) {
-            if (rA < rows) job.y[(int64_t)t * job.ldy + row0 + rA] = yA;
-            if (rB < rows) job.y[(int64_t)t * job.ldy + row0 + rB] = yB;
-          } else {
-            if (rA < rows) job.ws[((int64_t)split * M + t) * job.n + row0 + rA] = yA;
-            if (rB < rows) job.ws[((int64_t)split * M + t) * job.n + row0 + rB] = yB;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int r = sp * 32 + (e >> 1) * 16 + (e & 1) * 8 + g;  // slab e/2, row g or g+8
+            if (r < rows) {
+              if (job.splits == 1)
+                job.y[(int64_t)t * job.ldy + row0 + r] = y4[e];
+              else
+                job.ws[((int64_t)split * M + t) * job.n + row0 + r] = y4[e];
+            }
           }
         }
       }
-      named_barrier(2 + slab, 64);
+      named_barrier(2 + sp, 128);
     }
   }
 }

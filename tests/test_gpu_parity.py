@@ -348,33 +348,45 @@ def test_tc_q8_0_exact_integer_case_tolerance_zero(kq):
         assert np.array_equal(Y.astype(np.float64), (X.astype(np.int64) @ q.T) * 2.0**-5), splits
 
 
-def test_tc_pq2_0_single_weight_rows_pin_the_pairing(kq):
-    # row r holds one nonzero ternary weight, at column r (all other codes 1,
-    # value 0): y[r] = +-d x'[r], so a wrong code pairing, B permutation or
-    # positional scale moves or rescales the weight and fails.  The rotated
-    # activations x' are integers of magnitude 16..64 (x = R x' in FP64,
-    # rounded to fp32), so no x'[r] is near zero.
-    n, k, m = 128, 256, 16
-    d = 2.0**-3
+def _single_weight_pq2_0(kq, n, k, d=2.0**-3):
+    """PQ2_0 matrix whose row r holds one nonzero ternary weight, at column
+    (r * 37) % k (all other codes 1, value 0); returns (W, codes)."""
     blocks = np.zeros((n, k // 128, 34), dtype=np.uint8)
     dbits = np.array([d], dtype=np.float16).view(np.uint16)[0]
     blocks[:, :, 0] = dbits & 0xFF
     blocks[:, :, 1] = dbits >> 8
     codes = np.ones((n, k), dtype=np.uint8)
-    for r in range(n):
-        codes[r, r] = 2 if r % 3 else 0
+    cols = (np.arange(n) * 37) % k
+    codes[np.arange(n), cols] = np.where(np.arange(n) % 3, 2, 0)
     for j in range(k):
         blocks[:, j // 128, 2 + (j % 128) // 4] |= (codes[:, j] << (2 * (j % 4))).astype(np.uint8)
     W = kq.QMatrix("pq2_0", n, k)
     kq.kq_prepare(W, torch.from_numpy(blocks.reshape(-1)).cuda())
+    return W, codes, cols
+
+
+@pytest.mark.parametrize("path", ["gemv", "tc"])
+def test_pq2_0_single_weight_rows(kq, path):
+    # row r holds one nonzero ternary weight: y[r] = +-d x'[col r], so the
+    # bound 1e-4 * sum |w x'| is 1e-4 * d |x'[col r]|.  This pins the code
+    # pairing and B permutation, and fails a kernel that forms sum c x' and
+    # subtracts sum x' afterwards (the accumulator's rounding of the cancelled
+    # terms is far above the bound).  The rotated activations x' are integers
+    # of magnitude 16..64 (x = R x' in FP64, rounded to fp32).
+    n, k = 200, 5120
+    m = 1 if path == "gemv" else 16
+    W, codes, cols = _single_weight_pq2_0(kq, n, k)
     rng = np.random.default_rng(13)
     xr = (rng.integers(16, 65, size=(m, k)) * rng.choice([-1, 1], size=(m, k))).astype(np.float32)
     X = oracle.rotate_rows(xr)[1]  # R is its own inverse
-    Y = _run_tc(kq, W, torch.from_numpy(X.reshape(-1)).cuda(), m, 1)
+    if path == "gemv":
+        Y = _run_gemv(kq, W, torch.from_numpy(X.reshape(-1)).cuda()).reshape(1, n)
+    else:
+        Y = _run_tc(kq, W, torch.from_numpy(X.reshape(-1)).cuda(), m, 1)
     Xr = oracle.rotate_rows(X)[0]
-    sign = codes[np.arange(n), np.arange(n)].astype(np.float64) - 1
-    expect = Xr[:, :n] * d * sign
-    assert np.all(np.abs(Y - expect) <= TOL * np.abs(expect))
+    sign = codes[np.arange(n), cols].astype(np.float64) - 1
+    expect = Xr[:, cols] * 2.0**-3 * sign
+    assert np.all(np.abs(Y - expect) <= TOL * np.abs(expect)), np.max(np.abs(Y - expect) / (TOL * np.abs(expect)))
 
 
 def test_tc_workspace_too_small_is_rejected(kq, wl):
