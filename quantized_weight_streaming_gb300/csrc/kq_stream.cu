@@ -71,7 +71,7 @@ constexpr int kScratchFloats = 128;   // per-warp scratch (one Hadamard block)
 constexpr int kCombineFloats = 4 * 3 * 32 * 4;  // K-quarter partials handed to the first warp of each slab pair
 constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kXMax * 4 + 2 * (size_t)kBlkMax * 4 +
                               (size_t)kConsumerWarps * kScratchFloats * 4 + (size_t)kCombineFloats * 4 +
-                              2 * kStages * 8 + 16;
+                              2 * kStages * 8 + 8 * 8 + 16;
 
 __device__ unsigned int g_stream_status = 0;
 __device__ __forceinline__ void stream_flag(int status) { atomicOr(&g_stream_status, 1u << status); }
@@ -128,6 +128,26 @@ struct ItemCursor {
   Job job;
   const CUtensorMap* mc = nullptr;
   const CUtensorMap* ms = nullptr;
+  int32_t split = 0, rb = 0;  // the item's K split and 128-row block within the job
+  int64_t last = -2;          // the item last decoded
+  // Moves to `item` and decodes its (split, row block): by one step from the
+  // previous item of the same job (items are split-major), else by one
+  // 32-bit division.
+  __device__ void next(const Params& p, int64_t item) {
+    const int32_t j0 = j;
+    seek(p, item);
+    if (j == j0 && item == last + 1) {
+      if (++rb == job.row_blocks) {
+        rb = 0;
+        ++split;
+      }
+    } else {
+      const int32_t local = (int32_t)(item - job.item_begin);
+      split = local / job.row_blocks;
+      rb = local - split * job.row_blocks;
+    }
+    last = item;
+  }
   __device__ void seek(const Params& p, int64_t item) {
     if (p.jobs == nullptr) {
       if (j < 0) {
@@ -462,13 +482,19 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   float* combine = scratch_all + kConsumerWarps * kScratchFloats;
   uint64_t* full = reinterpret_cast<uint64_t*>(combine + kCombineFloats);
   uint64_t* empty = full + kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + kStages);
+  uint64_t* cfull = empty + kStages;  // [4] PQ2_0: K-quarter partials of a slab pair written
+  uint64_t* cfree = cfull + 4;        // [4] PQ2_0: the slab pair's partials consumed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(cfree + 4);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps);
+    }
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&cfull[q], 3);
+      mbar_init(&cfree[q], 1);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -487,16 +513,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       bool ok = true;
       int32_t last_j = -1;
       for (int64_t item = ib; item < ie && ok; ++item) {
-        cur.seek(p, item);
+        cur.next(p, item);
         if (cur.j != last_j) {
           prefetch_tmap(cur.mc);
           prefetch_tmap(cur.ms);
           last_j = cur.j;
         }
         const Job& job = cur.job;
-        const int64_t local = item - job.item_begin;
-        const int split = (int)(local / job.row_blocks);
-        const int rb = (int)(local % job.row_blocks);
+        const int split = cur.split, rb = cur.rb;
         const int64_t kbeg = (int64_t)split * job.split_k;
         const int64_t kend = min64(job.k, kbeg + job.split_k);
         for (int64_t k0 = kbeg; k0 < kend; k0 += F::kChunk, ++tile) {
@@ -533,14 +557,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   float* scratch = scratch_all + cw * kScratchFloats;
   ItemCursor cur;
   int32_t cached_job = -1, cached_split = -1;
-  int64_t tile = 0;
+  int ring = 0;            // stage of the next tile
+  uint32_t ring_par = 0;   // its phase parity
+  uint32_t combines = 0;   // PQ2_0 slab-pair handoffs so far
   int xlen_pad = 0;
   for (int64_t item = ib; item < ie; ++item) {
-    cur.seek(p, item);
+    cur.next(p, item);
     const Job& job = cur.job;
-    const int64_t local = item - job.item_begin;
-    const int split = (int)(local / job.row_blocks);
-    const int rb = (int)(local % job.row_blocks);
+    const int split = cur.split, rb = cur.rb;
     const int64_t row0 = (int64_t)rb * kTileRows;
     const int rows = (int)min64(kTileRows, job.n - row0);
     const int64_t kbeg = (int64_t)split * job.split_k;
@@ -562,10 +586,16 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 
     // After an abort every warp keeps walking the item list (so the named
     // barriers stay matched) but waits for and computes nothing.
-    int ci = 0;
-    for (int64_t k0 = kbeg; k0 < kend; k0 += F::kChunk, ++tile, ++ci) {
-      const int s = (int)(tile % kStages);
-      const uint32_t par = (uint32_t)((tile / kStages) & 1);
+    const int klen = (int)(kend - kbeg);
+    const int nch = (klen + F::kChunk - 1) / F::kChunk;
+    for (int ci = 0; ci < nch; ++ci) {
+      const int s = ring;
+      const uint32_t par = ring_par;
+      if (++ring == kStages) {
+        ring = 0;
+        ring_par ^= 1u;
+      }
+      const int64_t k0 = kbeg + (int64_t)ci * F::kChunk;
       if (*abort_flag) continue;
       if (!mbar_wait_bounded(&full[s], par)) {
         *abort_flag = 1;
@@ -579,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         if (k0 + (int64_t)(lane + 1) * F::kGran <= kend)
           q8_0_tile<M>(st, st_scales, rows, ci, xlen_pad, xbuf, cw, lane, acc8);
       } else {
-        const int nblk_valid = (int)min64(8, (kend - k0) / 128);
+        const int nblk_valid = min(8, (klen - ci * F::kChunk) / 128);
         pq2_0_tile<M>(st, st_scales, rows, ci, nblk_valid, xbuf, fx, sx, xlen_pad, cw, lane, acc4);
       }
       __syncwarp();
@@ -621,16 +651,31 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       }
     } else {
       // warps cw, cw + 4, cw + 8, cw + 12 hold the four K quarters of the
-      // same 32 rows: the last three hand their partials over, the first
-      // adds them in quarter order
+      // same 32 rows: the last three hand their partials over through the
+      // slab pair's buffer and go on (they only wait, before writing, until
+      // the previous handoff has been read); the first adds them in quarter
+      // order and writes the outputs
       const int sp = cw & 3, kq = cw >> 2;
       float* cb = combine + sp * (3 * 32 * 4);
+      const uint32_t cpar = combines & 1u;
+      ++combines;
+      if (*abort_flag) continue;
       if (kq > 0) {
-        float4 v = make_float4(acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]);
-        *reinterpret_cast<float4*>(cb + ((kq - 1) * 32 + lane) * 4) = v;
-      }
-      named_barrier(2 + sp, 128);
-      if (kq == 0 && !*abort_flag) {
+        if (!mbar_wait_bounded(&cfree[sp], cpar ^ 1u)) {
+          *abort_flag = 1;
+          stream_flag(KQ_ERR_TIMEOUT);
+          continue;
+        }
+        *reinterpret_cast<float4*>(cb + ((kq - 1) * 32 + lane) * 4) =
+            make_float4(acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cfull[sp]);
+      } else {
+        if (!mbar_wait_bounded(&cfull[sp], cpar)) {
+          *abort_flag = 1;
+          stream_flag(KQ_ERR_TIMEOUT);
+          continue;
+        }
         const int g = lane >> 2, t = lane & 3;
         float y4[4] = {acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]};
 #pragma unroll
@@ -641,6 +686,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
           y4[2] += v.z;
           y4[3] += v.w;
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&cfree[sp]);
         if (t < M) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -654,7 +701,6 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
           }
         }
       }
-      named_barrier(2 + sp, 128);
     }
   }
 }
