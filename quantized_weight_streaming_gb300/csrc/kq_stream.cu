@@ -58,20 +58,33 @@ namespace kq {
 // ---- geometry ---------------------------------------------------------------
 constexpr int kConsumerWarps = 16;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
-constexpr int kRowsPerWarp = 8;
-constexpr int kTileRows = kConsumerWarps * kRowsPerWarp;  // 128
-constexpr int kChunkBytes = 256;                          // code bytes per row per tile (32 lanes x 8 B)
-constexpr int kTileCodeBytes = kTileRows * kChunkBytes;    // 32 KB
-constexpr int kTileScaleBytes = kTileRows * 16;            // 8 fp16 scales per row per tile
-constexpr int kStageBytes = kTileCodeBytes + kTileScaleBytes;
-constexpr int kStages = 4;
+constexpr int kRowsPerWarp = 8;   // Q8_0 rows per consumer warp
+constexpr int kChunkBytes = 256;  // code bytes per row per tile (32 lanes x 8 B)
 constexpr int kXMax = 18432;          // activation floats (or B-fragment words) staged per item (all m)
 constexpr int kBlkMax = kXMax / 128;  // PQ2_0 per-block side arrays
 constexpr int kScratchFloats = 128;   // per-warp scratch (one Hadamard block)
-constexpr int kCombineFloats = 4 * 3 * 32 * 4;  // K-quarter partials handed to the first warp of each slab pair
-constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kXMax * 4 + 2 * (size_t)kBlkMax * 4 +
-                              (size_t)kConsumerWarps * kScratchFloats * 4 + (size_t)kCombineFloats * 4 +
-                              2 * kStages * 8 + 8 * 8 + 16;
+
+// Per-format tile geometry.  Q8_0: 128-row tiles (16 warps x 8 rows), a
+// ring of 4 stages.  PQ2_0: 256-row tiles, each consumer warp owning 64 rows
+// (four 16-row slabs) and a quarter of the tile's K, so every B fragment it
+// loads serves four slabs; a ring of 2 stages of 68 KB.  The PQ2_0 K-part
+// combine buffer shares its space with the staging scratch: the two are
+// never in use at the same time (staging runs between CTA-wide barriers,
+// after every warp has finished its handoffs).
+template <int FMT>
+struct Geo {
+  static constexpr int kTileRows = FMT == KQ_PQ2_0 ? 256 : 128;
+  static constexpr int kTileCodeBytes = kTileRows * kChunkBytes;
+  static constexpr int kTileScaleBytes = kTileRows * 16;  // 8 fp16 scales per row per tile
+  static constexpr int kStageBytes = kTileCodeBytes + kTileScaleBytes;
+  static constexpr int kStages = FMT == KQ_PQ2_0 ? 2 : 4;
+  static constexpr int kCombineFloats = FMT == KQ_PQ2_0 ? 4 * 3 * 32 * 8 : 0;  // 4 row groups x 3 handing warps
+  static constexpr int kScratchRegion =
+      kConsumerWarps * kScratchFloats > kCombineFloats ? kConsumerWarps * kScratchFloats : kCombineFloats;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kXMax * 4 + 2 * (size_t)kBlkMax * 4 +
+                                       (size_t)kScratchRegion * 4 + 2 * kStages * 8 + 8 * 8 + 16;
+};
+constexpr int tile_rows(int fmt) { return fmt == KQ_PQ2_0 ? Geo<KQ_PQ2_0>::kTileRows : Geo<KQ_Q8_0>::kTileRows; }
 
 __device__ unsigned int g_stream_status = 0;
 __device__ __forceinline__ void stream_flag(int status) { atomicOr(&g_stream_status, 1u << status); }
@@ -243,13 +256,6 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return (uint32_t)__half_as_ushort(__float2half_rn(lo)) | ((uint32_t)__half_as_ushort(__float2half_rn(hi)) << 16);
 }
 
-// Byte offset, inside a stage, of code byte `col` (0..255) of tile row `row`
-// for the two 128-byte swizzled half boxes.
-__device__ __forceinline__ int swz_code_offset(int row, int col) {
-  const int half = col >> 7, o = col & 127;
-  return half * (kTileRows * 128) + row * 128 + ((((o >> 4) ^ (row & 7))) << 4) + (o & 15);
-}
-
 // B table entry (uint2) of (block b of the slice, word group q, MMA j,
 // column n < 2M, thread t): 64 M entries of 8 bytes per block of 128
 // positions, i.e. 4 M bytes per position, the size of M fp32 activations.
@@ -386,36 +392,29 @@ __device__ __forceinline__ void q8_0_tile(const uint8_t* st_codes, const uint16_
 }
 
 // ---------------------------------------------------------------------------
-// PQ2_0 consumer math for one tile: warp cw takes the 32 rows of slab pair
-// cw % 4 (two 16-row slabs) and the K quarter cw / 4 (2 blocks, 256 codes
-// per row), so every B fragment it loads serves both slabs and its 16 MMAs
-// per block form four independent chains.  acc[s][0] / acc[s][1] are the
-// partial outputs of rows g and g+8 of slab s for activation row m = t.
+// PQ2_0 consumer math for one 256-row tile: warp cw takes the 64 rows of row
+// group cw % 4 (four 16-row slabs) and the K quarter cw / 4 (2 blocks, 256
+// codes per row), so every B fragment it loads serves four slabs and its 32
+// MMAs per block form eight independent chains.  acc[s][0] / acc[s][1] are
+// the partial outputs of rows g and g+8 of slab s for activation row m = t.
 // ---------------------------------------------------------------------------
 template <int M>
 __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16_t* st_scales, int rows, int ci,
                                            int nblk_valid, const float* xbuf, const float* fx, const float* sx,
-                                           int xlen_pad, int cw, int lane, float (&acc)[2][2]) {
-  const int sp = cw & 3, kq = cw >> 2;
-  if (sp * 32 >= rows) return;
+                                           int xlen_pad, int cw, int lane, float (&acc)[4][2]) {
+  constexpr int kRows = Geo<KQ_PQ2_0>::kTileRows;
+  const int rg = cw & 3, kq = cw >> 2;
+  if (rg * 64 >= rows) return;
   const int g = lane >> 2, t = lane & 3;
   const int kh = kq >> 1;  // 128-byte half box holding this quarter
-  // Rows g, g+8 of both slabs share r % 8 = g, so the swizzled offset of word
-  // t of chunk c is base + ((c ^ g) << 4) for all four rows.
-  const uint8_t* base = st_codes + kh * (kTileRows * 128) + (sp * 32 + g) * 128 + 4 * t;
+  // Rows g, g+8 of every slab share r % 8 = g, so the swizzled offset of word
+  // t of chunk c is base + ((c ^ g) << 4) for all eight rows.
+  const uint8_t* base = st_codes + kh * (kRows * 128) + (rg * 64 + g) * 128 + 4 * t;
   const int g16 = g << 4;
   const bool has_b = g < 2 * M;
   const uint2* bthread = reinterpret_cast<const uint2*>(xbuf) + (has_b ? g : 0) * 4 + t;
-  // the tile's two block scales of the four rows (fp16 pairs), and the two
-  // blocks' activation factors and sums
+  // the two blocks' activation factors and sums
   const int bt0 = 2 * kq;  // first block of the quarter inside the tile row
-  uint32_t dpair[2][2];
-#pragma unroll
-  for (int s2 = 0; s2 < 2; ++s2) {
-    const int rA = sp * 32 + s2 * 16 + g;
-    dpair[s2][0] = *reinterpret_cast<const uint32_t*>(st_scales + rA * 8 + bt0);
-    dpair[s2][1] = *reinterpret_cast<const uint32_t*>(st_scales + (rA + 8) * 8 + bt0);
-  }
   const int b0 = ci * 8 + bt0;  // first block inside the staged slice
   const int tm = t < M ? t : 0;  // lanes t >= M hold no activation row
   const float2 F2 = *reinterpret_cast<const float2*>(fx + tm * (xlen_pad / 128) + b0);
@@ -424,21 +423,20 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
   for (int bl = 0; bl < 2; ++bl) {
     if (bt0 + bl >= nblk_valid) break;
     const uint2* bb = bthread + (b0 + bl) * (2 * 4 * 2 * M * 4);
-    float c[2][2][4];
+    // one accumulator per slab: four chains of 8 MMAs, interleaved
+    float c[4][4];
 #pragma unroll
-    for (int s2 = 0; s2 < 2; ++s2)
+    for (int s4 = 0; s4 < 4; ++s4)
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) c[s2][q][e] = 0.f;
+      for (int e = 0; e < 4; ++e) c[s4][e] = 0.f;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int off = ((((kq & 1) * 4 + 2 * bl + q) << 4) ^ g16);
-      uint32_t w[2][2];
+      uint32_t w[4][2];
 #pragma unroll
-      for (int s2 = 0; s2 < 2; ++s2) {
-        w[s2][0] = *reinterpret_cast<const uint32_t*>(base + s2 * (16 * 128) + off);
-        w[s2][1] = *reinterpret_cast<const uint32_t*>(base + s2 * (16 * 128) + 8 * 128 + off);
+      for (int s4 = 0; s4 < 4; ++s4) {
+        w[s4][0] = *reinterpret_cast<const uint32_t*>(base + s4 * (16 * 128) + off);
+        w[s4][1] = *reinterpret_cast<const uint32_t*>(base + s4 * (16 * 128) + 8 * 128 + off);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -446,22 +444,21 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
         if (has_b) bf = bb[(q * 4 + j) * (2 * M * 4)];
         const uint32_t m0 = 0x00030003u << pair_bit(j, 0), m1 = 0x00030003u << pair_bit(j, 1);
 #pragma unroll
-        for (int s2 = 0; s2 < 2; ++s2) {
-          const uint32_t xa = j < 3 ? w[s2][0] : w[s2][0] >> 4, xb = j < 3 ? w[s2][1] : w[s2][1] >> 4;
-          mma_16816(c[s2][q], xa & m0, xb & m0, xa & m1, xb & m1, bf.x, bf.y);
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const uint32_t xa = j < 3 ? w[s4][0] : w[s4][0] >> 4, xb = j < 3 ? w[s4][1] : w[s4][1] >> 4;
+          mma_16816(c[s4], xa & m0, xb & m0, xa & m1, xb & m1, bf.x, bf.y);
         }
       }
     }
     if (t < M) {
       const float F = bl ? F2.y : F2.x, S = bl ? S2.y : S2.x;
 #pragma unroll
-      for (int s2 = 0; s2 < 2; ++s2) {
-        const float dA = bl ? __high2float(*reinterpret_cast<const __half2*>(&dpair[s2][0]))
-                            : __low2float(*reinterpret_cast<const __half2*>(&dpair[s2][0]));
-        const float dB = bl ? __high2float(*reinterpret_cast<const __half2*>(&dpair[s2][1]))
-                            : __low2float(*reinterpret_cast<const __half2*>(&dpair[s2][1]));
-        acc[s2][0] = fmaf(dA, fmaf(F, (c[s2][0][0] + c[s2][0][1]) + (c[s2][1][0] + c[s2][1][1]), -S), acc[s2][0]);
-        acc[s2][1] = fmaf(dB, fmaf(F, (c[s2][0][2] + c[s2][0][3]) + (c[s2][1][2] + c[s2][1][3]), -S), acc[s2][1]);
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const int rA = rg * 64 + s4 * 16 + g;
+        const float dA = __half2float(__ushort_as_half(st_scales[rA * 8 + bt0 + bl]));
+        const float dB = __half2float(__ushort_as_half(st_scales[(rA + 8) * 8 + bt0 + bl]));
+        acc[s4][0] = fmaf(dA, fmaf(F, c[s4][0] + c[s4][1], -S), acc[s4][0]);
+        acc[s4][1] = fmaf(dB, fmaf(F, c[s4][2] + c[s4][3], -S), acc[s4][1]);
       }
     }
   }
@@ -473,14 +470,17 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
 template <int FMT, int M>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ Params p) {
   using F = Fmt<FMT>;
+  using G = Geo<FMT>;
+  constexpr int kStages = G::kStages, kStageBytes = G::kStageBytes, kTileRows = G::kTileRows;
+  constexpr int kTileCodeBytes = G::kTileCodeBytes;
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
   float* fx = xbuf + kXMax;
   float* sx = fx + kBlkMax;
   float* scratch_all = sx + kBlkMax;
-  float* combine = scratch_all + kConsumerWarps * kScratchFloats;
-  uint64_t* full = reinterpret_cast<uint64_t*>(combine + kCombineFloats);
+  float* combine = scratch_all;  // shares the scratch region (see Geo)
+  uint64_t* full = reinterpret_cast<uint64_t*>(scratch_all + G::kScratchRegion);
   uint64_t* empty = full + kStages;
   uint64_t* cfull = empty + kStages;  // [4] PQ2_0: K-quarter partials of a slab pair written
   uint64_t* cfree = cfull + 4;        // [4] PQ2_0: the slab pair's partials consumed
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       cached_split = split;
     }
     float acc8[FMT == KQ_Q8_0 ? kRowsPerWarp : 1][M];
-    float acc4[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    float acc4[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
     for (int r = 0; r < (FMT == KQ_Q8_0 ? kRowsPerWarp : 1); ++r)
 #pragma unroll
@@ -651,12 +651,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       }
     } else {
       // warps cw, cw + 4, cw + 8, cw + 12 hold the four K quarters of the
-      // same 32 rows: the last three hand their partials over through the
-      // slab pair's buffer and go on (they only wait, before writing, until
+      // same 64 rows: the last three hand their partials over through the
+      // row group's buffer and go on (they only wait, before writing, until
       // the previous handoff has been read); the first adds them in quarter
       // order and writes the outputs
       const int sp = cw & 3, kq = cw >> 2;
-      float* cb = combine + sp * (3 * 32 * 4);
+      float* cb = combine + sp * (3 * 32 * 8);
       const uint32_t cpar = combines & 1u;
       ++combines;
       if (*abort_flag) continue;
@@ -666,8 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
           stream_flag(KQ_ERR_TIMEOUT);
           continue;
         }
-        *reinterpret_cast<float4*>(cb + ((kq - 1) * 32 + lane) * 4) =
-            make_float4(acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]);
+        float4* dst = reinterpret_cast<float4*>(cb + ((kq - 1) * 32 + lane) * 8);
+        dst[0] = make_float4(acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]);
+        dst[1] = make_float4(acc4[2][0], acc4[2][1], acc4[3][0], acc4[3][1]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&cfull[sp]);
       } else {
@@ -677,26 +678,32 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
           continue;
         }
         const int g = lane >> 2, t = lane & 3;
-        float y4[4] = {acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]};
+        float y8[8] = {acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1],
+                       acc4[2][0], acc4[2][1], acc4[3][0], acc4[3][1]};
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
-          const float4 v = *reinterpret_cast<const float4*>(cb + (q * 32 + lane) * 4);
-          y4[0] += v.x;
-          y4[1] += v.y;
-          y4[2] += v.z;
-          y4[3] += v.w;
+          const float4* src = reinterpret_cast<const float4*>(cb + (q * 32 + lane) * 8);
+          const float4 v0 = src[0], v1 = src[1];
+          y8[0] += v0.x;
+          y8[1] += v0.y;
+          y8[2] += v0.z;
+          y8[3] += v0.w;
+          y8[4] += v1.x;
+          y8[5] += v1.y;
+          y8[6] += v1.z;
+          y8[7] += v1.w;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&cfree[sp]);
         if (t < M) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int r = sp * 32 + (e >> 1) * 16 + (e & 1) * 8 + g;  // slab e/2, row g or g+8
+          for (int e = 0; e < 8; ++e) {
+            const int r = sp * 64 + (e >> 1) * 16 + (e & 1) * 8 + g;  // slab e/2, row g or g+8
             if (r < rows) {
               if (job.splits == 1)
-                job.y[(int64_t)t * job.ldy + row0 + r] = y4[e];
+                job.y[(int64_t)t * job.ldy + row0 + r] = y8[e];
               else
-                job.ws[((int64_t)split * M + t) * job.n + row0 + r] = y4[e];
+                job.ws[((int64_t)split * M + t) * job.n + row0 + r] = y8[e];
             }
           }
         }
@@ -737,11 +744,11 @@ static Geometry make_geometry(int fmt, int64_t n, int64_t k, int64_t m, int requ
   const int64_t unit = chunk_of(fmt);
   const int64_t max_split = std::max<int64_t>(unit, (kXMax / m) / unit * unit);
   const int64_t min_splits = (k + max_split - 1) / max_split;
-  const int64_t row_blocks = (n + kTileRows - 1) / kTileRows;
+  const int64_t row_blocks = (n + tile_rows(fmt) - 1) / tile_rows(fmt);
   int64_t splits = std::max<int64_t>(requested > 0 ? requested : 1, min_splits);
   if (requested == 0 && sms > 0) {
     const int64_t chunks = (k + unit - 1) / unit;
-    constexpr double kTileUs = 0.75, kReduceUs = 2.5;
+    const double kTileUs = fmt == KQ_PQ2_0 ? 2.0 : 0.75, kReduceUs = 2.5;
     double best = 1e30;
     for (int64_t s = min_splits; s <= chunks; ++s) {
       const int64_t sk = round_up((k + s - 1) / s, unit);
@@ -792,7 +799,7 @@ static int make_maps(const kq_qmat* W, CUtensorMap* mc, CUtensorMap* ms) {
   // Q8_0: one 256-byte box per tile row; PQ2_0: two 128-byte boxes with the
   // 128-byte swizzle (the tensor-core consumer reads columns of 8 rows)
   const bool swz = W->fmt == KQ_PQ2_0;
-  cuuint32_t box[2] = {swz ? 32u : (cuuint32_t)(kChunkBytes / 4), kTileRows};
+  cuuint32_t box[2] = {swz ? 32u : (cuuint32_t)(kChunkBytes / 4), (cuuint32_t)tile_rows(W->fmt)};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(W->codes), gdim, gstride, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -800,7 +807,7 @@ static int make_maps(const kq_qmat* W, CUtensorMap* mc, CUtensorMap* ms) {
   if (r != CUDA_SUCCESS) return fail(KQ_ERR_CUDA, "tensor map of the codes plane: CUresult %d", (int)r);
   cuuint64_t sdim[2] = {(cuuint64_t)(sst / 2), (cuuint64_t)W->n};
   cuuint64_t sstr[1] = {(cuuint64_t)(sst * 2)};
-  cuuint32_t sbox[2] = {4, kTileRows};
+  cuuint32_t sbox[2] = {4, (cuuint32_t)tile_rows(W->fmt)};
   r = fn(ms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(W->scales), sdim, sstr, sbox, es,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -822,10 +829,10 @@ static int launch_stream(const Params& p, int grid, cudaStream_t st) {
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(stream_kernel<FMT, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)kSmemBytes);
+                                    (int)Geo<FMT>::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return fail(KQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  stream_kernel<FMT, M><<<grid, kThreads, kSmemBytes, st>>>(p);
+  stream_kernel<FMT, M><<<grid, kThreads, Geo<FMT>::kSmemBytes, st>>>(p);
   KQ_CUDA_TRY(cudaGetLastError());
   return KQ_OK;
 }
@@ -1042,7 +1049,7 @@ int kq_decode_plan_create(const kq_qmat* mats, int64_t count, kq_plan** out) {
     j.split_k = (int32_t)W.k;
     const double rb = (double)code_row_bytes(fmt, W.k) + 2.0 * (W.k / block_of(fmt));
     for (int32_t r = 0; r < g.row_blocks; ++r)
-      item_bytes.push_back(rb * (double)std::min<int64_t>(kTileRows, W.n - (int64_t)r * kTileRows));
+      item_bytes.push_back(rb * (double)std::min<int64_t>(tile_rows(fmt), W.n - (int64_t)r * tile_rows(fmt)));
     items += g.row_blocks;
     xf += W.k;
     yf += W.n;
