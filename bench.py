@@ -515,6 +515,30 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def profile_gemm(spec):
+    """Three kq_gemm_small_m calls on one synthetic matrix (for ncu captures of
+    the GEMM kernels: -k regex:tc_gemm_kernel -s 2 -c 1)."""
+    import torch
+    import synth
+    import quantized_weight_streaming_gb300 as kq
+    import workloads
+
+    fmt, n, k, m = spec.split(",")
+    n, k, m = int(n), int(k), int(m)
+    torch.cuda.set_device(0)
+    W = workloads.build_matrix(fmt, n, k, 0, synth.stream_id("small_m", 0, 0))
+    X = workloads.build_activation(k, 0, synth.stream_id("small_m", 1, 0), rows=m)
+    Y = torch.empty(m * n, dtype=torch.float32, device="cuda")
+    nbytes = kq.kq_gemv_workspace_bytes(W, m)
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        kq.kq_gemm_small_m(W, X, m, Y, ws)
+    torch.cuda.synchronize()
+    if kq.kq_device_status(True) != kq.KQ_OK:
+        raise SystemExit("device status not OK")
+    print(json.dumps({"profile_gemm": spec, "ok": True}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -529,9 +553,13 @@ def main():
                     help="only the first N projections of the workload (small profiling cases)")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the stream kernel from an ncu capture (reported as is)")
+    ap.add_argument("--profile-gemm", default=None, metavar="FMT,N,K,M",
+                    help="profiling case: build one N x K matrix and run kq_gemm_small_m with M rows three times")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)  # at least three untimed warm-up steps
-    if args.impl == "reference":
+    if args.profile_gemm:
+        profile_gemm(args.profile_gemm)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_kq(args)
