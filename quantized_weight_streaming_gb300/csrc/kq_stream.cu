@@ -566,9 +566,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     const Job& job = cur.job;
     const int split = cur.split, rb = cur.rb;
     const int64_t row0 = (int64_t)rb * kTileRows;
-    const int rows = (int)min64(kTileRows, job.n - row0);
+    const int rows = min(kTileRows, (int)(job.n - row0));
     const int64_t kbeg = (int64_t)split * job.split_k;
-    const int64_t kend = min64(job.k, kbeg + job.split_k);
+    const int64_t kend = kbeg + min((int64_t)job.split_k, job.k - kbeg);
     if (cur.j != cached_job || split != cached_split) {
       xlen_pad = (int)(((kend - kbeg) + F::kChunk - 1) / F::kChunk * F::kChunk);
       named_barrier(1, kConsumerWarps * 32);  // everyone is done with the previous slice
@@ -678,6 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
           continue;
         }
         const int g = lane >> 2, t = lane & 3;
+        // this lane's output row of activation t (lanes t >= M write nothing)
+        float* yout = (job.splits == 1 ? job.y + (int64_t)t * job.ldy : job.ws + ((int64_t)split * M + t) * job.n) + row0;
+        const int rmax = t < M ? rows - (sp * 64 + g) : 0;  // rows of this lane's set that exist
         float y8[8] = {acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1],
                        acc4[2][0], acc4[2][1], acc4[3][0], acc4[3][1]};
 #pragma unroll
@@ -695,17 +698,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&cfree[sp]);
-        if (t < M) {
+        float* yl = yout + sp * 64 + g;
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int r = sp * 64 + (e >> 1) * 16 + (e & 1) * 8 + g;  // slab e/2, row g or g+8
-            if (r < rows) {
-              if (job.splits == 1)
-                job.y[(int64_t)t * job.ldy + row0 + r] = y8[e];
-              else
-                job.ws[((int64_t)split * M + t) * job.n + row0 + r] = y8[e];
-            }
-          }
+        for (int e = 0; e < 8; ++e) {
+          const int dr = (e >> 1) * 16 + (e & 1) * 8;  // slab e/2, row g or g+8
+          if (dr < rmax) yl[dr] = y8[e];
         }
       }
     }
