@@ -298,6 +298,36 @@ def _gemv_graph_measure(kq, wl_mod, fmt, n, k, m, stream, replays=20):
     return out
 
 
+CONTROL_RINGS = ((34816, 4), (69632, 2), (65536, 3))  # the Q8_0 and PQ2_0 stream-kernel rings, and a deeper one
+
+
+def _control_measure(kq, nbytes, stream, reps=10):
+    """Read-only streaming control (kq_stream_read) over nbytes, the same byte
+    count as one decode step: the in-harness ceiling of a kernel that reads
+    each byte once through shared memory.  Best of the ring shapes above; each
+    timed over `reps` launches after warm-up (input far larger than L2)."""
+    import torch
+
+    nbytes = nbytes // 16 * 16
+    src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    src.fill_(0x5A)
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    by_ring = {}
+    for stage_bytes, stages in CONTROL_RINGS:
+        run = lambda: kq.kq_stream_read(src, nbytes, sink, stage_bytes=stage_bytes, stages=stages, stream=stream)
+        for _ in range(3):
+            run()
+        secs = _time_steps(run, reps, stream)
+        by_ring[f"{stages}x{stage_bytes}"] = round(nbytes / (secs / reps) / 1e9, 1)
+    if kq.kq_device_status(True) != kq.KQ_OK:
+        raise RuntimeError("device status not ok after the control kernel")
+    del src
+    torch.cuda.empty_cache()
+    best = max(by_ring, key=by_ring.get)
+    return {"kernel": "kq::stream_read_kernel (kq_stream_read)", "gbs": by_ring[best], "ring": best,
+            "bytes": nbytes, "by_ring": by_ring}
+
+
 def run_kq(args):
     import torch
 
@@ -319,13 +349,15 @@ def run_kq(args):
     head = _decode_measure(kq, workloads, args.workload, args.steps, args.warmup, stream, sampler_gpu=gpu_index,
                            world=world, limit=args.matrices)
     peak, peak_kind = _peaks()
+    control = _control_measure(kq, head["bytes_per_step"], stream) if rank == 0 else None
     extras = {}
     if not args.no_extras and rank == 0:
         sec = _decode_measure(kq, workloads, SECONDARY if args.workload != SECONDARY else HEADLINE,
                               max(3, args.steps // 2), args.warmup, stream)
         extras["decode_steps"] = {sec["config"]: {
             "gbs": round(sec["gbs"], 1), "us_per_step": round(sec["per_step_s"] * 1e6, 2),
-            "frac_of_measured_hbm": round(sec["gbs"] / peak, 4), "e2e_gbs": round(sec["e2e_gbs"], 1),
+            "frac_of_measured_hbm": round(sec["gbs"] / peak, 4),
+            "frac_of_control": round(sec["gbs"] / control["gbs"], 4), "e2e_gbs": round(sec["e2e_gbs"], 1),
             "weight_bytes": sec["weight_bytes"], "matrices": sec["matrices"]}}
         gemv = []
         for fmt, n, k, m in (("q8_0", 1024, 2560, 1), ("pq2_0", 10240, 5120, 1), ("q8_0", 9728, 2560, 1),
@@ -361,6 +393,8 @@ def run_kq(args):
                    "parallelism": f"replicas x{world}", "seed": 0},
         "frac_of_measured_hbm": round(per_gpu_gbs / peak, 4),
         "frac_of_nominal_8tbs": round(per_gpu_gbs / 8000.0, 4),
+        "frac_of_control": round(per_gpu_gbs / control["gbs"], 4) if control else None,
+        "control": control,
         "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(per_gpu_gbs / peak, 4),
                      "traffic": args.traffic if args.traffic is not None else _traffic(args.workload),

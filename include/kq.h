@@ -232,6 +232,29 @@ int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, vo
                    void* stream);
 void kq_decode_plan_destroy(kq_plan* plan);
 
+/* ---- read-only streaming control -------------------------------------------- */
+
+/* The in-harness bandwidth ceiling of a kernel that reads each byte once:
+ * streams d_src[0, bytes) from device memory exactly once through shared
+ * memory, on the data path of the GEMV kernels (one persistent CTA per SM,
+ * bulk asynchronous copies with an L2 evict-first hint into a ring of
+ * `stages` buffers of `stage_bytes`, consumer warps reading every 16-byte
+ * word back from shared memory), and XORs the XOR of all 32-bit words of the
+ * range into *d_sink (zero *d_sink first to read that XOR itself).  Its
+ * bandwidth is the control that GEMV bandwidths are compared with ("Bonsai 2
+ * 27B" page, section 8: the practical ceiling measured by a read-only
+ * streaming kernel; "Kipp Benchmarks", decode is weight-bandwidth-bound).
+ *  - bytes: a positive multiple of 16.  d_src, d_sink: 16-byte aligned
+ *    device memory owned by the caller.
+ *  - stage_bytes: a multiple of 16 in [1024, 98304]; stages: 1..8; the ring
+ *    (stages x stage_bytes plus 16 bytes of barriers per stage and 16 more)
+ *    must fit 227 KB of shared memory.
+ *  - Errors: KQ_ERR_INVALID_ARG, KQ_ERR_SHAPE, KQ_ERR_ALIGNMENT, KQ_ERR_CUDA;
+ *    a bounded device wait that expires sets KQ_ERR_TIMEOUT for
+ *    kq_device_status. */
+int kq_stream_read(const void* d_src, int64_t bytes, int32_t stage_bytes, int32_t stages, uint32_t* d_sink,
+                   void* stream);
+
 /* ---- device status --------------------------------------------------------- */
 
 /* binaryVersion (major*10 + minor) of the streaming kernel as loaded on the

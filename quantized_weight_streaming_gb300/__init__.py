@@ -92,6 +92,7 @@ SIGNATURES = {
     "kq_decode_workspace_bytes": (_SZ, [_P]),
     "kq_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _SZ, _P]),
     "kq_decode_plan_destroy": (None, [_P]),
+    "kq_stream_read": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P]),
     "kq_device_status": (ctypes.c_int, [ctypes.c_int]),
     "kq_kernel_binary_version": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
 }
@@ -301,6 +302,13 @@ def kq_gemm_splitk_noalloc(W, d_X, m, d_Y, splits, stream=None):
 
 def kq_gemm_splitk_noalloc_max_bytes():
     return _lib.kq_gemm_splitk_noalloc_max_bytes()
+
+
+def kq_stream_read(d_src, nbytes, d_sink, stage_bytes=34816, stages=4, stream=None):
+    """Read-only streaming control: stream nbytes of d_src once through shared
+    memory; XORs the XOR of its 32-bit words into d_sink[0]."""
+    _check(_lib.kq_stream_read(_ptr(d_src), nbytes, stage_bytes, stages, _ptr(d_sink), _stream(stream)),
+           "kq_stream_read")
 
 
 def kq_device_status(clear=True):

@@ -933,7 +933,8 @@ int read_stream_status(int clear) {
   return (int)v;
 }
 
-int read_prep_status(int clear);  // kq_prep.cu
+int read_prep_status(int clear);     // kq_prep.cu
+int read_control_status(int clear);  // kq_control.cu
 
 }  // namespace kq
 
@@ -1197,8 +1198,9 @@ int kq_device_status(int clear) {
   clear_error();
   KQ_CUDA_TRY(cudaDeviceSynchronize());
   int a = read_stream_status(clear), b = read_prep_status(clear), c = read_tc_status(clear);
-  if (a < 0 || b < 0 || c < 0) return fail(KQ_ERR_CUDA, "reading the device status word failed");
-  const unsigned v = (unsigned)a | (unsigned)b | (unsigned)c;
+  int d = read_control_status(clear);
+  if (a < 0 || b < 0 || c < 0 || d < 0) return fail(KQ_ERR_CUDA, "reading the device status word failed");
+  const unsigned v = (unsigned)a | (unsigned)b | (unsigned)c | (unsigned)d;
   if (v & (1u << KQ_ERR_TIMEOUT)) return fail(KQ_ERR_TIMEOUT, "a bounded device wait expired");
   if (v & (1u << KQ_ERR_NONFINITE)) return fail(KQ_ERR_NONFINITE, "non-finite weight met on the device");
   if (v & (1u << KQ_ERR_RANGE)) return fail(KQ_ERR_RANGE, "scale overflowed fp16 on the device");

@@ -148,6 +148,14 @@ def test_device_entry_points_validate_before_any_cuda_call(kq):
     assert lib.kq_decode_plan_create(mixed, 0, ctypes.byref(h)) == kq.KQ_ERR_SHAPE
     assert lib.kq_decode_step(None, A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
     assert lib.kq_gemv_workspace_bytes(ctypes.byref(bad_k), 1) == 0
+    assert lib.kq_stream_read(None, 1024, 4096, 4, A, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_stream_read(A, 1000, 4096, 4, A, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_stream_read(A, 0, 4096, 4, A, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_stream_read(A, 1024, 4100, 4, A, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_stream_read(A, 1024, 512, 4, A, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_stream_read(A, 1024, 4096, 9, A, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_stream_read(A, 1024, 98304, 3, A, None) == kq.KQ_ERR_INVALID_ARG  # ring above 227 KB
+    assert lib.kq_stream_read(A + 8, 1024, 4096, 4, A, None) == kq.KQ_ERR_ALIGNMENT
 
 
 def test_status_strings(kq):

@@ -406,6 +406,21 @@ def test_tc_workspace_too_small_is_rejected(kq, wl):
 # decode-step driver
 # ----------------------------------------------------------------------------
 
+@pytest.mark.parametrize("nbytes,stage_bytes,stages", [(16, 1024, 1), (1040, 1024, 2), (5_000_000 + 48, 34816, 4),
+                                                      (3 * 98304 + 16, 98304, 2), (300_000_016, 69632, 2)])
+def test_stream_read_control_xor(kq, nbytes, stage_bytes, stages):
+    """The read-only control kernel reads every byte once: the XOR of all
+    32-bit words is integer work, compared bit-exactly with numpy's."""
+    g = torch.Generator(device="cuda").manual_seed(nbytes)
+    src = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda", generator=g)
+    sink = torch.zeros(4, dtype=torch.int32, device="cuda")
+    kq.kq_stream_read(src, nbytes, sink, stage_bytes=stage_bytes, stages=stages)
+    _sync_ok(kq)
+    want = np.bitwise_xor.reduce(src.cpu().numpy().view(np.uint32))
+    assert int(sink[0].item()) & 0xFFFFFFFF == int(want)
+    assert not sink[1:].any()
+
+
 def test_decode_plan_small_mixed_shapes(kq, wl):
     spec = [(16, 256), (33, 1024), (1, 5120), (300, 2048), (17, 17408), (64, 128)]
     for fmt in ("q8_0", "pq2_0"):
