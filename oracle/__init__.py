@@ -60,6 +60,8 @@ def lib():
         L.orc_hadamard.restype = ctypes.c_int
         L.orc_rotate_rows.argtypes = [P, I64, I64, ctypes.c_int32, P, P]
         L.orc_rotate_rows.restype = ctypes.c_int
+        L.orc_rotate_rows_signed.argtypes = [P, I64, I64, ctypes.c_int32, P, P, P]
+        L.orc_rotate_rows_signed.restype = ctypes.c_int
         L.orc_gemv_f64.argtypes = [P, I64, I64, P, P, I64, ctypes.c_int32, P, P]
         L.orc_gemv_f64.restype = ctypes.c_int
         L.orc_max_threads.restype = ctypes.c_int
@@ -143,15 +145,24 @@ def hadamard(n):
     return out
 
 
-def rotate_rows(x, n=HADAMARD_N):
-    """Blockwise R = H_n/sqrt(n) along the last axis.  Returns (fp64, fp32)."""
+def rotate_rows(x, n=HADAMARD_N, signs=None):
+    """Blockwise R = H_n S / sqrt(n) along the last axis (S = diag(signs), the
+    identity when signs is None).  Returns (fp64, fp32)."""
     x = _f32(x)
     shape = x.shape
     x2 = x.reshape(-1, shape[-1])
     rows, k = x2.shape
     o64 = np.empty((rows, k), dtype=np.float64)
     o32 = np.empty((rows, k), dtype=np.float32)
-    _check(lib().orc_rotate_rows(x2.ctypes.data, rows, k, int(n), o64.ctypes.data, o32.ctypes.data), "rotate_rows")
+    if signs is None:
+        sp = None
+    else:
+        sg = np.ascontiguousarray(signs, dtype=np.int8)
+        if sg.shape != (k,):
+            raise OracleError("signs length mismatch")
+        sp = sg.ctypes.data
+    _check(lib().orc_rotate_rows_signed(x2.ctypes.data, rows, k, int(n), sp, o64.ctypes.data, o32.ctypes.data),
+           "rotate_rows")
     return o64.reshape(shape), o32.reshape(shape)
 
 

@@ -21,7 +21,9 @@
  *    H_n the natural-order Sylvester matrix H[r][c] = (-1)^popcount(r & c),
  *    applied block-diagonally along K; the stored weight is W' = W R^T
  *    (rotate, then quantize) and the activation gets x' = R x before the
- *    product.  Signs are the identity here (S = I) and n = 128.
+ *    product.  n = 128 with S = I by default; orc_rotate_rows_signed takes
+ *    the page's general form, any power-of-two n (1024 on the page) and a
+ *    +-1 sign per position of K applied before the transform.
  *
  * Readings where the pages are silent:
  *  - round() is round-half-away-from-zero (C round), decided on the FP64
@@ -68,6 +70,13 @@ int orc_hadamard(int32_t n, double* h_out);
  * of K.  out64 (may be NULL) gets the FP64 values, out32 (may be NULL) the
  * same values rounded once to fp32. */
 int orc_rotate_rows(const float* in, int64_t rows, int64_t k, int32_t n, double* out64, float* out32);
+
+/* The same with a diagonal sign matrix first (the Bonsai page, section 4.1:
+ * R = (1/sqrt(n)) H_n S, S = diag(signs), one +-1 per position of K; sign
+ * flip, then the transform, section 4.2).  signs == NULL is S = I; an entry
+ * other than +1 or -1 is ORC_ERR_SHAPE. */
+int orc_rotate_rows_signed(const float* in, int64_t rows, int64_t k, int32_t n, const int8_t* signs, double* out64,
+                           float* out32);
 
 /* y_i = sum_j w_ij x_j and absdot_i = sum_j |w_ij x_j| in FP64 for the listed
  * rows (rows == NULL: all n rows, in order); w holds the n x k matrix (or

@@ -107,6 +107,61 @@ def test_rotation_is_block_diagonal():
     assert np.max(np.abs(r64 - B @ x.astype(np.float64))) < 1e-12
 
 
+def _signs(k, seed):
+    return np.where(np.random.default_rng(seed).random(k) < 0.5, -1, 1).astype(np.int8)
+
+
+def test_signed_rotation_all_plus_signs_is_the_unsigned_rotation():
+    x = np.random.default_rng(3).standard_normal((3, 2048)).astype(np.float32)
+    for n in (128, 1024):
+        a64, a32 = oracle.rotate_rows(x, n)
+        b64, b32 = oracle.rotate_rows(x, n, signs=np.ones(2048, dtype=np.int8))
+        assert np.array_equal(a64, b64) and np.array_equal(a32, b32)
+
+
+def test_signed_rotation_n1024_matches_scipy_hadamard():
+    """The page's rotation (Bonsai page, sections 4.1-4.2): per 1024-block,
+    x' = H_1024 (s * x) / 32 with scipy's Sylvester matrix, sign first; K =
+    5120 is five blocks with one K-wide sign vector."""
+    k = 5120
+    s = _signs(k, 7)
+    x = np.random.default_rng(4).standard_normal((2, k)).astype(np.float32)
+    got64, got32 = oracle.rotate_rows(x, 1024, signs=s)
+    H = scipy.linalg.hadamard(1024).astype(np.float64)
+    want = np.concatenate([(H @ (s[b * 1024:(b + 1) * 1024] * x[:, b * 1024:(b + 1) * 1024].astype(np.float64)).T).T
+                           for b in range(5)], axis=1) / 32.0
+    assert np.allclose(got64, want, rtol=0, atol=1e-12 * np.abs(x).sum())
+    assert np.array_equal(got32, got64.astype(np.float32))
+    # the transform is orthogonal: S H / 32 undoes it, and norms are kept
+    back = np.concatenate([s[b * 1024:(b + 1) * 1024] * (H @ got64[:, b * 1024:(b + 1) * 1024].T).T / 32.0
+                           for b in range(5)], axis=1)
+    assert np.allclose(back, x, rtol=0, atol=1e-11)
+    assert np.allclose(np.linalg.norm(got64, axis=1), np.linalg.norm(x.astype(np.float64), axis=1), rtol=1e-13)
+
+
+def test_signed_rotation_of_a_signed_unit_vector():
+    """R (s_j e_j) = H e_j / 32 (a column of H over 32): the sign cancels."""
+    k = 2048
+    s = _signs(k, 9)
+    for j in (0, 5, 1023, 1024 + 77):
+        x = np.zeros((1, k), dtype=np.float32)
+        x[0, j] = float(s[j])
+        got, _ = oracle.rotate_rows(x, 1024, signs=s)
+        b, c = divmod(j, 1024)
+        col = scipy.linalg.hadamard(1024)[:, c] / 32.0
+        want = np.zeros(k)
+        want[b * 1024:(b + 1) * 1024] = col
+        assert np.array_equal(got[0], want)
+
+
+def test_signed_rotation_rejects_bad_signs():
+    x = np.zeros((1, 1024), dtype=np.float32)
+    bad = np.ones(1024, dtype=np.int8)
+    bad[3] = 0
+    with pytest.raises(oracle.OracleError):
+        oracle.rotate_rows(x, 1024, signs=bad)
+
+
 def test_rotation_of_grid_weights_is_one_multiply_of_an_exact_sum():
     # Synthetic weights are integers times 2^-20, so H w is an exact integer
     # sum; the oracle must return fl64(fl64(1/sqrt(128)) * (H w)).
