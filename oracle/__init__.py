@@ -56,6 +56,13 @@ def lib():
         for name in ("orc_q8_0_quantize", "orc_q8_0_dequant", "orc_pq2_0_quantize", "orc_pq2_0_dequant"):
             getattr(L, name).argtypes = [P, I64, I64, P]
             getattr(L, name).restype = ctypes.c_int
+        for name in ("orc_ptq1_0_quantize", "orc_ptq1_0_dequant"):
+            getattr(L, name).argtypes = [P, I64, I64, P]
+            getattr(L, name).restype = ctypes.c_int
+        L.orc_ptq1_0_encode_byte.argtypes = [P]
+        L.orc_ptq1_0_encode_byte.restype = ctypes.c_int
+        L.orc_ptq1_0_decode_trit.argtypes = [ctypes.c_int32, ctypes.c_int32]
+        L.orc_ptq1_0_decode_trit.restype = ctypes.c_int
         L.orc_hadamard.argtypes = [ctypes.c_int32, P]
         L.orc_hadamard.restype = ctypes.c_int
         L.orc_rotate_rows.argtypes = [P, I64, I64, ctypes.c_int32, P, P]
@@ -134,6 +141,31 @@ def pq2_0_dequant(blocks, n, k):
     out = np.empty((n, k), dtype=np.float32)
     _check(lib().orc_pq2_0_dequant(b.ctypes.data, n, k, out.ctypes.data), "pq2_0_dequant")
     return out
+
+
+def ptq1_0_quantize(w_rot):
+    """PTQ1_0 blocks [n, k/128, 28] of already rotated weights."""
+    w = _f32(w_rot)
+    n, k = w.shape
+    out = np.zeros((n, k // 128, 28), dtype=np.uint8)
+    _check(lib().orc_ptq1_0_quantize(w.ctypes.data, n, k, out.ctypes.data), "ptq1_0_quantize")
+    return out
+
+
+def ptq1_0_dequant(blocks, n, k):
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    out = np.empty((n, k), dtype=np.float32)
+    _check(lib().orc_ptq1_0_dequant(b.ctypes.data, n, k, out.ctypes.data), "ptq1_0_dequant")
+    return out
+
+
+def ptq1_0_encode_byte(trits):
+    t = np.ascontiguousarray(trits, dtype=np.int32)
+    return lib().orc_ptq1_0_encode_byte(t.ctypes.data)
+
+
+def ptq1_0_decode_trit(q, n):
+    return lib().orc_ptq1_0_decode_trit(int(q), int(n))
 
 
 # -- rotation -----------------------------------------------------------------

@@ -85,6 +85,8 @@ uint16_t orc_half_from_float(float x) {
 #define Q8_0_BYTES 34
 #define PQ2_0_QK 128
 #define PQ2_0_BYTES 34
+#define PTQ1_0_QK 128
+#define PTQ1_0_BYTES 28 /* 24 bytes of five trits, 2 of four trits, then the fp16 scale */
 
 int orc_q8_0_quantize(const float* w, int64_t n, int64_t k, uint8_t* blocks) {
   if (n < 0 || k <= 0 || k % Q8_0_QK != 0) return ORC_ERR_SHAPE;
@@ -195,6 +197,108 @@ int orc_pq2_0_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out)
       for (int j = 0; j < PQ2_0_QK; ++j) {
         int code = (blk[2 + j / 4] >> (2 * (j % 4))) & 3;
         w_out[r * k + b * PQ2_0_QK + j] = (float)(code - 1) * d;
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* PTQ1_0: the same trits and scale as PQ2_0, packed in base 3                 */
+/* ------------------------------------------------------------------------ */
+
+/* Byte and trit index of element e of a block (the page's element-order
+ * table): 0-79 are trit e/16 of byte e%16, 80-119 trit (e-80)/8 of byte
+ * 16 + (e-80)%8, 120-127 trit (e-120)/2 of byte 24 + (e-120)%2 (qh). */
+static void ptq1_0_place(int e, int* byte, int* n) {
+  if (e < 80) {
+    *n = e / 16;
+    *byte = e % 16;
+  } else if (e < 120) {
+    *n = (e - 80) / 8;
+    *byte = 16 + (e - 80) % 8;
+  } else {
+    *n = (e - 120) / 2;
+    *byte = 24 + (e - 120) % 2;
+  }
+}
+
+/* q = ceil(256 v / 243), v the five trits read as a base-3 number with the
+ * first trit most significant (a qh byte's missing fifth trit is 0). */
+static uint8_t ptq1_0_byte(const int t[5]) {
+  int v = t[0] * 81 + t[1] * 27 + t[2] * 9 + t[3] * 3 + t[4];
+  return (uint8_t)((256 * v + 242) / 243);
+}
+
+/* trit n of byte q: ((q * 3^n) mod 256) * 3 / 256, rounded down. */
+static int ptq1_0_trit(uint8_t q, int n) {
+  int p = 1;
+  for (int i = 0; i < n; ++i) p *= 3;
+  return ((((int)q * p) & 0xFF) * 3) >> 8;
+}
+
+int orc_ptq1_0_encode_byte(const int32_t* trits) {
+  int t[5];
+  for (int i = 0; i < 5; ++i) t[i] = trits[i];
+  return ptq1_0_byte(t);
+}
+
+int orc_ptq1_0_decode_trit(int32_t q, int32_t n) { return ptq1_0_trit((uint8_t)q, n); }
+
+int orc_ptq1_0_quantize(const float* w_rot, int64_t n, int64_t k, uint8_t* blocks) {
+  if (n < 0 || k <= 0 || k % PTQ1_0_QK != 0) return ORC_ERR_SHAPE;
+  int64_t nb = k / PTQ1_0_QK;
+  for (int64_t i = 0; i < n * k; ++i)
+    if (!isfinite(w_rot[i])) return ORC_ERR_NONFINITE;
+  int status = ORC_OK;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* wb = w_rot + r * k + b * PTQ1_0_QK;
+      uint8_t* out = blocks + (r * nb + b) * PTQ1_0_BYTES;
+      float amax = 0.0f;
+      for (int j = 0; j < PTQ1_0_QK; ++j) {
+        float a = fabsf(wb[j]);
+        if (a > amax) amax = a;
+      }
+      uint16_t dh = orc_half_from_float(amax); /* the PQ2_0 scale: d = max|w| over the group */
+      if ((dh & 0x7C00) == 0x7C00) {
+#pragma omp atomic write
+        status = ORC_ERR_RANGE;
+      }
+      float df = orc_float_from_half(dh);
+      int trits[26][5];
+      memset(trits, 0, sizeof(trits));
+      for (int j = 0; j < PTQ1_0_QK; ++j) {
+        long t = 0;
+        if (df != 0.0f) {
+          t = lround((double)wb[j] / (double)df);
+          if (t > 1) t = 1;
+          if (t < -1) t = -1;
+        }
+        int byte, tn;
+        ptq1_0_place(j, &byte, &tn);
+        trits[byte][tn] = (int)(t + 1);
+      }
+      for (int byte = 0; byte < 26; ++byte) out[byte] = ptq1_0_byte(trits[byte]);
+      out[26] = (uint8_t)(dh & 0xFF); /* the scale comes last */
+      out[27] = (uint8_t)(dh >> 8);
+    }
+  }
+  return status;
+}
+
+int orc_ptq1_0_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out) {
+  if (n < 0 || k <= 0 || k % PTQ1_0_QK != 0) return ORC_ERR_SHAPE;
+  int64_t nb = k / PTQ1_0_QK;
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* blk = blocks + (r * nb + b) * PTQ1_0_BYTES;
+      float d = orc_float_from_half((uint16_t)(blk[26] | (blk[27] << 8)));
+      for (int j = 0; j < PTQ1_0_QK; ++j) {
+        int byte, tn;
+        ptq1_0_place(j, &byte, &tn);
+        w_out[r * k + b * PTQ1_0_QK + j] = (float)(ptq1_0_trit(blk[byte], tn) - 1) * d;
       }
     }
   }

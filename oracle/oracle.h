@@ -63,6 +63,21 @@ int orc_q8_0_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out);
 int orc_pq2_0_quantize(const float* w_rot, int64_t n, int64_t k, uint8_t* blocks);
 int orc_pq2_0_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out);
 
+/* PTQ1_0 ("Bonsai 2 27B", section 3.2): the trits and the fp16 scale of
+ * PQ2_0 (value (t-1)*d, d = max|w|, t = round(w/d) + 1) packed in base 3 into
+ * 28-byte blocks of 128: qs[24] with five trits per byte, qh[2] with four,
+ * then d (last, unlike PQ2_0).  A byte holds q = ceil(256 v / 243), v the
+ * trits as a base-3 number with the first trit most significant (a qh byte's
+ * absent fifth trit taken as 0); trit n is ((q 3^n) mod 256) * 3 / 256,
+ * rounded down.  Element order, from the page's table: 0-79 are trit e/16 of
+ * qs[e%16], 80-119 trit (e-80)/8 of qs[16+(e-80)%8], 120-127 trit (e-120)/2
+ * of qh[(e-120)%2].  w_rot is the already rotated n x k matrix, k % 128 == 0. */
+int orc_ptq1_0_quantize(const float* w_rot, int64_t n, int64_t k, uint8_t* blocks);
+int orc_ptq1_0_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out);
+/* The byte rule and the trit rule on their own (trits: five values 0..2). */
+int orc_ptq1_0_encode_byte(const int32_t* trits);
+int orc_ptq1_0_decode_trit(int32_t q, int32_t n);
+
 /* Unnormalised Sylvester Hadamard matrix, n x n row-major, entries +-1. */
 int orc_hadamard(int32_t n, double* h_out);
 

@@ -360,6 +360,68 @@ def test_ternary_all_ones_block_dots_to_zero_and_all_twos_to_d_sum():
 # GEMV
 # ----------------------------------------------------------------------------
 
+def _ptq1_0_golden():
+    bytes_, blocks = [], []
+    for line in open(os.path.join(GOLDEN, "ptq1_0_bytes.txt")):
+        line = line.split("#")[0].strip()
+        if line.startswith("byte "):
+            lhs, rhs = line[5:].split("=")
+            bytes_.append(([int(t) for t in lhs.split()], int(rhs)))
+        elif line.startswith("block "):
+            head, rest = line[6:].split(":")
+            e, sgn = head.split()
+            diffs = dict((int(a), int(b)) for a, b in (kv.split("=") for kv in rest.split()))
+            blocks.append((int(e), int(sgn), diffs))
+    return bytes_, blocks
+
+
+def test_ptq1_0_byte_rule_from_page_worked_values():
+    bytes_, _ = _ptq1_0_golden()
+    assert len(bytes_) >= 7
+    for trits, q in bytes_:
+        assert oracle.ptq1_0_encode_byte(trits) == q, trits
+
+
+def test_ptq1_0_trit_rule_inverts_the_byte_rule_for_every_byte():
+    """Brute force over all 243 five-trit bytes (and the 81 four-trit qh
+    bytes): the page's trit extraction returns every trit the byte rule
+    packed."""
+    import itertools
+
+    for trits in itertools.product(range(3), repeat=5):
+        q = oracle.ptq1_0_encode_byte(list(trits))
+        assert 0 <= q <= 255
+        assert [oracle.ptq1_0_decode_trit(q, n) for n in range(5)] == list(trits)
+
+
+def test_ptq1_0_single_element_blocks_match_hand_worked_bytes():
+    """The element-order table and the scale's place (last) on hand-built
+    blocks."""
+    _, blocks = _ptq1_0_golden()
+    assert len(blocks) >= 5
+    for e, sgn, diffs in blocks:
+        w = np.zeros((1, 128), dtype=np.float32)
+        w[0, e] = sgn * 2.0 ** -4
+        got = oracle.ptq1_0_quantize(w)[0, 0]
+        want = np.array([128] * 24 + [127, 127, 0x00, 0x2C], dtype=np.uint8)
+        for b, v in diffs.items():
+            want[b] = v
+        assert np.array_equal(got, want), (e, got)
+        deq = oracle.ptq1_0_dequant(got[None, None], 1, 128)
+        assert np.array_equal(deq, w)
+
+
+def test_ptq1_0_is_a_lossless_transcode_of_pq2_0():
+    """Same trits and scale as PQ2_0 (the page: the two packs are lossless
+    transcodes of each other): the dequantized matrices are equal."""
+    w = synth.fill_host("w", 64 * 1024, 3, synth.stream_id("test", 0, 205)).reshape(64, 1024)
+    _, w_rot = oracle.rotate_rows(w)
+    a = oracle.ptq1_0_dequant(oracle.ptq1_0_quantize(w_rot), 64, 1024)
+    b = oracle.pq2_0_dequant(oracle.pq2_0_quantize(w_rot), 64, 1024)
+    assert np.array_equal(a, b)
+    assert oracle.ptq1_0_quantize(w_rot).nbytes * 34 == oracle.pq2_0_quantize(w_rot).nbytes * 28
+
+
 def test_gemv_brute_force_4x128_pq2_0():
     w = synth.fill_host("w", 4 * 128, 9, synth.stream_id("test", 0, 9)).reshape(4, 128)
     x = synth.fill_host("x", 128, 9, synth.stream_id("test", 1, 9))
