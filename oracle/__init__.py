@@ -56,7 +56,7 @@ def lib():
         for name in ("orc_q8_0_quantize", "orc_q8_0_dequant", "orc_pq2_0_quantize", "orc_pq2_0_dequant"):
             getattr(L, name).argtypes = [P, I64, I64, P]
             getattr(L, name).restype = ctypes.c_int
-        for name in ("orc_ptq1_0_quantize", "orc_ptq1_0_dequant"):
+        for name in ("orc_ptq1_0_quantize", "orc_ptq1_0_dequant", "orc_scale4_quantize", "orc_scale4_dequant"):
             getattr(L, name).argtypes = [P, I64, I64, P]
             getattr(L, name).restype = ctypes.c_int
         L.orc_ptq1_0_encode_byte.argtypes = [P]
@@ -157,6 +157,36 @@ def ptq1_0_dequant(blocks, n, k):
     out = np.empty((n, k), dtype=np.float32)
     _check(lib().orc_ptq1_0_dequant(b.ctypes.data, n, k, out.ctypes.data), "ptq1_0_dequant")
     return out
+
+
+def scale4_quantize(w):
+    """scale4_gs32 blocks [n, k/32, 18]."""
+    w = _f32(w)
+    n, k = w.shape
+    out = np.zeros((n, k // 32, 18), dtype=np.uint8)
+    _check(lib().orc_scale4_quantize(w.ctypes.data, n, k, out.ctypes.data), "scale4_quantize")
+    return out
+
+
+def scale4_dequant(blocks, n, k):
+    b = np.ascontiguousarray(blocks, dtype=np.uint8)
+    out = np.empty((n, k), dtype=np.float32)
+    _check(lib().orc_scale4_dequant(b.ctypes.data, n, k, out.ctypes.data), "scale4_dequant")
+    return out
+
+
+def scale4_reference(w, x):
+    """Quantize W to scale4_gs32 and return (blocks, dequantized W, y, absdot)."""
+    w = _f32(w)
+    n, k = w.shape
+    blocks = scale4_quantize(w)
+    deq = scale4_dequant(blocks, n, k)
+    x = np.asarray(x, dtype=np.float32)
+    if x.ndim == 1:
+        y, a = gemv(deq, x.astype(np.float64))
+    else:
+        y, a = gemm(deq, x.astype(np.float64))
+    return blocks, deq, y, a
 
 
 def ptq1_0_encode_byte(trits):
@@ -270,6 +300,8 @@ def pq2_0_reference(w, x):
 def reference(fmt, w, x):
     if fmt == "q8_0":
         return q8_0_reference(w, x)
+    if fmt == "scale4":
+        return scale4_reference(w, x)
     if fmt == "pq2_0":
         return pq2_0_reference(w, x)
     raise OracleError(fmt)

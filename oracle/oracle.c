@@ -86,6 +86,8 @@ uint16_t orc_half_from_float(float x) {
 #define PQ2_0_QK 128
 #define PQ2_0_BYTES 34
 #define PTQ1_0_QK 128
+#define SCALE4_QK 32
+#define SCALE4_BYTES 18 /* fp16 scale, then 16 bytes of nibbles */
 #define PTQ1_0_BYTES 28 /* 24 bytes of five trits, 2 of four trits, then the fp16 scale */
 
 int orc_q8_0_quantize(const float* w, int64_t n, int64_t k, uint8_t* blocks) {
@@ -299,6 +301,65 @@ int orc_ptq1_0_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out
         int byte, tn;
         ptq1_0_place(j, &byte, &tn);
         w_out[r * k + b * PTQ1_0_QK + j] = (float)(ptq1_0_trit(blk[byte], tn) - 1) * d;
+      }
+    }
+  }
+  return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* scale4_gs32: symmetric 4-bit with an implicit zero point of 8              */
+/* ------------------------------------------------------------------------ */
+
+int orc_scale4_quantize(const float* w, int64_t n, int64_t k, uint8_t* blocks) {
+  if (n < 0 || k <= 0 || k % SCALE4_QK != 0) return ORC_ERR_SHAPE;
+  int64_t nb = k / SCALE4_QK;
+  for (int64_t i = 0; i < n * k; ++i)
+    if (!isfinite(w[i])) return ORC_ERR_NONFINITE;
+  int status = ORC_OK;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* wb = w + r * k + b * SCALE4_QK;
+      uint8_t* out = blocks + (r * nb + b) * SCALE4_BYTES;
+      /* the weight of largest magnitude, with its sign (the first on a tie) */
+      float m = 0.0f;
+      for (int j = 0; j < SCALE4_QK; ++j)
+        if (fabsf(wb[j]) > fabsf(m)) m = wb[j];
+      float d = m / -8.0f; /* fp32 quotient, then fp16 */
+      uint16_t dh = orc_half_from_float(d);
+      if ((dh & 0x7C00) == 0x7C00) {
+#pragma omp atomic write
+        status = ORC_ERR_RANGE;
+      }
+      float df = orc_float_from_half(dh); /* quantize against the fp16-rounded scale */
+      memset(out, 0, SCALE4_BYTES);
+      out[0] = (uint8_t)(dh & 0xFF);
+      out[1] = (uint8_t)(dh >> 8);
+      for (int j = 0; j < SCALE4_QK; ++j) {
+        long q = 8;
+        if (df != 0.0f) {
+          q = lround((double)wb[j] / (double)df) + 8;
+          if (q > 15) q = 15;
+          if (q < 0) q = 0;
+        }
+        out[2 + j / 2] |= (uint8_t)(q << (4 * (j % 2)));
+      }
+    }
+  }
+  return status;
+}
+
+int orc_scale4_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out) {
+  if (n < 0 || k <= 0 || k % SCALE4_QK != 0) return ORC_ERR_SHAPE;
+  int64_t nb = k / SCALE4_QK;
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const uint8_t* blk = blocks + (r * nb + b) * SCALE4_BYTES;
+      float d = orc_float_from_half((uint16_t)(blk[0] | (blk[1] << 8)));
+      for (int j = 0; j < SCALE4_QK; ++j) {
+        int q = (blk[2 + j / 2] >> (4 * (j % 2))) & 15;
+        w_out[r * k + b * SCALE4_QK + j] = (float)(q - 8) * d;
       }
     }
   }

@@ -78,6 +78,19 @@ int orc_ptq1_0_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out
 int orc_ptq1_0_encode_byte(const int32_t* trits);
 int orc_ptq1_0_decode_trit(int32_t q, int32_t n);
 
+/* scale4_gs32 ("Kipp Benchmarks", section "Scale-only 4-bit (scale4_gs32)"):
+ * 32-weight groups of 16 packed nibbles plus one fp16 scale (18 bytes,
+ * 4.5 bits per weight), w = d (q - 8), q in 0..15; the converter takes the
+ * weight of largest magnitude m with its sign and d = m / -8 (Q4_0-class),
+ * and quantizes against the fp16-rounded scale.  Readings where the page is
+ * silent: the fp32 quotient m / -8 rounded to fp16 to nearest even; the first
+ * weight on a tie of magnitudes; q = round-half-away-from-zero(w / d) + 8
+ * clamped to [0, 15]; a group whose fp16 scale is zero gets q = 8; the scale
+ * first (bytes 0-1, little endian), then element j in byte 2 + j/2 at bit
+ * offset 4 (j % 2), the same nibble order rule as the PQ2_0 crumbs. */
+int orc_scale4_quantize(const float* w, int64_t n, int64_t k, uint8_t* blocks);
+int orc_scale4_dequant(const uint8_t* blocks, int64_t n, int64_t k, float* w_out);
+
 /* Unnormalised Sylvester Hadamard matrix, n x n row-major, entries +-1. */
 int orc_hadamard(int32_t n, double* h_out);
 

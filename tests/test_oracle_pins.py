@@ -422,6 +422,68 @@ def test_ptq1_0_is_a_lossless_transcode_of_pq2_0():
     assert oracle.ptq1_0_quantize(w_rot).nbytes * 34 == oracle.pq2_0_quantize(w_rot).nbytes * 28
 
 
+def _scale4_golden():
+    cases = []
+    for line in open(os.path.join(GOLDEN, "scale4_bytes.txt")):
+        if line.startswith("#") or "|" not in line:
+            continue
+        head, hx = line.split("|")
+        name, spec = head.split(":", 1)
+        w = np.zeros(32, dtype=np.float32)
+        for kv in spec.split()[1:]:
+            j, v = kv.split(":")
+            w[int(j)] = float(v) * 2.0 ** -7
+        cases.append((name.strip(), w, bytes.fromhex(hx.strip())))
+    return cases
+
+
+def test_scale4_hand_worked_blocks():
+    cases = _scale4_golden()
+    assert len(cases) == 5
+    for name, w, want in cases:
+        got = oracle.scale4_quantize(w[None])[0, 0]
+        assert bytes(got) == want, (name, bytes(got).hex())
+
+
+def test_scale4_round_trip_of_grid_weights_is_exact():
+    """w = d (q - 8) with d = -2^-7 and the extreme q = 0 present: the
+    quantizer recovers every q and the dequantized block equals w."""
+    rng = np.random.default_rng(12)
+    for _ in range(20):
+        q = rng.integers(1, 16, size=32)
+        q[rng.integers(0, 32)] = 0
+        w = ((q - 8) * -(2.0 ** -7)).astype(np.float32)[None]
+        blocks = oracle.scale4_quantize(w)
+        assert np.array_equal(oracle.scale4_dequant(blocks, 1, 32), w)
+
+
+def test_scale4_dequant_error_bound_and_range():
+    w = synth.fill_host("w", 16 * 1024, 4, synth.stream_id("test", 0, 206)).reshape(16, 1024)
+    blocks = oracle.scale4_quantize(w)
+    deq = oracle.scale4_dequant(blocks, 16, 1024)
+    bits = blocks.reshape(-1, 18)[:, 0].astype(np.uint16) | (blocks.reshape(-1, 18)[:, 1].astype(np.uint16) << 8)
+    d = np.abs(oracle.half_value(bits)).repeat(32)
+    err = np.abs(deq.reshape(-1) - w.reshape(-1))
+    # half a step, or one step for the one clamped value (q - 8 = +8 -> +7)
+    assert np.all(err <= d * (1 + 2 ** -10) + 1e-12)
+    assert np.mean(err <= d / 2 * (1 + 2 ** -10)) > 0.99
+    with pytest.raises(oracle.OracleError):
+        oracle.scale4_quantize(np.full((1, 32), 6e5, dtype=np.float32))  # |d| = 6e5/8 overflows fp16
+    with pytest.raises(oracle.OracleError):
+        oracle.scale4_quantize(np.zeros((1, 48), dtype=np.float32))
+
+
+def test_gemv_brute_force_4x128_scale4():
+    rng = np.random.default_rng(13)
+    w = (rng.standard_normal((4, 128)) * 0.02).astype(np.float32)
+    x = rng.standard_normal(128).astype(np.float32)
+    _, deq, y, a = oracle.scale4_reference(w, x)
+    for i in range(4):
+        want = sum(float(deq[i, j]) * float(x[j]) for j in range(128))
+        assert abs(y[i] - want) <= 1e-12 * sum(abs(float(deq[i, j]) * float(x[j])) for j in range(128))
+        assert abs(a[i] - sum(abs(float(deq[i, j]) * float(x[j])) for j in range(128))) <= 1e-12 * a[i]
+
+
 def test_gemv_brute_force_4x128_pq2_0():
     w = synth.fill_host("w", 4 * 128, 9, synth.stream_id("test", 0, 9)).reshape(4, 128)
     x = synth.fill_host("x", 128, 9, synth.stream_id("test", 1, 9))
