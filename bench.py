@@ -175,10 +175,11 @@ def aggregate_gbs(bytes_per_step, steps, seconds_max, world):
     return bytes_per_step * steps * world / seconds_max / 1e9
 
 
-def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None, world=1, limit=None):
+def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None, world=1, limit=None, linked=False,
+                    e2e=True):
     import torch
 
-    W = wl_mod.DecodeWorkload(config, seed=0, limit=limit)
+    W = wl_mod.DecodeWorkload(config, seed=0, limit=limit, linked=linked)
     bytes_per_step = W.weight_bytes + W.activation_bytes
     for _ in range(warmup):
         W.step(stream)
@@ -201,6 +202,15 @@ def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None,
     if kq.kq_device_status(True) != kq.KQ_OK:
         raise RuntimeError("device status not ok after the timed region")
     per_step = secs / steps
+    if not e2e:
+        out = {"config": config, "matrices": len(W.mats_spec), "weight_bytes": W.weight_bytes,
+               "bytes_per_step": bytes_per_step, "seconds": secs, "per_step_s": per_step,
+               "gbs": bytes_per_step / per_step / 1e9, "stages": W.plan.stages,
+               "split_matrices": W.plan.split_matrices}
+        W.close()
+        del W
+        torch.cuda.empty_cache()
+        return out
     # end to end: activations from pinned host memory, outputs back to pinned host memory
     xh = torch.empty(W.x.numel(), dtype=torch.float32, pin_memory=True)
     xh.copy_(W.x.cpu())
@@ -359,6 +369,17 @@ def run_kq(args):
             "frac_of_measured_hbm": round(sec["gbs"] / peak, 4),
             "frac_of_control": round(sec["gbs"] / control["gbs"], 4), "e2e_gbs": round(sec["e2e_gbs"], 1),
             "weight_bytes": sec["weight_bytes"], "matrices": sec["matrices"]}}
+        # the same projections with the model's dependencies: stage by stage
+        # (q/k/v -> o -> gate/up -> down -> next layer), one cooperative launch
+        chain = {}
+        for cfg in (HEADLINE, SECONDARY):
+            ch = _decode_measure(kq, workloads, cfg, max(3, args.steps // 4), args.warmup, stream, linked=True,
+                                 e2e=False)
+            chain[cfg] = {"gbs": round(ch["gbs"], 1), "us_per_step": round(ch["per_step_s"] * 1e6, 2),
+                          "frac_of_measured_hbm": round(ch["gbs"] / peak, 4),
+                          "frac_of_control": round(ch["gbs"] / control["gbs"], 4), "stages": ch["stages"],
+                          "split_matrices": ch["split_matrices"], "matrices": ch["matrices"]}
+        extras["decode_chain"] = chain
         gemv = []
         for fmt, n, k, m in (("q8_0", 1024, 2560, 1), ("pq2_0", 10240, 5120, 1), ("q8_0", 9728, 2560, 1),
                              ("q8_0", 9728, 2560, 4), ("q8_0", 9728, 2560, 16), ("q8_0", 9728, 2560, 64),

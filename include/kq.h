@@ -16,10 +16,13 @@
  *          q in {0,1,2}, element j in byte j/4 at bit offset 2*(j%4), value
  *          (q-1)*d, d = max|w| and q = round(w/d)+1 ("Bonsai 2 27B - ternary
  *          g128 + blockwise Hadamard", section 3.1).  The weights are stored
- *          rotated, W' = W R^T with R = H_128/sqrt(128) applied block-diagonally
- *          along K (same page, sections 4.1-4.2, with n = 128 and no sign
- *          vector), so the activation gets x' = R x before the product; the
- *          PQ2_0 GEMV takes the UNROTATED x and applies R itself.
+ *          rotated, W' = W R^T with R = H_n S / sqrt(n) applied
+ *          block-diagonally along K (same page, sections 4.1-4.2): n = 128
+ *          with S = I (the default), or the page's own n = 1024 with a +-1
+ *          sign per position of K (S = diag(signs), one sign vector per K
+ *          width).  The activation gets x' = R x (sign flip, then the
+ *          transform) before the product; the PQ2_0 GEMV takes the UNROTATED
+ *          x and applies R itself.
  *
  * Conventions.
  *  - Every function returns a kq_status (int); 0 is success.  On failure
@@ -67,10 +70,18 @@ typedef enum {
   KQ_ERR_UNSUPPORTED = 9  /* device or combination of arguments not supported      */
 } kq_status;
 
-typedef enum { KQ_Q8_0 = 0, KQ_PQ2_0 = 1 } kq_format;
+/* KQ_PTQ1_0 is a storage format only ("Bonsai 2 27B", section 3.2: the
+ * PQ2_0 trits and scale packed in base 3, 28 bytes per 128 weights, 1.75
+ * bits per weight; the page ships it as a download option and unpacks it to
+ * the PQ2_0 words at load time).  kq_prepare turns PTQ1_0 blocks into PQ2_0
+ * planes; every GEMV runs on those. */
+typedef enum { KQ_Q8_0 = 0, KQ_PQ2_0 = 1, KQ_PTQ1_0 = 2 } kq_format;
 
 /* A quantized matrix resident in device memory (planes as described above).
- * had_block is the Hadamard block of the fold: 128 for PQ2_0, 0 for Q8_0. */
+ * had_block is the Hadamard block n of the fold: 128 or 1024 for PQ2_0 (k a
+ * multiple of it), 0 for Q8_0.  signs (PQ2_0 only) is NULL for S = I, or k
+ * int8 entries, each +1 or -1, in 16-byte-aligned device memory owned by
+ * the caller (matrices of one K width share one vector on the page). */
 typedef struct {
   int32_t fmt;
   int32_t had_block;
@@ -78,6 +89,7 @@ typedef struct {
   int64_t k;
   const void* codes;
   const void* scales;
+  const int8_t* signs;
 } kq_qmat;
 
 /* ---- status and layout ---------------------------------------------------- */
@@ -88,9 +100,11 @@ const char* kq_last_error(void);
 /* ABI version, bumped on incompatible change. */
 int kq_version(void);
 
-/* Weights per block: 32 (Q8_0) or 128 (PQ2_0); 0 for an unknown format. */
+/* Weights per block: 32 (Q8_0) or 128 (PQ2_0, PTQ1_0); 0 for an unknown format. */
 int64_t kq_block_size(int fmt);
-/* Bytes of one 34-byte block times the number of blocks of an n x k matrix. */
+/* Bytes of one block (34 for Q8_0 and PQ2_0, 28 for PTQ1_0) times the number
+ * of blocks of an n x k matrix.  The plane queries below give, for PTQ1_0,
+ * the PQ2_0 planes kq_prepare writes. */
 int64_t kq_blocks_bytes(int fmt, int64_t n, int64_t k);
 /* Row stride of the scales plane in fp16 elements: k/block rounded up to 8. */
 int64_t kq_scale_stride(int fmt, int64_t k);
@@ -112,6 +126,16 @@ int kq_quantize_q8_0(const float* w, int64_t n, int64_t k, void* blocks);
  * Errors: KQ_ERR_SHAPE (k % 128), KQ_ERR_NONFINITE, KQ_ERR_RANGE. */
 int kq_quantize_pq2_0(const float* w_rot, int64_t n, int64_t k, void* blocks);
 
+/* PTQ1_0 per row and 128-block of the ROTATED weights: the PQ2_0 scale and
+ * trits (same rules as kq_quantize_pq2_0) packed in base 3: 24 bytes of five
+ * trits, 2 bytes of four, then the fp16 scale (28 bytes).  A byte holds
+ * ceil(256 v / 243), v its trits as a base-3 number with the first trit most
+ * significant (a four-trit byte's fifth trit is 0).  Element e is trit e/16
+ * of byte e%16 for e < 80, trit (e-80)/8 of byte 16+(e-80)%8 for e < 120,
+ * trit (e-120)/2 of byte 24+(e-120)%2 above (the page's element-order table).
+ * Errors: KQ_ERR_SHAPE (k % 128), KQ_ERR_NONFINITE, KQ_ERR_RANGE. */
+int kq_quantize_ptq1_0(const float* w_rot, int64_t n, int64_t k, void* blocks);
+
 /* Blockwise normalised Walsh-Hadamard transform of each row, on the host:
  * out[b*block + i] = (1/sqrt(block)) * sum_c H[i][c] in[b*block + c], with the
  * sum taken in FP64, one FP64 multiply, one rounding to fp32.  block is a
@@ -120,8 +144,10 @@ int kq_hadamard_blockwise_host(const float* in, float* out, int64_t rows, int64_
 
 /* ---- device weight preparation ------------------------------------------- */
 
-/* Repack n*k/block AoS blocks (device memory, 34-byte blocks as produced by
- * the host quantizers) into the codes and scales planes. */
+/* Repack n*k/block AoS blocks (device memory, as produced by the host
+ * quantizers) into the codes and scales planes.  fmt = KQ_PTQ1_0 reads
+ * 28-byte PTQ1_0 blocks and writes the PQ2_0 planes of the same trits and
+ * scales (a lossless transcode; the matrix is then a PQ2_0 matrix). */
 int kq_prepare(int fmt, const void* d_blocks, int64_t n, int64_t k, void* d_codes, void* d_scales, void* stream);
 
 /* Quantize an n x k fp32 matrix in device memory straight into planes, with
@@ -140,6 +166,20 @@ int kq_dequantize(const kq_qmat* W, float* d_out, void* stream);
  * same arithmetic as kq_hadamard_blockwise_host (FP64 butterflies, one FP64
  * multiply, one rounding), bit-identical to it.  d_in == d_out is allowed. */
 int kq_hadamard_blockwise(const float* d_in, float* d_out, int64_t rows, int64_t k, int32_t block, void* stream);
+
+/* The page's rotation R = H_n S / sqrt(n) of each row, block-diagonal along
+ * K (the Bonsai page, sections 4.1-4.2): out = (1/sqrt(n)) H_n (s * in) per
+ * n-block, the sign flip exact, then the same FP64 butterflies, one FP64
+ * multiply and one rounding as above (so the host and device versions are
+ * bit-identical).  signs: k int8 entries, +1 or -1 (host memory for the
+ * host version, device memory for the device one), or NULL for S = I.
+ * Used offline to fold the rotation into weights (W' = W R^T: each row
+ * w' = R w) before quantizing to PQ2_0.  block: a power of two dividing k,
+ * up to 4096. */
+int kq_rotate_blockwise_host(const float* in, float* out, int64_t rows, int64_t k, int32_t block,
+                             const int8_t* signs);
+int kq_rotate_blockwise(const float* d_in, float* d_out, int64_t rows, int64_t k, int32_t block,
+                        const int8_t* d_signs, void* stream);
 
 /* ---- GEMV / small-M GEMM --------------------------------------------------- */
 
@@ -227,10 +267,66 @@ typedef struct kq_plan kq_plan;
 int kq_decode_plan_create(const kq_qmat* mats, int64_t count, kq_plan** out);
 /* Total packed activation / output lengths in floats, and weight bytes. */
 int kq_decode_plan_sizes(const kq_plan* plan, int64_t* x_floats, int64_t* y_floats, int64_t* weight_bytes);
+/* Workspace bytes of kq_decode_step (0 for a plan made by kq_decode_plan_create). */
 size_t kq_decode_workspace_bytes(const kq_plan* plan);
 int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, void* d_ws, size_t ws_bytes,
                    void* stream);
 void kq_decode_plan_destroy(kq_plan* plan);
+
+/* Decode plans with the dependencies of a real decode step.  In a model's
+ * decode the projections of a layer read activations produced by earlier
+ * projections: q, k and v (or gate and up) read one shared input, o reads
+ * what attention made of q, the FFN reads what the block made of o, the next
+ * layer reads the FFN's output.  The Bonsai 2 27B page memoises one
+ * transform per activation site, shared by q/k/v and by gate/up (sections
+ * 4.2 and 7), and counts the cost of dispatching the dependent layer chain
+ * one kernel at a time (sections 8.6-8.7).  A
+ * linked plan states, per matrix, where its activation comes from and which
+ * stage it belongs to; kq_decode_step then runs the whole list in one
+ * cooperative persistent launch in which a matrix starts its arithmetic
+ * only after the matrices it depends on have written their outputs, while
+ * the weight stream keeps running ahead across stage boundaries.
+ *
+ * The operations between projections that are not projections (attention,
+ * normalisation, activation functions, residual adds) are outside this
+ * library; the plainest stand-in is kept: the activation of a dependent
+ * matrix is alpha times a prefix of an earlier matrix's output. */
+typedef enum {
+  KQ_SRC_PACKED = 0,    /* a fresh slot of d_x_packed, in list order over the matrices with this kind */
+  KQ_SRC_INPUT_OF = 1,  /* the same activation as matrix `of` (k equal): a grouped matvec */
+  KQ_SRC_OUTPUT_OF = 2  /* x[i] = fp32(alpha * y_of[i]), i < k <= n_of; stage of `of` < this stage */
+} kq_src_kind;
+
+typedef struct {
+  int32_t src;   /* kq_src_kind */
+  int32_t stage; /* >= 0, nondecreasing along the list */
+  int64_t of;    /* an earlier matrix (index < this one) for KQ_SRC_INPUT_OF / KQ_SRC_OUTPUT_OF */
+  float alpha;   /* KQ_SRC_OUTPUT_OF: finite scale of the successor activation; else ignored */
+  int32_t reserved; /* 0 */
+} kq_link;
+
+/* Creates a linked plan: count matrices of one format with one link each.
+ *  - Every matrix writes its output to d_y_packed at offset sum_{j<i} n_j
+ *    (all of them, also those read by later stages).  d_x_packed holds only
+ *    the KQ_SRC_PACKED activations, in list order.
+ *  - Stages with fewer 128-/256-row blocks than the GPU has SMs split K;
+ *    the partial sums live in the step's workspace, and every reader (the
+ *    dependent matrices' activation staging and the final write of y) adds
+ *    them in split order, so results stay deterministic.
+ *  - Matrices that share one activation (KQ_SRC_INPUT_OF) share its
+ *    staged, transformed copy inside each CTA (the transform memo): a CTA
+ *    that goes on to an item of another matrix of the group with the same K
+ *    range does not stage or transform the activation again.
+ *  - Errors: KQ_ERR_INVALID_ARG (NULL, unknown kind, `of` not earlier,
+ *    non-finite alpha, reserved != 0), KQ_ERR_SHAPE (k mismatch of a link,
+ *    decreasing stage, an output read in its own or a later stage),
+ *    KQ_ERR_UNSUPPORTED (mixed formats, k above the staging limit), KQ_ERR_CUDA.
+ * kq_decode_workspace_bytes gives the step's workspace (stage counters and
+ * split partials); kq_decode_step runs it.  Steps of one plan that share a
+ * workspace must be ordered (one stream). */
+int kq_decode_plan_create_linked(const kq_qmat* mats, const kq_link* links, int64_t count, kq_plan** out);
+/* Number of stages of a plan and of matrices whose K is split. */
+int kq_decode_plan_stages(const kq_plan* plan, int32_t* stages, int32_t* split_matrices);
 
 /* ---- read-only streaming control -------------------------------------------- */
 

@@ -38,7 +38,8 @@ KQ_ERR_UNSUPPORTED = 9
 
 KQ_Q8_0 = 0
 KQ_PQ2_0 = 1
-FORMATS = {"q8_0": KQ_Q8_0, "pq2_0": KQ_PQ2_0}
+KQ_PTQ1_0 = 2  # storage format: kq_prepare transcodes it to PQ2_0 planes
+FORMATS = {"q8_0": KQ_Q8_0, "pq2_0": KQ_PQ2_0, "ptq1_0": KQ_PTQ1_0}
 
 
 class KQError(RuntimeError):
@@ -50,7 +51,18 @@ class KQError(RuntimeError):
 
 class kq_qmat(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int32), ("had_block", ctypes.c_int32), ("n", ctypes.c_int64),
-                ("k", ctypes.c_int64), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p)]
+                ("k", ctypes.c_int64), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("signs", ctypes.c_void_p)]
+
+
+KQ_SRC_PACKED = 0
+KQ_SRC_INPUT_OF = 1
+KQ_SRC_OUTPUT_OF = 2
+
+
+class kq_link(ctypes.Structure):
+    _fields_ = [("src", ctypes.c_int32), ("stage", ctypes.c_int32), ("of", ctypes.c_int64),
+                ("alpha", ctypes.c_float), ("reserved", ctypes.c_int32)]
 
 
 _P = ctypes.c_void_p
@@ -71,12 +83,15 @@ SIGNATURES = {
     "kq_scales_bytes": (_I64, [ctypes.c_int, _I64, _I64]),
     "kq_quantize_q8_0": (ctypes.c_int, [_P, _I64, _I64, _P]),
     "kq_quantize_pq2_0": (ctypes.c_int, [_P, _I64, _I64, _P]),
+    "kq_quantize_ptq1_0": (ctypes.c_int, [_P, _I64, _I64, _P]),
     "kq_hadamard_blockwise_host": (ctypes.c_int, [_P, _P, _I64, _I64, _I32]),
     "kq_prepare": (ctypes.c_int, [ctypes.c_int, _P, _I64, _I64, _P, _P, _P]),
     "kq_quantize_q8_0_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "kq_quantize_pq2_0_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "kq_dequantize": (ctypes.c_int, [_QP, _P, _P]),
     "kq_hadamard_blockwise": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _P]),
+    "kq_rotate_blockwise_host": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _P]),
+    "kq_rotate_blockwise": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _P, _P]),
     "kq_gemv_workspace_bytes": (_SZ, [_QP, _I64]),
     "kq_gemv_q8_0": (ctypes.c_int, [_QP, _P, _P, _P, _SZ, _P]),
     "kq_gemv_pq2_0": (ctypes.c_int, [_QP, _P, _P, _P, _SZ, _P]),
@@ -88,6 +103,8 @@ SIGNATURES = {
     "kq_gemm_splitk_noalloc": (ctypes.c_int, [_QP, _P, _I64, _P, _I32, _P]),
     "kq_gemm_splitk_noalloc_max_bytes": (_SZ, []),
     "kq_decode_plan_create": (ctypes.c_int, [_QP, _I64, ctypes.POINTER(_P)]),
+    "kq_decode_plan_create_linked": (ctypes.c_int, [_QP, ctypes.POINTER(kq_link), _I64, ctypes.POINTER(_P)]),
+    "kq_decode_plan_stages": (ctypes.c_int, [_P, ctypes.POINTER(_I32), ctypes.POINTER(_I32)]),
     "kq_decode_plan_sizes": (ctypes.c_int, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "kq_decode_workspace_bytes": (_SZ, [_P]),
     "kq_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _SZ, _P]),
@@ -177,6 +194,14 @@ def kq_quantize_pq2_0(w_rot):
     return out[: n * (k // 128) * 34].reshape(n, k // 128, 34)
 
 
+def kq_quantize_ptq1_0(w_rot):
+    w = np.ascontiguousarray(w_rot, dtype=np.float32)
+    n, k = w.shape
+    out = np.zeros(max(kq_blocks_bytes("ptq1_0", n, k), 1), dtype=np.uint8)
+    _check(_lib.kq_quantize_ptq1_0(w.ctypes.data, n, k, out.ctypes.data), "kq_quantize_ptq1_0")
+    return out[: n * (k // 128) * 28].reshape(n, k // 128, 28)
+
+
 def kq_hadamard_blockwise_host(x, block=128):
     x = np.ascontiguousarray(x, dtype=np.float32)
     x2 = x.reshape(-1, x.shape[-1])
@@ -190,9 +215,11 @@ def kq_hadamard_blockwise_host(x, block=128):
 
 class QMatrix:
     """A quantized matrix in device memory: torch tensors for the codes and
-    scales planes plus the kq_qmat descriptor that points at them."""
+    scales planes plus the kq_qmat descriptor that points at them.  PQ2_0
+    takes the rotation block (128, or the page's 1024) and an optional int8
+    device tensor of k signs (kept referenced here)."""
 
-    def __init__(self, fmt, n, k, device="cuda"):
+    def __init__(self, fmt, n, k, device="cuda", had_block=None, signs=None):
         import torch
 
         self.fmt = _fmt(fmt)
@@ -203,8 +230,12 @@ class QMatrix:
             raise KQError(KQ_ERR_SHAPE, f"QMatrix({fmt}, {n}, {k})")
         self.codes = torch.empty(cb, dtype=torch.uint8, device=device)
         self.scales = torch.empty(sb // 2, dtype=torch.int16, device=device)
-        self.desc = kq_qmat(self.fmt, 128 if self.fmt == KQ_PQ2_0 else 0, self.n, self.k, self.codes.data_ptr(),
-                            self.scales.data_ptr())
+        if had_block is None:
+            had_block = 128 if self.fmt == KQ_PQ2_0 else 0
+        self.had_block = int(had_block)
+        self.signs = signs
+        self.desc = kq_qmat(self.fmt, self.had_block, self.n, self.k, self.codes.data_ptr(),
+                            self.scales.data_ptr(), None if signs is None else signs.data_ptr())
 
     @property
     def nbytes(self):
@@ -216,8 +247,11 @@ class QMatrix:
         return self.codes.numel() + self.n * (self.k // kq_block_size(self.fmt)) * 2
 
 
-def kq_prepare(W, d_blocks, stream=None):
-    _check(_lib.kq_prepare(W.fmt, _ptr(d_blocks), W.n, W.k, W.codes.data_ptr(), W.scales.data_ptr(), _stream(stream)),
+def kq_prepare(W, d_blocks, stream=None, block_fmt=None):
+    """Blocks (device memory) -> W's planes; block_fmt="ptq1_0" transcodes
+    PTQ1_0 blocks into a PQ2_0 matrix."""
+    fmt = W.fmt if block_fmt is None else _fmt(block_fmt)
+    _check(_lib.kq_prepare(fmt, _ptr(d_blocks), W.n, W.k, W.codes.data_ptr(), W.scales.data_ptr(), _stream(stream)),
            "kq_prepare")
 
 
@@ -238,6 +272,21 @@ def kq_dequantize(W, d_out, stream=None):
 def kq_hadamard_blockwise(d_in, d_out, rows, k, block=128, stream=None):
     _check(_lib.kq_hadamard_blockwise(_ptr(d_in), _ptr(d_out), rows, k, block, _stream(stream)),
            "kq_hadamard_blockwise")
+
+
+def kq_rotate_blockwise(d_in, d_out, rows, k, block, d_signs=None, stream=None):
+    _check(_lib.kq_rotate_blockwise(_ptr(d_in), _ptr(d_out), rows, k, block, _ptr(d_signs), _stream(stream)),
+           "kq_rotate_blockwise")
+
+
+def kq_rotate_blockwise_host(x, block, signs=None):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    x2 = x.reshape(-1, x.shape[-1])
+    out = np.empty_like(x2)
+    sg = None if signs is None else np.ascontiguousarray(signs, dtype=np.int8)
+    _check(_lib.kq_rotate_blockwise_host(x2.ctypes.data, out.ctypes.data, x2.shape[0], x2.shape[1], block,
+                                         None if sg is None else sg.ctypes.data), "kq_rotate_blockwise_host")
+    return out.reshape(x.shape)
 
 
 def kq_gemv_workspace_bytes(W, m=1):
@@ -316,14 +365,26 @@ def kq_device_status(clear=True):
 
 
 class DecodePlan:
-    """kq_decode_plan_create / kq_decode_step / kq_decode_plan_destroy."""
+    """kq_decode_plan_create (or, with links, kq_decode_plan_create_linked) /
+    kq_decode_step / kq_decode_plan_destroy.  links: one (src, stage, of,
+    alpha) tuple per matrix."""
 
-    def __init__(self, mats):
+    def __init__(self, mats, links=None):
         self.mats = list(mats)
         arr = (kq_qmat * len(self.mats))(*[m.desc for m in self.mats])
         h = ctypes.c_void_p()
-        _check(_lib.kq_decode_plan_create(arr, len(self.mats), ctypes.byref(h)), "kq_decode_plan_create")
+        if links is None:
+            _check(_lib.kq_decode_plan_create(arr, len(self.mats), ctypes.byref(h)), "kq_decode_plan_create")
+        else:
+            links = list(links)
+            la = (kq_link * len(links))(*[kq_link(int(src), int(stage), int(of), float(alpha), 0)
+                                          for src, stage, of, alpha in links])
+            _check(_lib.kq_decode_plan_create_linked(arr, la, len(links), ctypes.byref(h)),
+                   "kq_decode_plan_create_linked")
         self.handle = h
+        st, ns = _I32(), _I32()
+        _check(_lib.kq_decode_plan_stages(h, ctypes.byref(st), ctypes.byref(ns)), "kq_decode_plan_stages")
+        self.stages, self.split_matrices = st.value, ns.value
         xf, yf, wb = _I64(), _I64(), _I64()
         _check(_lib.kq_decode_plan_sizes(h, ctypes.byref(xf), ctypes.byref(yf), ctypes.byref(wb)),
                "kq_decode_plan_sizes")

@@ -39,11 +39,18 @@ int check_qmat(const kq_qmat* W, int expect_fmt) {
   int64_t bs = block_of(W->fmt);
   if (W->k < bs || W->k % bs != 0)
     return fail(KQ_ERR_SHAPE, "k = %lld is not a positive multiple of %lld", (long long)W->k, (long long)bs);
-  int want_had = W->fmt == KQ_PQ2_0 ? 128 : 0;
-  if (W->had_block != want_had)
-    return fail(KQ_ERR_UNSUPPORTED, "had_block = %d (this format needs %d)", W->had_block, want_had);
+  if (W->fmt == KQ_PQ2_0) {
+    if (W->had_block != 128 && W->had_block != 1024)
+      return fail(KQ_ERR_UNSUPPORTED, "had_block = %d (PQ2_0 takes 128 or 1024)", W->had_block);
+    if (W->k % W->had_block != 0)
+      return fail(KQ_ERR_SHAPE, "k = %lld is not a multiple of had_block = %d", (long long)W->k, W->had_block);
+  } else {
+    if (W->had_block != 0) return fail(KQ_ERR_UNSUPPORTED, "had_block = %d (Q8_0 takes 0)", W->had_block);
+    if (W->signs) return fail(KQ_ERR_UNSUPPORTED, "signs given for a Q8_0 matrix");
+  }
   if (!W->codes || !W->scales) return fail(KQ_ERR_INVALID_ARG, "NULL plane pointer");
   if (!aligned16(W->codes) || !aligned16(W->scales)) return fail(KQ_ERR_ALIGNMENT, "plane not 16-byte aligned");
+  if (W->signs && !aligned16(W->signs)) return fail(KQ_ERR_ALIGNMENT, "signs not 16-byte aligned");
   return KQ_OK;
 }
 
@@ -71,14 +78,14 @@ const char* kq_status_string(int s) {
 
 const char* kq_last_error(void) { return g_last_error; }
 
-int kq_version(void) { return 1; }
+int kq_version(void) { return 2; }
 
 int64_t kq_block_size(int fmt) { return block_of(fmt); }
 
 int64_t kq_blocks_bytes(int fmt, int64_t n, int64_t k) {
   int64_t bs = block_of(fmt);
   if (!bs || n < 0 || k < 0 || k % bs) return 0;
-  return n * (k / bs) * 34;
+  return n * (k / bs) * block_bytes(fmt);
 }
 
 int64_t kq_scale_stride(int fmt, int64_t k) {
@@ -192,23 +199,91 @@ int kq_quantize_pq2_0(const float* w_rot, int64_t n, int64_t k, void* blocks) {
   return KQ_OK;
 }
 
+// PTQ1_0: the PQ2_0 scale and trits, then the base-3 packing.
+static void ptq1_0_place(int e, int* byte, int* n) {
+  if (e < 80) {
+    *byte = e % 16;
+    *n = e / 16;
+  } else if (e < 120) {
+    *byte = 16 + (e - 80) % 8;
+    *n = (e - 80) / 8;
+  } else {
+    *byte = 24 + (e - 120) % 2;
+    *n = (e - 120) / 2;
+  }
+}
+
+int kq_quantize_ptq1_0(const float* w_rot, int64_t n, int64_t k, void* blocks) {
+  clear_error();
+  if (int s = check_host_weights(w_rot, n, k, 128, blocks)) return s;
+  const int64_t nb = k / 128;
+  // the scales first, so that a range error leaves the output untouched
+  std::vector<uint16_t> dh(static_cast<size_t>(n * nb));
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* src = w_rot + r * k + b * 128;
+      float amax = 0.f;
+      for (int j = 0; j < 128; ++j) amax = std::fmax(amax, std::fabs(src[j]));
+      uint16_t h = half_bits_rn(amax);
+      if ((h & 0x7C00u) == 0x7C00u)
+        return fail(KQ_ERR_RANGE, "row %lld block %lld: scale %g overflows fp16", (long long)r, (long long)b,
+                    (double)amax);
+      dh[static_cast<size_t>(r * nb + b)] = h;
+    }
+  }
+  uint8_t* out = static_cast<uint8_t*>(blocks);
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* src = w_rot + r * k + b * 128;
+      uint8_t* blk = out + (r * nb + b) * 28;
+      const uint16_t h = dh[static_cast<size_t>(r * nb + b)];
+      const double d = half_to_float(h);
+      int v[26] = {0};  // each byte's trits as a base-3 number, first trit most significant
+      int trits[26][5] = {};
+      for (int j = 0; j < 128; ++j) {
+        long t = 0;
+        if (d != 0.0) t = std::lround(static_cast<double>(src[j]) / d);
+        t = t > 1 ? 1 : (t < -1 ? -1 : t);
+        int byte, tn;
+        ptq1_0_place(j, &byte, &tn);
+        trits[byte][tn] = static_cast<int>(t + 1);
+      }
+      for (int i = 0; i < 26; ++i) {
+        for (int tn = 0; tn < 5; ++tn) v[i] = v[i] * 3 + trits[i][tn];
+        blk[i] = static_cast<uint8_t>((256 * v[i] + 242) / 243);  // ceil(256 v / 243)
+      }
+      blk[26] = static_cast<uint8_t>(h & 0xFF);
+      blk[27] = static_cast<uint8_t>(h >> 8);
+    }
+  }
+  return KQ_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Host blockwise Hadamard: in-place FP64 butterflies (natural Sylvester order),
 // then one FP64 multiply by 1/sqrt(block) and one rounding to fp32.
 // ---------------------------------------------------------------------------
 
 int kq_hadamard_blockwise_host(const float* in, float* out, int64_t rows, int64_t k, int32_t block) {
+  return kq_rotate_blockwise_host(in, out, rows, k, block, nullptr);
+}
+
+int kq_rotate_blockwise_host(const float* in, float* out, int64_t rows, int64_t k, int32_t block,
+                             const int8_t* signs) {
   clear_error();
   if (!in || !out) return fail(KQ_ERR_INVALID_ARG, "NULL pointer");
   if (block < 1 || (block & (block - 1)) != 0) return fail(KQ_ERR_SHAPE, "block %d is not a power of two", block);
   if (rows < 1 || k < block || k % block)
     return fail(KQ_ERR_SHAPE, "rows = %lld, k = %lld, block = %d", (long long)rows, (long long)k, block);
+  if (signs)
+    for (int64_t c = 0; c < k; ++c)
+      if (signs[c] != 1 && signs[c] != -1) return fail(KQ_ERR_INVALID_ARG, "signs[%lld] = %d", (long long)c, signs[c]);
   const double scale = 1.0 / std::sqrt(static_cast<double>(block));
   std::vector<double> v(static_cast<size_t>(block));
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t b0 = 0; b0 < k; b0 += block) {
       const float* src = in + r * k + b0;
-      for (int32_t i = 0; i < block; ++i) v[i] = src[i];
+      for (int32_t i = 0; i < block; ++i) v[i] = signs ? (double)signs[b0 + i] * src[i] : (double)src[i];
       for (int32_t h = 1; h < block; h <<= 1) {
         for (int32_t i = 0; i < block; i += 2 * h) {
           for (int32_t j = i; j < i + h; ++j) {

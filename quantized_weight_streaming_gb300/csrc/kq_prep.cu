@@ -35,6 +35,40 @@ __global__ void prepare_kernel(const uint8_t* __restrict__ blocks, int64_t n, in
   }
 }
 
+// PTQ1_0 block -> PQ2_0 planes: trit n of byte q is ((q 3^n) mod 256) * 3 / 256;
+// element e sits in byte e%16 (e < 80, trit e/16), 16+(e-80)%8 (e < 120,
+// trit (e-80)/8) or 24+(e-120)%2 (trit (e-120)/2); the fp16 scale is last.
+// One thread per block; the trit becomes the PQ2_0 code of the same element.
+__global__ void prepare_ptq1_0_kernel(const uint8_t* __restrict__ blocks, int64_t n, int64_t nb, int64_t sstride,
+                                      uint8_t* __restrict__ codes, uint16_t* __restrict__ scales) {
+  int64_t total = n * nb;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    int64_t r = i / nb, b = i % nb;
+    const uint8_t* blk = blocks + i * 28;
+    scales[r * sstride + b] = (uint16_t)(blk[26] | (blk[27] << 8));
+    uint32_t words[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int e = 0; e < 128; ++e) {
+      int byte, tn;
+      if (e < 80) {
+        byte = e % 16;
+        tn = e / 16;
+      } else if (e < 120) {
+        byte = 16 + (e - 80) % 8;
+        tn = (e - 80) / 8;
+      } else {
+        byte = 24 + (e - 120) % 2;
+        tn = (e - 120) / 2;
+      }
+      const uint32_t pw[5] = {1u, 3u, 9u, 27u, 81u};
+      const uint32_t trit = (((uint32_t)blk[byte] * pw[tn]) & 0xFFu) * 3u >> 8;
+      words[e / 16] |= trit << (2 * (e % 16));
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(codes + i * 32);  // row r, bytes b*32 .. (row stride nb*32)
+#pragma unroll
+    for (int w = 0; w < 8; ++w) dst[w] = words[w];
+  }
+}
+
 __global__ void zero_scale_padding_kernel(int64_t n, int64_t nb, int64_t sstride, uint16_t* __restrict__ scales) {
   int64_t pad = sstride - nb;
   int64_t total = n * pad;
@@ -106,13 +140,22 @@ __global__ void quantize_pq2_0_kernel(const float* __restrict__ w, int64_t n, in
 // --------------------------------------------------------------------------
 
 // block == 128: one warp per block, four elements per lane.
+// signs (NULL: none) hold one +-1 per position of a row of k = bpr blocks;
+// the flip is exact in FP64 and comes before the butterflies.
 __global__ void hadamard128_f64_kernel(const float* __restrict__ in, float* __restrict__ out, int64_t nblocks,
-                                       double scale) {
+                                       double scale, const int8_t* __restrict__ signs, int64_t bpr) {
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
   for (int64_t i = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; i < nblocks; i += warps) {
     float4 f = *reinterpret_cast<const float4*>(in + i * 128 + 4 * lane);
     double v[4] = {f.x, f.y, f.z, f.w};
+    if (signs) {
+      const char4 s4 = *reinterpret_cast<const char4*>(signs + (i % bpr) * 128 + 4 * lane);
+      v[0] *= (double)s4.x;
+      v[1] *= (double)s4.y;
+      v[2] *= (double)s4.z;
+      v[3] *= (double)s4.w;
+    }
     // strides 1 and 2 inside the lane
     double a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
     v[0] = a0 + a2;
@@ -139,10 +182,12 @@ __global__ void hadamard128_f64_kernel(const float* __restrict__ in, float* __re
 
 // Any power-of-two block up to 4096: one CTA per block, butterflies in shared memory.
 __global__ void hadamard_f64_smem_kernel(const float* __restrict__ in, float* __restrict__ out, int64_t nblocks,
-                                         int block, double scale) {
+                                         int block, double scale, const int8_t* __restrict__ signs, int64_t bpr) {
   extern __shared__ double buf[];
   for (int64_t i = blockIdx.x; i < nblocks; i += gridDim.x) {
-    for (int j = threadIdx.x; j < block; j += blockDim.x) buf[j] = in[i * block + j];
+    const int8_t* sg = signs ? signs + (i % bpr) * block : nullptr;
+    for (int j = threadIdx.x; j < block; j += blockDim.x)
+      buf[j] = sg ? (double)sg[j] * (double)in[i * block + j] : (double)in[i * block + j];
     __syncthreads();
     for (int h = 1; h < block; h <<= 1) {
       for (int t = threadIdx.x; t < block / 2; t += blockDim.x) {
@@ -218,10 +263,14 @@ int kq_prepare(int fmt, const void* d_blocks, int64_t n, int64_t k, void* d_code
   clear_error();
   if (int s = check_planes_out(fmt, n, k, d_codes, d_scales)) return s;
   if (!d_blocks) return fail(KQ_ERR_INVALID_ARG, "NULL blocks");
-  const int64_t nb = k / block_of(fmt), ss = scale_stride(fmt, k);
+  const int64_t nb = k / block_of(fmt), ss = scale_stride(plane_format(fmt), k);
   cudaStream_t st = (cudaStream_t)stream;
-  prepare_kernel<<<grid_for(n * nb, 256), 256, 0, st>>>((const uint8_t*)d_blocks, n, nb, ss, (uint8_t*)d_codes,
-                                                        (uint16_t*)d_scales);
+  if (fmt == KQ_PTQ1_0)
+    prepare_ptq1_0_kernel<<<grid_for(n * nb, 256), 256, 0, st>>>((const uint8_t*)d_blocks, n, nb, ss,
+                                                                 (uint8_t*)d_codes, (uint16_t*)d_scales);
+  else
+    prepare_kernel<<<grid_for(n * nb, 256), 256, 0, st>>>((const uint8_t*)d_blocks, n, nb, ss, (uint8_t*)d_codes,
+                                                          (uint16_t*)d_scales);
   KQ_CUDA_TRY(cudaGetLastError());
   if (ss > nb) {
     zero_scale_padding_kernel<<<grid_for(n * (ss - nb), 256), 256, 0, st>>>(n, nb, ss, (uint16_t*)d_scales);
@@ -272,8 +321,14 @@ int kq_dequantize(const kq_qmat* W, float* d_out, void* stream) {
 }
 
 int kq_hadamard_blockwise(const float* d_in, float* d_out, int64_t rows, int64_t k, int32_t block, void* stream) {
+  return kq_rotate_blockwise(d_in, d_out, rows, k, block, nullptr, stream);
+}
+
+int kq_rotate_blockwise(const float* d_in, float* d_out, int64_t rows, int64_t k, int32_t block,
+                        const int8_t* d_signs, void* stream) {
   clear_error();
   if (!d_in || !d_out) return fail(KQ_ERR_INVALID_ARG, "NULL pointer");
+  if (d_signs && !aligned16(d_signs)) return fail(KQ_ERR_ALIGNMENT, "signs not 16-byte aligned");
   if (block < 1 || (block & (block - 1)) != 0) return fail(KQ_ERR_SHAPE, "block %d is not a power of two", block);
   if (block > 4096) return fail(KQ_ERR_UNSUPPORTED, "block %d > 4096", block);
   if (rows < 1 || k < block || k % block)
@@ -283,12 +338,13 @@ int kq_hadamard_blockwise(const float* d_in, float* d_out, int64_t rows, int64_t
   cudaStream_t st = (cudaStream_t)stream;
   if (block == 128) {
     if (!aligned16(d_in) || !aligned16(d_out)) return fail(KQ_ERR_ALIGNMENT, "pointer not 16-byte aligned");
-    hadamard128_f64_kernel<<<grid_for(nblocks * 32, 256), 256, 0, st>>>(d_in, d_out, nblocks, scale);
+    hadamard128_f64_kernel<<<grid_for(nblocks * 32, 256), 256, 0, st>>>(d_in, d_out, nblocks, scale, d_signs,
+                                                                        k / block);
   } else {
     int threads = block / 2 < 32 ? 32 : (block / 2 > 256 ? 256 : block / 2);
     int grid = grid_for(nblocks * threads, threads);
     hadamard_f64_smem_kernel<<<grid, threads, (size_t)block * sizeof(double), st>>>(d_in, d_out, nblocks, block,
-                                                                                    scale);
+                                                                                    scale, d_signs, k / block);
   }
   KQ_CUDA_TRY(cudaGetLastError());
   return KQ_OK;

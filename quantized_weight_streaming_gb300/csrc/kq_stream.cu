@@ -96,12 +96,22 @@ struct Job {
   float* ws;       // [splits][m][n] partials (splits > 1)
   int64_t n, k, ldy;
   int64_t x_off, y_off;  // offsets into the packed activation / output (decode plan)
+  int64_t ws_off;        // offset of the split partials in the step's workspace (decode plan)
   int64_t item_begin;    // first global item of this job
   int64_t items;         // row_blocks * splits
   int32_t row_blocks;
   int32_t splits;
-  int32_t split_k;  // weights per split (multiple of the chunk)
-  int32_t pad;
+  int32_t split_k;    // weights per split (multiple of the chunk)
+  int32_t had_block;  // PQ2_0: Hadamard block of the rotation (128 or 1024)
+  const int8_t* signs;  // PQ2_0: +-1 per position of K applied before the transform, or nullptr
+};
+
+// Where a decode-plan job's activation comes from (linked plans).
+struct XLink {
+  int32_t src_job;    // -1: the packed input at x_off; else the output of job src_job
+  int32_t dep_stage;  // the stage whose completion the staging waits for (-1: none)
+  int32_t x_key;      // jobs with equal keys read the same activation (the transform memo)
+  float alpha;        // the successor activation is alpha * output
 };
 
 struct Params {
@@ -110,10 +120,16 @@ struct Params {
   Job job0;
   const Job* jobs;          // decode plan: device table of jobs ...
   const CUtensorMap* maps;  // ... and their maps, [2 * j] codes, [2 * j + 1] scales
+  const XLink* links;       // linked plan: activation sources, or nullptr (every job its own packed input)
   const float* x_base;      // packed activations (decode plan)
   float* y_base;            // packed outputs (decode plan)
-  const int64_t* bounds;    // per-CTA item ranges [bounds[c], bounds[c+1]) (plan), or nullptr
+  float* ws_base;           // split partials (linked plan)
+  int32_t* stage_done;      // linked plan: per stage, the CTAs that have finished it; or nullptr
+  const int32_t* split_jobs;  // linked plan: the jobs whose K is split (their y is written at the end)
+  const int64_t* bounds;    // item ranges of CTA c in stage s: [bounds[s (G+1) + c], bounds[s (G+1) + c + 1])
   int64_t total_items;
+  int32_t nstages;          // stages of the plan (1 without links)
+  int32_t n_split_jobs;
 };
 
 template <int FMT>
@@ -188,15 +204,17 @@ struct ItemCursor {
     job = p.jobs[j];
     job.x = p.x_base + job.x_off;
     job.y = p.y_base + job.y_off;
+    job.ws = p.ws_base + job.ws_off;
     mc = p.maps + 2 * j;
     ms = p.maps + 2 * j + 1;
   }
 };
 
-__device__ __forceinline__ void cta_range(const Params& p, int64_t& b, int64_t& e) {
+__device__ __forceinline__ void cta_range(const Params& p, int stage, int64_t& b, int64_t& e) {
   if (p.bounds) {
-    b = p.bounds[blockIdx.x];
-    e = p.bounds[blockIdx.x + 1];
+    const int64_t* bs = p.bounds + (int64_t)stage * (gridDim.x + 1);
+    b = bs[blockIdx.x];
+    e = bs[blockIdx.x + 1];
   } else {
     b = p.total_items * blockIdx.x / gridDim.x;
     e = p.total_items * (blockIdx.x + 1) / gridDim.x;
@@ -204,6 +222,91 @@ __device__ __forceinline__ void cta_range(const Params& p, int64_t& b, int64_t& 
 }
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }  // e in [-126, 127]
+
+// The activation a job reads: a plain vector, or alpha times the sum, in
+// split order, of an earlier job's split partials (a dependent chain).
+struct XSrc {
+  const float* base;   // the vector, or split 0 of the source's partials
+  int64_t stride;      // floats between consecutive partials
+  int64_t row_stride;  // floats between activation rows (m > 1)
+  int32_t nsum;        // partials added (1: a plain vector)
+  int32_t vec4;        // base and stride allow 16-byte loads
+  float alpha;
+  int32_t had;          // PQ2_0 rotation block (128 or 1024)
+  const int8_t* signs;  // PQ2_0 sign per position of K, or nullptr
+};
+
+// x[i..i+3] of activation row m; loads bypass L1 (the source may have been
+// written by other CTAs of this launch).  The partials are added in split
+// order, exactly as the final write of the source's output adds them.
+__device__ __forceinline__ float4 load_x4(const XSrc& xs, int m, int64_t i) {
+  const float* b = xs.base + (int64_t)m * xs.row_stride + i;
+  float4 v;
+  if (xs.vec4) {
+    v = __ldcg(reinterpret_cast<const float4*>(b));
+    for (int s = 1; s < xs.nsum; ++s) {
+      const float4 u = __ldcg(reinterpret_cast<const float4*>(b + s * xs.stride));
+      v.x += u.x;
+      v.y += u.y;
+      v.z += u.z;
+      v.w += u.w;
+    }
+  } else {
+    v = make_float4(__ldcg(b), __ldcg(b + 1), __ldcg(b + 2), __ldcg(b + 3));
+    for (int s = 1; s < xs.nsum; ++s) {
+      const float* u = b + s * xs.stride;
+      v.x += __ldcg(u);
+      v.y += __ldcg(u + 1);
+      v.z += __ldcg(u + 2);
+      v.w += __ldcg(u + 3);
+    }
+  }
+  v.x *= xs.alpha;
+  v.y *= xs.alpha;
+  v.z *= xs.alpha;
+  v.w *= xs.alpha;
+  return v;
+}
+
+// The rotation fields are read from the job table (or the single job), not
+// from the cursor's copy, so that they stay out of registers in the tile loop.
+__device__ __forceinline__ XSrc make_xsrc(const Params& p, int32_t j, const Job& job, const XLink& lk) {
+  XSrc xs;
+  const Job& jm = p.jobs ? p.jobs[j] : p.job0;
+  xs.had = jm.had_block;
+  xs.signs = jm.signs;
+  xs.row_stride = job.k;
+  xs.alpha = 1.f;
+  xs.nsum = 1;
+  xs.stride = 0;
+  xs.base = job.x;
+  if (lk.src_job >= 0) {
+    const Job& src = p.jobs[lk.src_job];
+    xs.alpha = lk.alpha;
+    if (src.splits > 1) {
+      xs.base = p.ws_base + src.ws_off;
+      xs.nsum = src.splits;
+      xs.stride = src.n;
+    } else {
+      xs.base = p.y_base + src.y_off;
+    }
+  }
+  xs.vec4 = ((reinterpret_cast<uintptr_t>(xs.base) & 15u) == 0 && (xs.stride & 3) == 0) ? 1 : 0;
+  return xs;
+}
+
+// Waits (one thread) until every CTA has finished `stage`; false on timeout.
+__device__ __forceinline__ bool wait_stage(const Params& p, int stage) {
+  const int32_t* ctr = p.stage_done + stage;
+  const long long start = clock64();
+  while (true) {
+    int32_t v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= (int32_t)gridDim.x) return true;
+    if (clock64() - start > kWaitLimitCycles) return false;
+    __nanosleep(64);
+  }
+}
 
 // Q8_0 swizzled activation layout: the 8 activations of lane l in tile chunk
 // t are read as two 16-byte pieces c = 0, 1 at [t][c][l], so the 32 lanes of
@@ -264,6 +367,25 @@ __device__ __forceinline__ int btab_index(int b, int q, int j, int n, int t) {
   return (((b * 2 + q) * 4 + j) * (2 * M) + n) * 4 + t;
 }
 
+// Unnormalised 128-point Walsh-Hadamard transform, natural (Sylvester) order,
+// of a block held 4 consecutive elements per lane: strides 1 and 2 in
+// registers, 4 .. 64 across lanes.
+__device__ __forceinline__ void fwht128_lane4(float (&v)[4], int lane) {
+  float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+  v[0] = a0 + a2;
+  v[2] = a0 - a2;
+  v[1] = a1 + a3;
+  v[3] = a1 - a3;
+#pragma unroll
+  for (int mk = 1; mk < 32; mk <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float q = __shfl_xor_sync(0xffffffffu, v[i], mk);
+      v[i] = (lane & mk) ? (q - v[i]) : (v[i] + q);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Activation prologue: stage x[m][kbeg, kend) of the current job.
 //  Q8_0: fp32 activations in the swizzled layout.
@@ -271,45 +393,86 @@ __device__ __forceinline__ int btab_index(int b, int q, int j, int n, int t) {
 //  block, plus per block the factor 2^(10+E) and the sum of x'.
 // ---------------------------------------------------------------------------
 template <int FMT, int M>
-__device__ void stage_activation(const Job& job, int64_t kbeg, int64_t kend, int xlen_pad, float* xbuf, float* fx,
+__device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int xlen_pad, float* xbuf, float* fx,
                                  float* sx, float* scratch, int cw, int lane) {
   const int len = (int)(kend - kbeg);
   constexpr int kT = 32 * kConsumerWarps;
   if (FMT == KQ_Q8_0) {
     float4* xb4 = reinterpret_cast<float4*>(xbuf);
     for (int m = 0; m < M; ++m) {
-      const float4* src = reinterpret_cast<const float4*>(job.x + (int64_t)m * job.k + kbeg);
-      for (int i = cw * 32 + lane; i < len / 4; i += kT) xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] = src[i];
+      for (int i = cw * 32 + lane; i < len / 4; i += kT)
+        xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] = load_x4(xs, m, kbeg + 4 * i);
     }
   } else {
     const int nblk = len / 128;
     uint2* btab = reinterpret_cast<uint2*>(xbuf);
     const float inv_sqrt128 = 0.08838834764831845f;
+    // The page's n = 1024 rotation is H_1024 = H_8 (x) H_128 in Sylvester
+    // order (index 128 a + e): H_128 on each 128-block, then H_8 across the
+    // eight blocks at each position e, then 1/32.  The two passes go through
+    // `raw` ([block][row][128] floats): the B-table region itself for one
+    // activation row (each warp then rewrites only its own block), the upper
+    // half of the buffer for more rows (the split keeps both halves apart).
+    const bool h1024 = xs.had == 1024;
+    float* raw = M == 1 ? xbuf : xbuf + kXMax / 2;
+    if (h1024) {
+      for (int tt = cw; tt < M * nblk; tt += kConsumerWarps) {
+        const int m = tt / nblk, b = tt % nblk;
+        float4 f = load_x4(xs, m, kbeg + b * 128 + 4 * lane);
+        float v[4] = {f.x, f.y, f.z, f.w};
+        if (xs.signs) {
+          const char4 s4 = *reinterpret_cast<const char4*>(xs.signs + kbeg + b * 128 + 4 * lane);
+          v[0] *= (float)s4.x;
+          v[1] *= (float)s4.y;
+          v[2] *= (float)s4.z;
+          v[3] *= (float)s4.w;
+        }
+        fwht128_lane4(v, lane);
+        *reinterpret_cast<float4*>(raw + ((int64_t)b * M + m) * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+      }
+      named_barrier(1, kConsumerWarps * 32);
+      const int cols = (nblk / 8) * M * 128;
+      for (int c = cw * 32 + lane; c < cols; c += kConsumerWarps * 32) {
+        const int e = c % 128, mm = (c / 128) % M, bb = c / (128 * M);
+        float v[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) v[a] = raw[((int64_t)(bb * 8 + a) * M + mm) * 128 + e];
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+          for (int a = 0; a < 8; ++a)
+            if (!(a & h)) {
+              const float x0 = v[a], x1 = v[a + h];
+              v[a] = x0 + x1;
+              v[a + h] = x0 - x1;
+            }
+#pragma unroll
+        for (int a = 0; a < 8; ++a) raw[((int64_t)(bb * 8 + a) * M + mm) * 128 + e] = v[a] * 0.03125f;
+      }
+      named_barrier(1, kConsumerWarps * 32);
+    }
     for (int tt = cw; tt < M * nblk; tt += kConsumerWarps) {
       const int m = tt / nblk, b = tt % nblk;
-      float4 f = *reinterpret_cast<const float4*>(job.x + (int64_t)m * job.k + kbeg + b * 128 + 4 * lane);
-      float v[4] = {f.x, f.y, f.z, f.w};
-      // fast Walsh-Hadamard transform, natural (Sylvester) order: strides 1, 2 in registers ...
-      float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
-      v[0] = a0 + a2;
-      v[2] = a0 - a2;
-      v[1] = a1 + a3;
-      v[3] = a1 - a3;
-      // ... strides 4 .. 64 across lanes
+      float v[4];
+      if (h1024) {  // x' of this block, transformed above
+        const float4 f = *reinterpret_cast<const float4*>(raw + ((int64_t)b * M + m) * 128 + 4 * lane);
+        v[0] = f.x;
+        v[1] = f.y;
+        v[2] = f.z;
+        v[3] = f.w;
+      } else {
+        const float4 f = load_x4(xs, m, kbeg + b * 128 + 4 * lane);
+        v[0] = f.x;
+        v[1] = f.y;
+        v[2] = f.z;
+        v[3] = f.w;
+        fwht128_lane4(v, lane);
 #pragma unroll
-      for (int mk = 1; mk < 32; mk <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          float q = __shfl_xor_sync(0xffffffffu, v[i], mk);
-          v[i] = (lane & mk) ? (q - v[i]) : (v[i] + q);
-        }
+        for (int i = 0; i < 4; ++i) v[i] *= inv_sqrt128;
       }
       float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[i] *= inv_sqrt128;
-        amax = fmaxf(amax, fabsf(v[i]));
-      }
+      for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
       for (int mk = 16; mk; mk >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, mk));
       // block exponent E with amax < 2^(E+1), clamped to [-100, 100]
@@ -501,17 +664,21 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   }
   __syncthreads();
 
-  int64_t ib, ie;
-  cta_range(p, ib, ie);
+  const int nst = p.nstages > 0 ? p.nstages : 1;
 
   if (warp == 0) {
     // ------------------------------- producer -------------------------------
+    // The weight stream never waits for a stage: it runs ahead into the next
+    // stage's tiles as far as the ring allows.
     if (lane == 0) {
       const uint64_t policy = l2_policy_evict_first();
       ItemCursor cur;
       int64_t tile = 0;
       bool ok = true;
       int32_t last_j = -1;
+      for (int st = 0; st < nst && ok; ++st) {
+      int64_t ib, ie;
+      cta_range(p, st, ib, ie);
       for (int64_t item = ib; item < ie && ok; ++item) {
         cur.next(p, item);
         if (cur.j != last_j) {
@@ -545,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
           tma_load_2d(st + kTileCodeBytes, cur.ms, (int32_t)(k0 / F::kBlock / 2), rb * kTileRows, &full[s], policy);
         }
       }
+      }
       // Never leave the CTA with copies in flight: wait for the last stages issued.
       for (int64_t t = tile - 1; t >= 0 && t >= tile - kStages; --t)
         (void)mbar_wait_bounded(&full[t % kStages], (uint32_t)((t / kStages) & 1));
@@ -556,11 +724,19 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   const int cw = warp - 1;
   float* scratch = scratch_all + cw * kScratchFloats;
   ItemCursor cur;
-  int32_t cached_job = -1, cached_split = -1;
+  // the staged activation slice: key of its activation and its K range
+  // (kbeg << 16 | kend, both below 2^15); a job sharing the activation and
+  // the range reuses it: the transform memo
+  int32_t cached_key = -1;
+  uint32_t cached_range = 0xFFFFFFFFu;
+  int ready = -1;          // every stage up to this one has finished on all CTAs
   int ring = 0;            // stage of the next tile
   uint32_t ring_par = 0;   // its phase parity
   uint32_t combines = 0;   // PQ2_0 slab-pair handoffs so far
   int xlen_pad = 0;
+  for (int st = 0; st < nst; ++st) {
+  int64_t ib, ie;
+  cta_range(p, st, ib, ie);
   for (int64_t item = ib; item < ie; ++item) {
     cur.next(p, item);
     const Job& job = cur.job;
@@ -569,13 +745,23 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     const int rows = min(kTileRows, (int)(job.n - row0));
     const int64_t kbeg = (int64_t)split * job.split_k;
     const int64_t kend = kbeg + min((int64_t)job.split_k, job.k - kbeg);
-    if (cur.j != cached_job || split != cached_split) {
+    const int32_t key = p.links ? p.links[cur.j].x_key : cur.j;
+    const uint32_t range = ((uint32_t)kbeg << 16) | (uint32_t)kend;
+    if (key != cached_key || range != cached_range) {
+      const XLink lk = p.links ? p.links[cur.j] : XLink{-1, -1, cur.j, 1.f};
       xlen_pad = (int)(((kend - kbeg) + F::kChunk - 1) / F::kChunk * F::kChunk);
+      if (lk.dep_stage > ready) {  // the activation is an output of an earlier stage
+        if (cw == 0 && lane == 0 && !*abort_flag && !wait_stage(p, lk.dep_stage)) {
+          *abort_flag = 1;
+          stream_flag(KQ_ERR_TIMEOUT);
+        }
+        ready = lk.dep_stage;
+      }
       named_barrier(1, kConsumerWarps * 32);  // everyone is done with the previous slice
-      stage_activation<FMT, M>(job, kbeg, kend, xlen_pad, xbuf, fx, sx, scratch, cw, lane);
+      stage_activation<FMT, M>(make_xsrc(p, cur.j, job, lk), kbeg, kend, xlen_pad, xbuf, fx, sx, scratch, cw, lane);
       named_barrier(1, kConsumerWarps * 32);
-      cached_job = cur.j;
-      cached_split = split;
+      cached_key = key;
+      cached_range = range;
     }
     float acc8[FMT == KQ_Q8_0 ? kRowsPerWarp : 1][M];
     float acc4[4][2] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
@@ -707,6 +893,38 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       }
     }
   }
+  // linked plan: this CTA has written every output of its items of stage st
+  if (p.stage_done) {
+    named_barrier(1, kConsumerWarps * 32);
+    if (cw == 0 && lane == 0) {
+      __threadfence();
+      atomicAdd(p.stage_done + st, 1);
+    }
+  }
+  }
+
+  // Linked plan: once every stage has finished everywhere, the outputs of the
+  // split jobs are their partials added in split order (the order every
+  // dependent activation used), each CTA a slice of the rows of every job.
+  if (p.n_split_jobs > 0) {
+    if (cw == 0 && lane == 0 && !*abort_flag && !wait_stage(p, nst - 1)) {
+      *abort_flag = 1;
+      stream_flag(KQ_ERR_TIMEOUT);
+    }
+    named_barrier(1, kConsumerWarps * 32);
+    if (*abort_flag) return;
+    for (int q = 0; q < p.n_split_jobs; ++q) {
+      const Job& J = p.jobs[p.split_jobs[q]];
+      const int64_t r0 = J.n * blockIdx.x / gridDim.x, r1 = J.n * (blockIdx.x + 1) / gridDim.x;
+      const float* w = p.ws_base + J.ws_off;
+      float* y = p.y_base + J.y_off;
+      for (int64_t r = r0 + cw * 32 + lane; r < r1; r += kConsumerWarps * 32) {
+        float v = __ldcg(w + r);
+        for (int sp = 1; sp < J.splits; ++sp) v += __ldcg(w + (int64_t)sp * J.n + r);
+        y[r] = v;
+      }
+    }
+  }
 }
 
 // Second pass of split-K: y[m][row] = sum over splits in split order.
@@ -736,10 +954,17 @@ struct Geometry {
 // picks the count that minimises an estimate of the kernel time on `sms`
 // CTAs: tiles of the busiest CTA times the time of a tile, plus the second
 // pass when there is more than one split.
-static Geometry make_geometry(int fmt, int64_t n, int64_t k, int64_t m, int requested, int sms = 0) {
+// The staged slice of m rows must fit kXMax floats, or half of it for the
+// n = 1024 rotation with m > 1 (its transform passes use the other half).
+static int64_t staging_floats(const kq_qmat* W, int64_t m) {
+  return W->fmt == KQ_PQ2_0 && W->had_block == 1024 && m > 1 ? kXMax / 2 : kXMax;
+}
+
+static Geometry make_geometry(int fmt, int64_t n, int64_t k, int64_t m, int requested, int sms = 0,
+                              int64_t xmax = kXMax) {
   Geometry g;
   const int64_t unit = chunk_of(fmt);
-  const int64_t max_split = std::max<int64_t>(unit, (kXMax / m) / unit * unit);
+  const int64_t max_split = std::max<int64_t>(unit, (xmax / m) / unit * unit);
   const int64_t min_splits = (k + max_split - 1) / max_split;
   const int64_t row_blocks = (n + tile_rows(fmt) - 1) / tile_rows(fmt);
   int64_t splits = std::max<int64_t>(requested > 0 ? requested : 1, min_splits);
@@ -867,7 +1092,8 @@ static int sms_or_default() {
 
 static size_t splitk_ws_bytes(const kq_qmat* W, int64_t m, int splits) {
   int64_t mm = std::min<int64_t>(m, kMaxRowsPerLaunch);
-  Geometry g = make_geometry(W->fmt, W->n, W->k, mm, splits, splits == 0 ? sms_or_default() : 0);
+  Geometry g = make_geometry(W->fmt, W->n, W->k, mm, splits, splits == 0 ? sms_or_default() : 0,
+                             staging_floats(W, mm));
   return g.splits > 1 ? (size_t)g.splits * (size_t)mm * (size_t)W->n * sizeof(float) : 0;
 }
 
@@ -889,10 +1115,10 @@ static int gemm_impl(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, 
   cudaStream_t st = (cudaStream_t)stream;
   for (int64_t m0 = 0; m0 < m; m0 += kMaxRowsPerLaunch) {
     const int mm = (int)std::min<int64_t>(kMaxRowsPerLaunch, m - m0);
-    Geometry g = make_geometry(W->fmt, W->n, W->k, mm, splits, splits == 0 ? sms : 0);
+    Geometry g = make_geometry(W->fmt, W->n, W->k, mm, splits, splits == 0 ? sms : 0, staging_floats(W, mm));
     // the staged activation slice (or its B table, 4 bytes per position and
     // row for PQ2_0) must fit the shared-memory buffer
-    if ((int64_t)mm * g.split_k > kXMax)
+    if ((int64_t)mm * g.split_k > staging_floats(W, mm))
       return fail(KQ_ERR_UNSUPPORTED, "internal: split of %d weights x %d rows exceeds the staging buffer", g.split_k, mm);
     Job& j = p.job0;
     j.x = d_X + m0 * W->k;
@@ -906,6 +1132,8 @@ static int gemm_impl(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, 
     j.row_blocks = g.row_blocks;
     j.splits = g.splits;
     j.split_k = g.split_k;
+    j.had_block = W->had_block;
+    j.signs = W->signs;
     p.jobs = nullptr;
     p.maps = nullptr;
     p.bounds = nullptr;
@@ -946,13 +1174,234 @@ struct kq_plan {
   int64_t count = 0;
   int64_t x_floats = 0, y_floats = 0, weight_bytes = 0;
   int grid = 0;
+  int32_t nstages = 1;
+  int32_t n_split = 0;
+  bool linked = false;
   int64_t total_items = 0;
+  size_t counter_bytes = 0;  // linked plan: stage counters at the start of the workspace ...
+  size_t ws_bytes = 0;       // ... then the split partials
   kq::Job* d_jobs = nullptr;
   CUtensorMap* d_maps = nullptr;
   int64_t* d_bounds = nullptr;
+  kq::XLink* d_links = nullptr;
+  int32_t* d_split_jobs = nullptr;
 };
 
 using namespace kq;
+
+static void destroy_plan(kq_plan* p) {
+  if (!p) return;
+  cudaFree(p->d_jobs);
+  cudaFree(p->d_maps);
+  cudaFree(p->d_bounds);
+  cudaFree(p->d_links);
+  cudaFree(p->d_split_jobs);
+  delete p;
+}
+
+// Checks the links of a linked plan (see kq_link in kq.h).
+static int check_links(const kq_qmat* mats, const kq_link* links, int64_t count) {
+  for (int64_t i = 0; i < count; ++i) {
+    const kq_link& L = links[i];
+    if (L.reserved != 0) return fail(KQ_ERR_INVALID_ARG, "link %lld: reserved field not 0", (long long)i);
+    if (L.stage < 0 || (i > 0 && L.stage < links[i - 1].stage))
+      return fail(KQ_ERR_SHAPE, "link %lld: stage %d (stages start at 0 and never decrease)", (long long)i, L.stage);
+    if (L.src == KQ_SRC_PACKED) continue;
+    if (L.src != KQ_SRC_INPUT_OF && L.src != KQ_SRC_OUTPUT_OF)
+      return fail(KQ_ERR_INVALID_ARG, "link %lld: unknown source kind %d", (long long)i, L.src);
+    if (L.of < 0 || L.of >= i)
+      return fail(KQ_ERR_INVALID_ARG, "link %lld: source matrix %lld is not an earlier one", (long long)i,
+                  (long long)L.of);
+    const kq_qmat& S = mats[L.of];
+    if (L.src == KQ_SRC_INPUT_OF) {
+      if (S.k != mats[i].k)
+        return fail(KQ_ERR_SHAPE, "link %lld: k = %lld differs from matrix %lld's k = %lld", (long long)i,
+                    (long long)mats[i].k, (long long)L.of, (long long)S.k);
+    } else {
+      if (mats[i].k > S.n)
+        return fail(KQ_ERR_SHAPE, "link %lld: k = %lld exceeds matrix %lld's output length %lld", (long long)i,
+                    (long long)mats[i].k, (long long)L.of, (long long)S.n);
+      if (links[L.of].stage >= L.stage)
+        return fail(KQ_ERR_SHAPE, "link %lld: reads the output of matrix %lld of stage %d from stage %d",
+                    (long long)i, (long long)L.of, links[L.of].stage, L.stage);
+      if (!std::isfinite(L.alpha)) return fail(KQ_ERR_INVALID_ARG, "link %lld: alpha is not finite", (long long)i);
+    }
+  }
+  return KQ_OK;
+}
+
+// Builds a plan.  links == nullptr: every matrix reads its own packed input,
+// one stage, no splits (kq_decode_plan_create).
+static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count, kq_plan** out) {
+  if (!mats || !out) return fail(KQ_ERR_INVALID_ARG, "NULL pointer");
+  if (count < 1) return fail(KQ_ERR_SHAPE, "count = %lld", (long long)count);
+  if (count > INT32_MAX / 2) return fail(KQ_ERR_SHAPE, "count = %lld", (long long)count);
+  *out = nullptr;
+  const int fmt = mats[0].fmt;
+  for (int64_t i = 0; i < count; ++i) {
+    if (int s = check_qmat(&mats[i], -1)) return fail(s, "matrix %lld: %s", (long long)i, kq_last_error());
+    if (mats[i].fmt != fmt) return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: mixed formats in one plan", (long long)i);
+    if (mats[i].k > kXMax)
+      return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: k = %lld > %d", (long long)i, (long long)mats[i].k, kXMax);
+  }
+  if (links)
+    if (int s = check_links(mats, links, count)) return s;
+  int sms = 0;
+  if (int s = device_sms(&sms)) return s;
+  const int32_t nstages = links ? links[count - 1].stage + 1 : 1;
+  // row blocks of every stage: a stage with fewer row blocks than SMs splits K
+  std::vector<int64_t> stage_rb((size_t)nstages, 0);
+  for (int64_t i = 0; i < count; ++i)
+    stage_rb[(size_t)(links ? links[i].stage : 0)] += (mats[i].n + tile_rows(fmt) - 1) / tile_rows(fmt);
+  std::vector<Job> jobs((size_t)count);
+  std::vector<CUtensorMap> maps((size_t)(2 * count));
+  std::vector<XLink> xl((size_t)count);
+  std::vector<int32_t> split_jobs;
+  std::vector<double> item_bytes;
+  std::vector<int64_t> stage_first((size_t)nstages + 1, 0);  // first item of each stage
+  int64_t items = 0, xf = 0, yf = 0, wb = 0, wsf = 0;
+  const int64_t unit = chunk_of(fmt);
+  for (int64_t i = 0; i < count; ++i) {
+    const kq_qmat& W = mats[i];
+    if (int s = make_maps(&W, &maps[(size_t)(2 * i)], &maps[(size_t)(2 * i + 1)])) return s;
+    const int32_t stg = links ? links[i].stage : 0;
+    const int64_t row_blocks = (W.n + tile_rows(fmt) - 1) / tile_rows(fmt);
+    int64_t splits = 1, split_k = W.k;
+    if (links && stage_rb[(size_t)stg] < sms) {
+      const int64_t chunks = (W.k + unit - 1) / unit;
+      const int64_t want = std::min<int64_t>(chunks, (sms + stage_rb[(size_t)stg] - 1) / stage_rb[(size_t)stg]);
+      split_k = round_up((W.k + want - 1) / want, unit);
+      splits = (W.k + split_k - 1) / split_k;
+    }
+    Job& j = jobs[(size_t)i];
+    j = Job{};
+    j.y_off = yf;
+    j.n = W.n;
+    j.k = W.k;
+    j.ldy = W.n;
+    j.item_begin = items;
+    j.items = row_blocks * splits;
+    j.row_blocks = (int32_t)row_blocks;
+    j.splits = (int32_t)splits;
+    j.split_k = (int32_t)split_k;
+    j.had_block = W.had_block;
+    j.signs = W.signs;
+    if (splits > 1) {
+      j.ws_off = wsf;
+      wsf += round_up(splits * W.n, 4);
+      split_jobs.push_back((int32_t)i);
+    }
+    // activation source; INPUT_OF inherits its source's, so a group shares one key
+    XLink& L = xl[(size_t)i];
+    const int src = links ? links[i].src : KQ_SRC_PACKED;
+    if (src == KQ_SRC_PACKED) {
+      j.x_off = xf;
+      xf += W.k;
+      L = XLink{-1, -1, (int32_t)i, 1.f};
+    } else if (src == KQ_SRC_INPUT_OF) {
+      j.x_off = jobs[(size_t)links[i].of].x_off;
+      L = xl[(size_t)links[i].of];
+    } else {
+      j.x_off = 0;
+      L = XLink{(int32_t)links[i].of, links[(size_t)links[i].of].stage, (int32_t)i, links[i].alpha};
+    }
+    // items are split-major within a job (ItemCursor); bytes of each for the balance
+    const double rowbytes = (double)code_row_bytes(fmt, split_k) + 2.0 * (double)(split_k / block_of(fmt));
+    for (int64_t sp = 0; sp < splits; ++sp)
+      for (int64_t r = 0; r < row_blocks; ++r) {
+        const double kfrac = (double)std::min<int64_t>(split_k, W.k - sp * split_k) / (double)split_k;
+        item_bytes.push_back(rowbytes * kfrac *
+                             (double)std::min<int64_t>(tile_rows(fmt), W.n - r * tile_rows(fmt)));
+      }
+    items += j.items;
+    stage_first[(size_t)stg + 1] = items;
+    yf += W.n;
+    wb += kq_codes_bytes(fmt, W.n, W.k) + W.n * (W.k / block_of(fmt)) * 2;
+  }
+  for (int32_t s = 1; s <= nstages; ++s) stage_first[(size_t)s] = std::max(stage_first[(size_t)s], stage_first[(size_t)s - 1]);
+  kq_plan* p = new kq_plan();
+  p->fmt = fmt;
+  p->count = count;
+  p->x_floats = xf;
+  p->y_floats = yf;
+  p->weight_bytes = wb;
+  p->total_items = items;
+  p->nstages = nstages;
+  p->linked = links != nullptr;
+  p->n_split = (int32_t)split_jobs.size();
+  p->grid = (int)std::min<int64_t>(items, sms);
+  if (p->linked) {
+    p->counter_bytes = (size_t)round_up((int64_t)nstages * 4, 256);
+    p->ws_bytes = p->counter_bytes + (size_t)wsf * sizeof(float);
+  }
+  // byte-balanced contiguous item ranges, per stage and CTA
+  const int G = p->grid;
+  std::vector<int64_t> bounds((size_t)nstages * (G + 1));
+  for (int32_t s = 0; s < nstages; ++s) {
+    const int64_t b0 = stage_first[(size_t)s], b1 = stage_first[(size_t)s + 1];
+    int64_t* bs = bounds.data() + (size_t)s * (G + 1);
+    double total = 0;
+    for (int64_t it = b0; it < b1; ++it) total += item_bytes[(size_t)it];
+    for (int c = 0; c <= G; ++c) bs[c] = b1;
+    bs[0] = b0;
+    double accum = 0;
+    int c = 1;
+    for (int64_t it = b0; it < b1 && c < G; ++it) {
+      accum += item_bytes[(size_t)it];
+      while (c < G && accum >= total * c / G) bs[c++] = it + 1;
+    }
+  }
+  cudaError_t e = cudaMalloc(&p->d_jobs, sizeof(Job) * (size_t)count);
+  if (e == cudaSuccess) e = cudaMalloc(&p->d_maps, sizeof(CUtensorMap) * (size_t)(2 * count));
+  if (e == cudaSuccess) e = cudaMalloc(&p->d_bounds, sizeof(int64_t) * bounds.size());
+  if (e == cudaSuccess) e = cudaMemcpy(p->d_jobs, jobs.data(), sizeof(Job) * (size_t)count, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(p->d_maps, maps.data(), sizeof(CUtensorMap) * (size_t)(2 * count), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(p->d_bounds, bounds.data(), sizeof(int64_t) * bounds.size(), cudaMemcpyHostToDevice);
+  if (p->linked) {
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_links, sizeof(XLink) * (size_t)count);
+    if (e == cudaSuccess) e = cudaMemcpy(p->d_links, xl.data(), sizeof(XLink) * (size_t)count, cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !split_jobs.empty()) {
+      e = cudaMalloc(&p->d_split_jobs, sizeof(int32_t) * split_jobs.size());
+      if (e == cudaSuccess)
+        e = cudaMemcpy(p->d_split_jobs, split_jobs.data(), sizeof(int32_t) * split_jobs.size(),
+                       cudaMemcpyHostToDevice);
+    }
+  }
+  if (e != cudaSuccess) {
+    destroy_plan(p);
+    return fail(KQ_ERR_CUDA, "plan allocation: %s", cudaGetErrorString(e));
+  }
+  *out = p;
+  return KQ_OK;
+}
+
+template <int FMT>
+static int launch_plan(const Params& p, int grid, bool cooperative, cudaStream_t st) {
+  if (!cooperative) return launch_stream<FMT, 1>(p, grid, st);
+  // The CTAs of a linked plan wait for one another (stage counters): the
+  // cooperative launch guarantees that all of them are resident at once.
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(stream_kernel<FMT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)Geo<FMT>::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return fail(KQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Geo<FMT>::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  KQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, stream_kernel<FMT, 1>, p));
+  return KQ_OK;
+}
 
 extern "C" {
 
@@ -1013,83 +1462,20 @@ int kq_gemm_splitk(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, in
 
 int kq_decode_plan_create(const kq_qmat* mats, int64_t count, kq_plan** out) {
   clear_error();
-  if (!mats || !out) return fail(KQ_ERR_INVALID_ARG, "NULL pointer");
-  if (count < 1) return fail(KQ_ERR_SHAPE, "count = %lld", (long long)count);
-  *out = nullptr;
-  const int fmt = mats[0].fmt;
-  for (int64_t i = 0; i < count; ++i) {
-    if (int s = check_qmat(&mats[i], -1)) return fail(s, "matrix %lld: %s", (long long)i, kq_last_error());
-    if (mats[i].fmt != fmt) return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: mixed formats in one plan", (long long)i);
-    if (mats[i].k > kXMax)
-      return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: k = %lld > %d", (long long)i, (long long)mats[i].k, kXMax);
-  }
-  int sms = 0;
-  if (int s = device_sms(&sms)) return s;
-  std::vector<Job> jobs((size_t)count);
-  std::vector<CUtensorMap> maps((size_t)(2 * count));
-  std::vector<double> item_bytes;
-  int64_t items = 0, xf = 0, yf = 0, wb = 0;
-  for (int64_t i = 0; i < count; ++i) {
-    const kq_qmat& W = mats[i];
-    if (int s = make_maps(&W, &maps[(size_t)(2 * i)], &maps[(size_t)(2 * i + 1)])) return s;
-    Geometry g = make_geometry(fmt, W.n, W.k, 1, 1);
-    Job& j = jobs[(size_t)i];
-    j = Job{};
-    j.x_off = xf;
-    j.y_off = yf;
-    j.n = W.n;
-    j.k = W.k;
-    j.ldy = W.n;
-    j.item_begin = items;
-    j.items = g.row_blocks;
-    j.row_blocks = g.row_blocks;
-    j.splits = 1;
-    j.split_k = (int32_t)W.k;
-    const double rb = (double)code_row_bytes(fmt, W.k) + 2.0 * (W.k / block_of(fmt));
-    for (int32_t r = 0; r < g.row_blocks; ++r)
-      item_bytes.push_back(rb * (double)std::min<int64_t>(tile_rows(fmt), W.n - (int64_t)r * tile_rows(fmt)));
-    items += g.row_blocks;
-    xf += W.k;
-    yf += W.n;
-    wb += kq_codes_bytes(fmt, W.n, W.k) + W.n * (W.k / block_of(fmt)) * 2;
-  }
-  kq_plan* p = new kq_plan();
-  p->fmt = fmt;
-  p->count = count;
-  p->x_floats = xf;
-  p->y_floats = yf;
-  p->weight_bytes = wb;
-  p->total_items = items;
-  p->grid = (int)std::min<int64_t>(items, sms);
-  // byte-balanced contiguous item ranges, one per CTA
-  std::vector<int64_t> bounds((size_t)p->grid + 1, items);
-  double total = 0;
-  for (double b : item_bytes) total += b;
-  bounds[0] = 0;
-  double accum = 0;
-  int c = 1;
-  for (int64_t it = 0; it < items && c < p->grid; ++it) {
-    accum += item_bytes[(size_t)it];
-    while (c < p->grid && accum >= total * c / p->grid) bounds[(size_t)c++] = it + 1;
-  }
-  for (; c < p->grid; ++c) bounds[(size_t)c] = items;
-  bounds[(size_t)p->grid] = items;
-  cudaError_t e = cudaMalloc(&p->d_jobs, sizeof(Job) * (size_t)count);
-  if (e == cudaSuccess) e = cudaMalloc(&p->d_maps, sizeof(CUtensorMap) * (size_t)(2 * count));
-  if (e == cudaSuccess) e = cudaMalloc(&p->d_bounds, sizeof(int64_t) * (size_t)(p->grid + 1));
-  if (e == cudaSuccess) e = cudaMemcpy(p->d_jobs, jobs.data(), sizeof(Job) * (size_t)count, cudaMemcpyHostToDevice);
-  if (e == cudaSuccess)
-    e = cudaMemcpy(p->d_maps, maps.data(), sizeof(CUtensorMap) * (size_t)(2 * count), cudaMemcpyHostToDevice);
-  if (e == cudaSuccess)
-    e = cudaMemcpy(p->d_bounds, bounds.data(), sizeof(int64_t) * (size_t)(p->grid + 1), cudaMemcpyHostToDevice);
-  if (e != cudaSuccess) {
-    cudaFree(p->d_jobs);
-    cudaFree(p->d_maps);
-    cudaFree(p->d_bounds);
-    delete p;
-    return fail(KQ_ERR_CUDA, "plan allocation: %s", cudaGetErrorString(e));
-  }
-  *out = p;
+  return create_plan(mats, nullptr, count, out);
+}
+
+int kq_decode_plan_create_linked(const kq_qmat* mats, const kq_link* links, int64_t count, kq_plan** out) {
+  clear_error();
+  if (!links) return fail(KQ_ERR_INVALID_ARG, "NULL links");
+  return create_plan(mats, links, count, out);
+}
+
+int kq_decode_plan_stages(const kq_plan* plan, int32_t* stages, int32_t* split_matrices) {
+  clear_error();
+  if (!plan) return fail(KQ_ERR_INVALID_ARG, "NULL plan");
+  if (stages) *stages = plan->nstages;
+  if (split_matrices) *split_matrices = plan->n_split;
   return KQ_OK;
 }
 
@@ -1102,37 +1488,41 @@ int kq_decode_plan_sizes(const kq_plan* plan, int64_t* x_floats, int64_t* y_floa
   return KQ_OK;
 }
 
-size_t kq_decode_workspace_bytes(const kq_plan* plan) {
-  (void)plan;
-  return 0;
-}
+size_t kq_decode_workspace_bytes(const kq_plan* plan) { return plan ? plan->ws_bytes : 0; }
 
 int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, void* d_ws, size_t ws_bytes,
                    void* stream) {
   clear_error();
-  (void)d_ws;
-  (void)ws_bytes;
   if (!plan) return fail(KQ_ERR_INVALID_ARG, "NULL plan");
-  if (!d_x_packed || !d_y_packed) return fail(KQ_ERR_INVALID_ARG, "NULL activation or output");
+  if ((!d_x_packed && plan->x_floats > 0) || !d_y_packed) return fail(KQ_ERR_INVALID_ARG, "NULL activation or output");
   if (!aligned16(d_x_packed) || !aligned16(d_y_packed)) return fail(KQ_ERR_ALIGNMENT, "x or y not 16-byte aligned");
+  if (plan->ws_bytes > 0) {
+    if (!d_ws || ws_bytes < plan->ws_bytes)
+      return fail(KQ_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan->ws_bytes, d_ws ? ws_bytes : 0);
+    if (!aligned16(d_ws)) return fail(KQ_ERR_ALIGNMENT, "workspace not 16-byte aligned");
+  }
+  cudaStream_t st = (cudaStream_t)stream;
   Params p{};
   p.jobs = plan->d_jobs;
   p.maps = plan->d_maps;
+  p.links = plan->d_links;
   p.x_base = d_x_packed;
   p.y_base = d_y_packed;
   p.bounds = plan->d_bounds;
   p.total_items = plan->total_items;
-  if (plan->fmt == KQ_Q8_0) return launch_stream<KQ_Q8_0, 1>(p, plan->grid, (cudaStream_t)stream);
-  return launch_stream<KQ_PQ2_0, 1>(p, plan->grid, (cudaStream_t)stream);
+  p.nstages = plan->nstages;
+  if (plan->linked) {
+    p.stage_done = static_cast<int32_t*>(d_ws);
+    p.ws_base = reinterpret_cast<float*>(static_cast<uint8_t*>(d_ws) + plan->counter_bytes);
+    p.split_jobs = plan->d_split_jobs;
+    p.n_split_jobs = plan->n_split;
+    KQ_CUDA_TRY(cudaMemsetAsync(d_ws, 0, (size_t)plan->nstages * sizeof(int32_t), st));
+  }
+  if (plan->fmt == KQ_Q8_0) return launch_plan<KQ_Q8_0>(p, plan->grid, plan->linked, st);
+  return launch_plan<KQ_PQ2_0>(p, plan->grid, plan->linked, st);
 }
 
-void kq_decode_plan_destroy(kq_plan* plan) {
-  if (!plan) return;
-  cudaFree(plan->d_jobs);
-  cudaFree(plan->d_maps);
-  cudaFree(plan->d_bounds);
-  delete plan;
-}
+void kq_decode_plan_destroy(kq_plan* plan) { destroy_plan(plan); }
 
 // ---------------------------------------------------------------------------
 // Allocation-free split-K GEMM.

@@ -214,7 +214,7 @@ __device__ __forceinline__ int pq2_0_pos(int j) { return j < 8 ? 2 * j : 2 * (j 
 
 template <int FMT>
 __global__ void act_hilo_kernel(const float* __restrict__ X, int m, int mp, int64_t k, __half* __restrict__ B,
-                                float* __restrict__ bscale) {
+                                float* __restrict__ bscale, int had, const int8_t* __restrict__ signs) {
   // one CTA per activation row i < M' (rows i >= m are zero)
   const int i = blockIdx.x;
   __half* hi = B + (int64_t)i * k;
@@ -234,10 +234,20 @@ __global__ void act_hilo_kernel(const float* __restrict__ X, int m, int mp, int6
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   if (FMT == KQ_PQ2_0) {
     // x' = (1/sqrt(128)) H x per 128-block: butterflies of strides 1, 2 in
-    // registers, 4 .. 64 across lanes (each lane holds 4 consecutive values)
-    const float inv_sqrt128 = 0.08838834764831845f;
+    // registers, 4 .. 64 across lanes (each lane holds 4 consecutive values).
+    // The page's n = 1024 rotation (sign flip first) is H_8 (x) H_128 in
+    // Sylvester order: the same 128-point pass unscaled, then an 8-point
+    // pass across the eight 128-blocks of each 1024-block, times 1/32.
+    const float inv_sqrt128 = had == 1024 ? 1.f : 0.08838834764831845f;
     for (int64_t b = warp; b < nblk; b += nwarps) {
-      const float4 f = *reinterpret_cast<const float4*>(x + b * 128 + 4 * lane);
+      float4 f = *reinterpret_cast<const float4*>(x + b * 128 + 4 * lane);
+      if (signs) {
+        const char4 s4 = *reinterpret_cast<const char4*>(signs + b * 128 + 4 * lane);
+        f.x *= (float)s4.x;
+        f.y *= (float)s4.y;
+        f.z *= (float)s4.z;
+        f.w *= (float)s4.w;
+      }
       float v[4];
       const float a0 = f.x + f.y, a1 = f.x - f.y, a2 = f.z + f.w, a3 = f.z - f.w;
       v[0] = a0 + a2;
@@ -254,6 +264,26 @@ __global__ void act_hilo_kernel(const float* __restrict__ X, int m, int mp, int6
       }
       *reinterpret_cast<float4*>(xs + b * 128 + 4 * lane) =
           make_float4(v[0] * inv_sqrt128, v[1] * inv_sqrt128, v[2] * inv_sqrt128, v[3] * inv_sqrt128);
+    }
+    if (had == 1024) {
+      __syncthreads();
+      for (int64_t c = threadIdx.x; c < (k / 1024) * 128; c += blockDim.x) {
+        float* col = xs + (c / 128) * 1024 + (c % 128);
+        float v[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) v[a] = col[a * 128];
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+          for (int a = 0; a < 8; ++a)
+            if (!(a & h)) {
+              const float x0 = v[a], x1 = v[a + h];
+              v[a] = x0 + x1;
+              v[a + h] = x0 - x1;
+            }
+#pragma unroll
+        for (int a = 0; a < 8; ++a) col[a * 128] = v[a] * 0.03125f;
+      }
     }
   } else {
     for (int64_t j = threadIdx.x; j < k; j += blockDim.x) xs[j] = x[j];
@@ -707,7 +737,8 @@ int launch_tc(const tc::TcParams& p, int grid, cudaStream_t st) {
 }
 
 template <int FMT>
-int launch_act(const float* X, int m, int64_t k, int64_t mp, __half* B, float* bscale, cudaStream_t st) {
+int launch_act(const kq_qmat* W, const float* X, int m, int64_t k, int64_t mp, __half* B, float* bscale,
+               cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
@@ -716,7 +747,7 @@ int launch_act(const float* X, int m, int64_t k, int64_t mp, __half* B, float* b
   });
   KQ_CUDA_TRY(attr);
   const int bytes = (int)(k * sizeof(float));
-  tc::act_hilo_kernel<FMT><<<(int)mp, 256, bytes, st>>>(X, m, (int)mp, k, B, bscale);
+  tc::act_hilo_kernel<FMT><<<(int)mp, 256, bytes, st>>>(X, m, (int)mp, k, B, bscale, W->had_block, W->signs);
   KQ_CUDA_TRY(cudaGetLastError());
   return KQ_OK;
 }
@@ -799,9 +830,9 @@ int tc_gemm(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int split
 
   cudaStream_t st = (cudaStream_t)stream;
   if (q8) {
-    if (int s = launch_act<KQ_Q8_0>(d_X, (int)m, W->k, g.mp, B, bscale, st)) return s;
+    if (int s = launch_act<KQ_Q8_0>(W, d_X, (int)m, W->k, g.mp, B, bscale, st)) return s;
   } else {
-    if (int s = launch_act<KQ_PQ2_0>(d_X, (int)m, W->k, g.mp, B, bscale, st)) return s;
+    if (int s = launch_act<KQ_PQ2_0>(W, d_X, (int)m, W->k, g.mp, B, bscale, st)) return s;
   }
   const int grid = (int)std::min<int64_t>((int64_t)g.tiles * g.splits, sms);
   if (int s = q8 ? launch_tc<KQ_Q8_0>(p, grid, st) : launch_tc<KQ_PQ2_0>(p, grid, st)) return s;

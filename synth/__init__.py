@@ -87,6 +87,76 @@ def bonsai_27b_projections():
     return mats
 
 
+# --------------------------------------------------------------------------
+# Dependency structure of a decode step (linked decode plans).  A link is
+# (src, stage, of, alpha), src one of the kinds below (the values of the C
+# ABI's kq_src_kind).  The non-projection operations between projections
+# (attention, norms, activation functions, residuals) are outside the
+# library; each dependent activation is alpha times an earlier projection's
+# output, alpha = 1 / (sigma_w sqrt(k_src)) with sigma_w the spread of the
+# quantized synthetic weights, so that activations stay near unit scale
+# along the chain.
+# --------------------------------------------------------------------------
+SRC_PACKED = 0
+SRC_INPUT_OF = 1
+SRC_OUTPUT_OF = 2
+W_STD_EFF = {Q8_0: 0.0200, PQ2_0: 0.0222}  # std of the dequantized N(0, 0.02) weights of each format
+
+
+def chain_alpha(fmt, k_src):
+    """fp32 scale of the successor activation of a projection with input length k_src."""
+    return float(np.float32(1.0 / (W_STD_EFF[fmt] * np.sqrt(k_src))))
+
+
+def decode_links(config):
+    """One link per projection of a decode-step workload, in list order: the
+    layer's input feeds its first projection group (q/k/v, or GDN qkv/z),
+    the attention output projection reads q's output (prefix) or z's, the FFN
+    gate/up group reads the output projection, down reads up, the next layer
+    reads down, and the head reads the last down.  Stage 4l..4l+3 per layer l."""
+    mats = workload(config)
+    names = [m[0] for m in mats]
+    idx = {name: i for i, name in enumerate(names)}
+
+    def out_of(j, stage):
+        _, fmt, _, k = mats[j]
+        return (SRC_OUTPUT_OF, stage, j, chain_alpha(fmt, k))
+
+    links = [None] * len(mats)
+    prev = None  # index of the previous layer's down projection
+    if config == "qwen3_4b_q8_0_step":
+        layers, pre = 36, "layers."
+        groups = lambda l: (("q_proj", "k_proj", "v_proj"), "q_proj", "o_proj", "gate_proj", "up_proj", "down_proj")
+        head = "lm_head"
+    elif config == "bonsai_27b_pq2_0_step":
+        layers, pre = 64, "blk."
+
+        def groups(l):
+            if l % 4 == 3:
+                return (("attn_q", "attn_k", "attn_v"), "attn_q", "attn_output", "ffn_gate", "ffn_up", "ffn_down")
+            return (("attn_qkv", "attn_gate"), "attn_gate", "ssm_out", "ffn_gate", "ffn_up", "ffn_down")
+
+        head = "output"
+    else:
+        raise KeyError(config)
+    for l in range(layers):
+        first, o_src, o_name, g_name, u_name, d_name = groups(l)
+        at = lambda n: idx[f"{pre}{l}.{n}"]
+        s0 = 4 * l
+        root = at(first[0])
+        links[root] = (SRC_PACKED, s0, 0, 1.0) if prev is None else out_of(prev, s0)
+        for n in first[1:]:
+            links[at(n)] = (SRC_INPUT_OF, s0, root, 1.0)
+        links[at(o_name)] = out_of(at(o_src), s0 + 1)
+        links[at(g_name)] = out_of(at(o_name), s0 + 2)
+        links[at(u_name)] = (SRC_INPUT_OF, s0 + 2, at(g_name), 1.0)
+        links[at(d_name)] = out_of(at(u_name), s0 + 3)
+        prev = at(d_name)
+    links[idx[head]] = out_of(prev, 4 * layers)
+    assert all(lk is not None for lk in links)
+    return links
+
+
 SMALL_M_VALUES = (1, 4, 16, 64)
 SMALL_M_MATRICES = (("q8_0_2560x9728", Q8_0, 9728, 2560), ("pq2_0_5120x17408", PQ2_0, 17408, 5120))
 
@@ -171,6 +241,13 @@ def fill_host(kind, n, seed, stream, first_index=0):
     if n:
         _host_lib().synth_fill_host(out.ctypes.data, int(n), int(seed), int(stream), int(first_index), rng, e)
     return out
+
+
+def sign_vector(k, seed, stream):
+    """k signs (+1 / -1, int8) from the sign bits of a seeded activation
+    stream: the rotation's diagonal S of one K width."""
+    x = fill_host("x", k, seed, stream)
+    return np.where(x < 0, -1, 1).astype(np.int8)
 
 
 def matrix_rows_host(n_rows_total, k, rows, seed, stream):

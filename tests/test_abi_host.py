@@ -90,6 +90,39 @@ def test_host_hadamard_matches_oracle(kq):
         assert np.max(np.abs(kq.kq_hadamard_blockwise_host(x, block) - ref64)) < 1e-4
 
 
+@pytest.mark.parametrize("seed", [0, 1])
+def test_host_ptq1_0_quantizer_matches_oracle_bytes(kq, seed):
+    w = synth.fill_host("w", 40 * 1024, seed, synth.stream_id("test", 0, 204)).reshape(40, 1024)
+    _, w_rot = oracle.rotate_rows(w)
+    assert np.array_equal(kq.kq_quantize_ptq1_0(w_rot), oracle.ptq1_0_quantize(w_rot))
+    rng = np.random.default_rng(seed)
+    wide = (rng.standard_normal((16, 256)) * rng.uniform(1e-6, 50, size=(16, 1))).astype(np.float32)
+    wide[2, :128] = 0
+    assert np.array_equal(kq.kq_quantize_ptq1_0(wide), oracle.ptq1_0_quantize(wide))
+    assert kq.kq_blocks_bytes("ptq1_0", 40, 1024) == 40 * 8 * 28
+    assert kq.kq_codes_bytes("ptq1_0", 40, 1024) == kq.kq_codes_bytes("pq2_0", 40, 1024)
+
+
+def test_host_signed_rotation_matches_oracle(kq):
+    """The page's rotation, n = 1024 with a sign vector, on the host: grid
+    inputs make the block sums exact (bit-identical to the oracle), general
+    inputs agree within a few fp32 rounding steps."""
+    k = 5120
+    signs = np.where(np.random.default_rng(11).random(k) < 0.5, -1, 1).astype(np.int8)
+    w = synth.fill_host("w", 4 * k, 0, synth.stream_id("test", 0, 203)).reshape(4, k)
+    _, ref32 = oracle.rotate_rows(w, 1024, signs=signs)
+    assert np.array_equal(kq.kq_rotate_blockwise_host(w, 1024, signs), ref32)
+    x = np.random.default_rng(5).standard_normal((3, k)).astype(np.float32)
+    ref64, _ = oracle.rotate_rows(x, 1024, signs=signs)
+    got = kq.kq_rotate_blockwise_host(x, 1024, signs)
+    assert np.max(np.abs(got - ref64)) <= 2 * np.finfo(np.float32).eps * np.max(np.abs(ref64))
+    assert np.array_equal(kq.kq_rotate_blockwise_host(x, 128, None), kq.kq_hadamard_blockwise_host(x, 128))
+    bad = signs.copy()
+    bad[9] = 0
+    with pytest.raises(kq.KQError):
+        kq.kq_rotate_blockwise_host(x, 1024, bad)
+
+
 def test_host_errors_leave_output_untouched(kq):
     lib = kq.lib()
     out = np.full(34 * 4, 0xAB, dtype=np.uint8)
@@ -148,6 +181,16 @@ def test_device_entry_points_validate_before_any_cuda_call(kq):
     assert lib.kq_decode_plan_create(mixed, 0, ctypes.byref(h)) == kq.KQ_ERR_SHAPE
     assert lib.kq_decode_step(None, A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
     assert lib.kq_gemv_workspace_bytes(ctypes.byref(bad_k), 1) == 0
+    h1024 = kq.kq_qmat(kq.KQ_PQ2_0, 1024, 8, 1536, A, A)  # k not a multiple of the rotation block
+    assert lib.kq_gemv_pq2_0(ctypes.byref(h1024), A, A, None, 0, None) == kq.KQ_ERR_SHAPE
+    h512 = kq.kq_qmat(kq.KQ_PQ2_0, 512, 8, 1024, A, A)
+    assert lib.kq_gemv_pq2_0(ctypes.byref(h512), A, A, None, 0, None) == kq.KQ_ERR_UNSUPPORTED
+    q8_signs = kq.kq_qmat(kq.KQ_Q8_0, 0, 8, 64, A, A, A)
+    assert lib.kq_gemv_q8_0(ctypes.byref(q8_signs), A, A, None, 0, None) == kq.KQ_ERR_UNSUPPORTED
+    bad_signs = kq.kq_qmat(kq.KQ_PQ2_0, 1024, 8, 1024, A, A, A + 3)
+    assert lib.kq_gemv_pq2_0(ctypes.byref(bad_signs), A, A, None, 0, None) == kq.KQ_ERR_ALIGNMENT
+    assert lib.kq_rotate_blockwise(A, A, 1, 2048, 1024, A + 1, None) == kq.KQ_ERR_ALIGNMENT
+    assert lib.kq_rotate_blockwise(A, A, 1, 1000, 1024, None, None) == kq.KQ_ERR_SHAPE
     assert lib.kq_stream_read(None, 1024, 4096, 4, A, None) == kq.KQ_ERR_INVALID_ARG
     assert lib.kq_stream_read(A, 1000, 4096, 4, A, None) == kq.KQ_ERR_SHAPE
     assert lib.kq_stream_read(A, 0, 4096, 4, A, None) == kq.KQ_ERR_SHAPE
@@ -163,4 +206,4 @@ def test_status_strings(kq):
     for s in range(10):
         assert lib.kq_status_string(s)
     assert lib.kq_status_string(99) == b"unknown status"
-    assert lib.kq_version() == 1
+    assert lib.kq_version() == 2

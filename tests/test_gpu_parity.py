@@ -129,6 +129,25 @@ def test_device_quantizer_and_prepare_bit_exact(kq, wl, fmt, n, k):
     assert torch.equal(W2.codes, W.codes) and torch.equal(W2.scales, W.scales)
 
 
+@pytest.mark.parametrize("n,k", [(300, 5120), (17, 1024), (1000, 128)])
+def test_ptq1_0_transcode_to_pq2_0_planes(kq, wl, n, k):
+    """PTQ1_0 blocks (the page's base-3 download format) transcoded on the
+    device give exactly the PQ2_0 planes of the same rotated weights; the
+    GEMV on them matches the oracle."""
+    sid = synth.stream_id("test", 0, 460 + n)
+    w = synth.fill_host("w", n * k, 8, sid).reshape(n, k)
+    _, w_rot = oracle.rotate_rows(w)
+    ptq = oracle.ptq1_0_quantize(w_rot)
+    W = kq.QMatrix("pq2_0", n, k)
+    kq.kq_prepare(W, torch.from_numpy(ptq.reshape(-1)).cuda(), block_fmt="ptq1_0")
+    _sync_ok(kq)
+    assert np.array_equal(_planes_as_blocks(kq, W), oracle.pq2_0_quantize(w_rot))
+    x = synth.fill_host("x", k, 8, synth.stream_id("test", 1, 461))
+    _, _, y_ref, absdot = oracle.reference("pq2_0", w, x)
+    ok, worst = oracle.within_bound(_run_gemv(kq, W, torch.from_numpy(x).cuda()), y_ref, absdot, TOL)
+    assert ok, worst
+
+
 def test_device_quantizer_flags_nonfinite_and_range(kq):
     W = kq.QMatrix("q8_0", 2, 64)
     w = torch.zeros(128, dtype=torch.float32, device="cuda")
@@ -451,6 +470,234 @@ def test_decode_plan_small_mixed_shapes(kq, wl):
         _sync_ok(kq)
         assert torch.equal(y, y2)
         plan.close()
+
+
+# ----------------------------------------------------------------------------
+# the page's rotation: n = 1024 blocks with a sign vector
+# ----------------------------------------------------------------------------
+
+def _page_reference(w, X, signs):
+    """Oracle with R = H_1024 S / 32: W' = W R^T (rows rotated, then
+    quantized) and x' = R x per activation row.  Returns (blocks, y, absdot)."""
+    n, k = w.shape
+    _, w_rot = oracle.rotate_rows(w, 1024, signs=signs)
+    blocks = oracle.pq2_0_quantize(w_rot)
+    deq = oracle.pq2_0_dequant(blocks, n, k)
+    X = np.atleast_2d(X)
+    y, a = oracle.gemm(deq, oracle.rotate_rows(X, 1024, signs=signs)[0])
+    return blocks, y, a
+
+
+def test_device_signed_rotation_bit_identical_to_host(kq, wl):
+    for k, block in ((6144, 1024), (5120, 1024), (2048, 128)):
+        sh, sd = wl.build_signs(k, 0, synth.stream_id("test", 1, 410 + block))
+        x = np.random.default_rng(k).standard_normal((5, k)).astype(np.float32)
+        out = torch.empty(5 * k, dtype=torch.float32, device="cuda")
+        kq.kq_rotate_blockwise(torch.from_numpy(x).cuda(), out, 5, k, block, sd)
+        _sync_ok(kq)
+        assert np.array_equal(out.cpu().numpy().reshape(5, k), kq.kq_rotate_blockwise_host(x, block, sh))
+
+
+@pytest.mark.parametrize("n,k", [(300, 5120), (64, 17408), (1000, 1024), (40, 6144)])
+@pytest.mark.parametrize("with_signs", [True, False])
+def test_pq2_0_page_rotation_matches_oracle(kq, wl, n, k, with_signs):
+    """PQ2_0 with the page's n = 1024 rotation: device planes equal the
+    oracle's bytes; the GEMV, the split GEMV, the streaming small-M path (the
+    transform passes in the upper half of the staging buffer) and the
+    tensor-core path are within the bound."""
+    sid = synth.stream_id("test", 0, 420 + n)
+    sh, sd = wl.build_signs(k, 1, synth.stream_id("test", 1, 421 + k)) if with_signs else (None, None)
+    W = wl.build_matrix("pq2_0", n, k, 6, sid, had_block=1024, signs=sd)
+    w = synth.fill_host("w", n * k, 6, sid).reshape(n, k)
+    X = synth.fill_host("x", 16 * k, 6, synth.stream_id("test", 1, 422)).reshape(16, k)
+    blocks, y_ref, absdot = _page_reference(w, X, sh)
+    assert np.array_equal(_planes_as_blocks(kq, W), blocks)
+    Xd = torch.from_numpy(X).cuda()
+    y = _run_gemv(kq, W, Xd[0])
+    ok, worst = oracle.within_bound(y, y_ref[0], absdot[0], TOL)
+    assert ok, ("gemv", worst)
+    y3 = _run_gemv(kq, W, Xd[0], splits=3)
+    ok, worst = oracle.within_bound(y3, y_ref[0], absdot[0], TOL)
+    assert ok, ("split 3", worst)
+    for m in (3, 4, 16):
+        Y = torch.empty(m * n, dtype=torch.float32, device="cuda")
+        nb = kq.kq_gemv_workspace_bytes(W, m)
+        ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+        kq.kq_gemm_small_m(W, Xd[:m].reshape(-1), m, Y, ws)
+        _sync_ok(kq)
+        ok, worst = oracle.within_bound(Y.cpu().numpy().reshape(m, n), y_ref[:m], absdot[:m], TOL)
+        assert ok, (m, worst)
+
+
+def test_decode_plans_with_page_rotation(kq, wl):
+    """Unlinked and linked plans over matrices of three K widths sharing one
+    sign vector per width, as on the page."""
+    widths = (5120, 6144, 17408)
+    signs = {k: wl.build_signs(k, 2, synth.stream_id("test", 1, 430 + i)) for i, k in enumerate(widths)}
+    spec = [(6144, 5120), (5120, 6144), (17408, 5120), (5120, 17408)]
+    mats, host, rows = [], [], []
+    rng = np.random.default_rng(8)
+    for i, (n, k) in enumerate(spec):
+        sid = synth.stream_id("test", 0, 440 + i)
+        mats.append(wl.build_matrix("pq2_0", n, k, 7, sid, had_block=1024, signs=signs[k][1]))
+        r = np.unique(np.r_[0, n - 1, rng.integers(0, n, size=30)])  # sampled rows: the oracle is O(n k 1024)
+        rows.append(r)
+        host.append(synth.matrix_rows_host(n, k, r, 7, sid))
+    y_offsets = np.cumsum([0] + [n for n, _ in spec])
+    # unlinked: every matrix its own packed input
+    xs = [synth.fill_host("x", k, 7, synth.stream_id("test", 1, 450 + i)) for i, (_, k) in enumerate(spec)]
+    plan = kq.DecodePlan(mats)
+    y = torch.empty(plan.y_floats, dtype=torch.float32, device="cuda")
+    plan.step(torch.from_numpy(np.concatenate(xs)).cuda(), y)
+    _sync_ok(kq)
+    yh = y.cpu().numpy()
+    for i, (n, k) in enumerate(spec):
+        _, y_ref, absdot = _page_reference(host[i], xs[i], signs[k][0])
+        ok, worst = oracle.within_bound(yh[y_offsets[i] + rows[i]], y_ref[0], absdot[0], TOL)
+        assert ok, ("unlinked", i, worst)
+    plan.close()
+    # linked: 0 -> 1 (prefix of 6144 outputs) -> 2 -> 3, a chain of four stages
+    links = [(0, 0, 0, 1.0), (2, 1, 0, 0.5), (2, 2, 1, 0.25), (2, 3, 2, 0.125)]
+    plan = kq.DecodePlan(mats, links)
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    y = torch.full((plan.y_floats,), float("nan"), dtype=torch.float32, device="cuda")
+    plan.step(torch.from_numpy(xs[0]).cuda(), y, ws)
+    _sync_ok(kq)
+    yh = y.cpu().numpy()
+    xin = _linked_inputs(links, [k for _, k in spec], [xs[0]], yh, y_offsets)
+    for i, (n, k) in enumerate(spec):
+        _, y_ref, absdot = _page_reference(host[i], xin[i], signs[k][0])
+        ok, worst = oracle.within_bound(yh[y_offsets[i] + rows[i]], y_ref[0], absdot[0], TOL)
+        assert ok, ("linked", i, worst)
+    plan.close()
+
+
+def _linked_inputs(links, ks, x_packed, yh, y_offsets):
+    """The activation every matrix of a linked plan reads: its packed slot,
+    its group's input, or fp32(alpha * prefix of an earlier output) computed
+    on the host from the device output."""
+    xin, slot = [], 0
+    for i, (src, _, of, alpha) in enumerate(links):
+        if src == synth.SRC_PACKED:
+            xin.append(x_packed[slot])
+            slot += 1
+        elif src == synth.SRC_INPUT_OF:
+            xin.append(xin[of])
+        else:
+            o = int(y_offsets[of])
+            xin.append((np.float32(alpha) * yh[o:o + ks[i]]).astype(np.float32))
+    return xin
+
+
+# (n, k) and link (src, stage, of, alpha) of a small chain: a grouped stage of
+# three matrices (K split, ragged rows), a prefix of an output with a scale,
+# a group reading an output, an empty stage, a second packed input, and a
+# stage with enough row blocks to need no split
+_CHAIN = [((200, 4096), (0, 0, 0, 1.0)), ((64, 4096), (1, 0, 0, 1.0)), ((300, 4096), (1, 0, 0, 1.0)),
+          ((512, 256), (2, 1, 2, 0.5)), ((1000, 512), (2, 2, 3, 0.125)), ((333, 512), (1, 2, 4, 1.0)),
+          ((256, 896), (2, 4, 4, 0.03125)), ((40, 256), (0, 4, 0, 1.0)), ((40000, 256), (2, 5, 6, 0.0625)),
+          ((96, 128), (2, 6, 8, 3.0))]
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "pq2_0"])
+def test_linked_plan_chain(kq, wl, fmt):
+    mats, host, links = [], [], []
+    for i, ((n, k), lk) in enumerate(_CHAIN):
+        sw = synth.stream_id("test", 0, 360 + i)
+        mats.append(wl.build_matrix(fmt, n, k, 5, sw))
+        host.append(synth.fill_host("w", n * k, 5, sw).reshape(n, k))
+        links.append(lk)
+    plan = kq.DecodePlan(mats, links)
+    assert plan.stages == 7 and plan.split_matrices > 0
+    xp = [synth.fill_host("x", _CHAIN[i][0][1], 5, synth.stream_id("test", 1, 360 + i))
+          for i, lk in enumerate(links) if lk[0] == synth.SRC_PACKED]
+    x = torch.from_numpy(np.concatenate(xp)).cuda()
+    assert plan.x_floats == x.numel()
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    y_offsets = np.cumsum([0] + [W.n for W in mats])
+    outs = []
+    for rep in range(2):
+        # stale data must never be read: outputs and partials start as NaN
+        y = torch.full((plan.y_floats,), float("nan"), dtype=torch.float32, device="cuda")
+        ws.view(torch.float32).fill_(float("nan"))
+        plan.step(x, y, ws)
+        _sync_ok(kq)
+        outs.append(y.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1])  # deterministic
+    yh = outs[0]
+    assert np.isfinite(yh).all()
+    xin = _linked_inputs(links, [W.k for W in mats], xp, yh, y_offsets)
+    for i, (W, w) in enumerate(zip(mats, host)):
+        _, _, y_ref, absdot = oracle.reference(fmt, w, xin[i])
+        ok, worst = oracle.within_bound(yh[y_offsets[i]:y_offsets[i + 1]], y_ref, absdot, TOL)
+        assert ok, (fmt, i, worst)
+    plan.close()
+
+
+def test_linked_plan_rejects_bad_links(kq, wl):
+    mats = [wl.build_matrix("q8_0", 256, 256, 1, synth.stream_id("test", 0, 380 + i)) for i in range(3)]
+    bad = [
+        ([(0, 0, 0, 1.0), (1, 0, 0, 1.0), (2, 0, 1, 1.0)], kq.KQ_ERR_SHAPE),     # output read in its own stage
+        ([(0, 1, 0, 1.0), (0, 0, 0, 1.0), (0, 2, 0, 1.0)], kq.KQ_ERR_SHAPE),     # decreasing stage
+        ([(0, 0, 0, 1.0), (2, 1, 2, 1.0), (0, 2, 0, 1.0)], kq.KQ_ERR_INVALID_ARG),  # not an earlier matrix
+        ([(0, 0, 0, 1.0), (3, 1, 0, 1.0), (0, 2, 0, 1.0)], kq.KQ_ERR_INVALID_ARG),  # unknown kind
+        ([(0, 0, 0, 1.0), (2, 1, 0, float("inf")), (0, 2, 0, 1.0)], kq.KQ_ERR_INVALID_ARG),
+    ]
+    for links, status in bad:
+        with pytest.raises(kq.KQError) as e:
+            kq.DecodePlan(mats, links)
+        assert e.value.status == status, links
+    wide = wl.build_matrix("q8_0", 8, 512, 1, synth.stream_id("test", 0, 383))
+    with pytest.raises(kq.KQError) as e:  # k = 512 exceeds the source's 256 outputs
+        kq.DecodePlan([mats[0], wide], [(0, 0, 0, 1.0), (2, 1, 0, 1.0)])
+    assert e.value.status == kq.KQ_ERR_SHAPE
+    plan = kq.DecodePlan(mats, [(0, 0, 0, 1.0), (2, 1, 0, 1.0), (2, 2, 1, 1.0)])
+    x = torch.zeros(256, dtype=torch.float32, device="cuda")
+    y = torch.empty(plan.y_floats, dtype=torch.float32, device="cuda")
+    with pytest.raises(kq.KQError) as e:
+        plan.step(x, y, None)
+    assert e.value.status == kq.KQ_ERR_WORKSPACE
+    plan.close()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("config", ["qwen3_4b_q8_0_step", "bonsai_27b_pq2_0_step"])
+def test_linked_decode_step_full_size_sampled_rows(kq, wl, config):
+    """The model-ordered chain of a whole decode step (stage by stage, one
+    cooperative launch): sampled rows of every 5th projection and the head,
+    each against the oracle on the activation it read."""
+    W = wl.DecodeWorkload(config, seed=0, linked=True)
+    W.y.fill_(float("nan"))
+    W.step()
+    _sync_ok(kq)
+    y = W.y.cpu().numpy()
+    assert np.isfinite(y).all()
+    ks = [k for _, _, _, k in W.mats_spec]
+    xp = [synth.fill_host("x", ks[i], W.seed, synth.stream_id(config, synth.ROLE_X, i)) for i in W.packed]
+    xin = _linked_inputs(W.links, ks, xp, y, W.y_offsets)
+    rng = np.random.default_rng(1)
+    worst_all = 0.0
+    for i, (_, fmt, n, k) in enumerate(W.mats_spec):
+        if i % 5 and i != len(W.mats_spec) - 1:
+            continue
+        rows = np.unique(np.r_[0, n - 1, rng.integers(0, n, size=6)])
+        w = synth.matrix_rows_host(n, k, rows, W.seed, synth.stream_id(config, synth.ROLE_W, i))
+        if fmt == "pq2_0":
+            deq = oracle.pq2_0_dequant(oracle.pq2_0_quantize(oracle.rotate_rows(w)[1]), rows.size, k)
+            x64 = oracle.rotate_rows(xin[i])[0]
+        else:
+            deq = oracle.q8_0_dequant(oracle.q8_0_quantize(w), rows.size, k)
+            x64 = xin[i].astype(np.float64)
+        y_ref, absdot = oracle.gemv(deq, x64)
+        ok, worst = oracle.within_bound(y[int(W.y_offsets[i]) + rows], y_ref, absdot, TOL)
+        assert ok, (config, i, worst)
+        worst_all = max(worst_all, worst)
+    y2 = W.y.clone()
+    W.step()
+    _sync_ok(kq)
+    assert torch.equal(W.y, y2)
+    print(f"{config} linked: {W.plan.stages} stages, {W.plan.split_matrices} split, worst error/bound {worst_all:.3g}")
+    W.close()
 
 
 @pytest.mark.slow
