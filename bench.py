@@ -176,10 +176,10 @@ def aggregate_gbs(bytes_per_step, steps, seconds_max, world):
 
 
 def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None, world=1, limit=None, linked=False,
-                    e2e=True):
+                    e2e=True, rotation=None):
     import torch
 
-    W = wl_mod.DecodeWorkload(config, seed=0, limit=limit, linked=linked)
+    W = wl_mod.DecodeWorkload(config, seed=0, limit=limit, linked=linked, rotation=rotation)
     bytes_per_step = W.weight_bytes + W.activation_bytes
     for _ in range(warmup):
         W.step(stream)
@@ -380,6 +380,18 @@ def run_kq(args):
                           "frac_of_control": round(ch["gbs"] / control["gbs"], 4), "stages": ch["stages"],
                           "split_matrices": ch["split_matrices"], "matrices": ch["matrices"]}
         extras["decode_chain"] = chain
+        # more decode streams: the Qwen3-4B projections in scale4_gs32, and the
+        # Bonsai step with the page's own rotation (n = 1024, a sign vector per K width)
+        more = {}
+        for key, cfg, rot in (("qwen3_4b_scale4_step", "qwen3_4b_scale4_step", None),
+                              ("bonsai_27b_pq2_0_step_page_rotation", HEADLINE, "page")):
+            r = _decode_measure(kq, workloads, cfg, max(3, args.steps // 4), args.warmup, stream, e2e=False,
+                                rotation=rot)
+            more[key] = {"gbs": round(r["gbs"], 1), "us_per_step": round(r["per_step_s"] * 1e6, 2),
+                         "frac_of_measured_hbm": round(r["gbs"] / peak, 4),
+                         "frac_of_control": round(r["gbs"] / control["gbs"], 4), "weight_bytes": r["weight_bytes"],
+                         "matrices": r["matrices"]}
+        extras["decode_steps"].update(more)
         gemv = []
         for fmt, n, k, m in (("q8_0", 1024, 2560, 1), ("pq2_0", 10240, 5120, 1), ("q8_0", 9728, 2560, 1),
                              ("q8_0", 9728, 2560, 4), ("q8_0", 9728, 2560, 16), ("q8_0", 9728, 2560, 64),

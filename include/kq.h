@@ -12,6 +12,12 @@
  *          34 bytes per block, i.e. 136 bytes per 128-dim row as printed in
  *          "Kipp Benchmarks", Quantized KV cache bullet).
  *
+ *   SCALE4 scale4_gs32 ("Kipp Benchmarks", section "Scale-only 4-bit
+ *          (scale4_gs32)"): 32 weights per block, an fp16 scale d first and
+ *          16 bytes of 4-bit codes q, value d*(q-8); d = (the block's weight
+ *          of largest magnitude, with its sign) / -8, the codes quantized
+ *          against the fp16-rounded d (18 bytes, 4.5 bits per weight).
+ *
  *   PQ2_0  128 weights per block: an fp16 scale d and 2-bit codes
  *          q in {0,1,2}, element j in byte j/4 at bit offset 2*(j%4), value
  *          (q-1)*d, d = max|w| and q = round(w/d)+1 ("Bonsai 2 27B - ternary
@@ -44,6 +50,9 @@
  *           PQ2_0: uint32 [n][k/16], row stride k/4 bytes; each 32-bit word
  *           (little endian) holds elements 16i..16i+15 of its row at bits 2j,
  *           which is the byte order of the block's qs[] read as words.
+ *           SCALE4: bytes [n][k/2], row stride k/2; element j of a row in
+ *           byte j/2 at bit offset 4 (j % 2), which is the blocks' nibble
+ *           bytes concatenated (a 32-bit word holds elements 8i..8i+7).
  *  - scales fp16 [n][kq_scale_stride(fmt, k)]; entry [r][b] is the scale of
  *           block b of row r; the padding entries of each row are zero.
  */
@@ -75,7 +84,7 @@ typedef enum {
  * bits per weight; the page ships it as a download option and unpacks it to
  * the PQ2_0 words at load time).  kq_prepare turns PTQ1_0 blocks into PQ2_0
  * planes; every GEMV runs on those. */
-typedef enum { KQ_Q8_0 = 0, KQ_PQ2_0 = 1, KQ_PTQ1_0 = 2 } kq_format;
+typedef enum { KQ_Q8_0 = 0, KQ_PQ2_0 = 1, KQ_PTQ1_0 = 2, KQ_SCALE4 = 3 } kq_format;
 
 /* A quantized matrix resident in device memory (planes as described above).
  * had_block is the Hadamard block n of the fold: 128 or 1024 for PQ2_0 (k a
@@ -100,9 +109,9 @@ const char* kq_last_error(void);
 /* ABI version, bumped on incompatible change. */
 int kq_version(void);
 
-/* Weights per block: 32 (Q8_0) or 128 (PQ2_0, PTQ1_0); 0 for an unknown format. */
+/* Weights per block: 32 (Q8_0, SCALE4) or 128 (PQ2_0, PTQ1_0); 0 for an unknown format. */
 int64_t kq_block_size(int fmt);
-/* Bytes of one block (34 for Q8_0 and PQ2_0, 28 for PTQ1_0) times the number
+/* Bytes of one block (34 for Q8_0 and PQ2_0, 28 for PTQ1_0, 18 for SCALE4) times the number
  * of blocks of an n x k matrix.  The plane queries below give, for PTQ1_0,
  * the PQ2_0 planes kq_prepare writes. */
 int64_t kq_blocks_bytes(int fmt, int64_t n, int64_t k);
@@ -125,6 +134,15 @@ int kq_quantize_q8_0(const float* w, int64_t n, int64_t k, void* blocks);
  * whose fp16 scale is zero gets code 1.  Output: n*k/128 blocks of 34 bytes.
  * Errors: KQ_ERR_SHAPE (k % 128), KQ_ERR_NONFINITE, KQ_ERR_RANGE. */
 int kq_quantize_pq2_0(const float* w_rot, int64_t n, int64_t k, void* blocks);
+
+/* SCALE4 per row and 32-block: m = the weight of largest magnitude (the
+ * first on a tie), d = fp16(m / -8) (fp32 quotient, then round to nearest
+ * even), q = round-half-away-from-zero(w / float(d)) + 8 clamped to
+ * [0, 15]; a block whose fp16 scale is zero gets q = 8.  Output: n*k/32
+ * blocks of 18 bytes (d little endian, then element j in byte 2 + j/2 at bit
+ * offset 4 (j % 2)).  Errors: KQ_ERR_SHAPE (k % 32), KQ_ERR_NONFINITE,
+ * KQ_ERR_RANGE. */
+int kq_quantize_scale4(const float* w, int64_t n, int64_t k, void* blocks);
 
 /* PTQ1_0 per row and 128-block of the ROTATED weights: the PQ2_0 scale and
  * trits (same rules as kq_quantize_pq2_0) packed in base 3: 24 bytes of five
@@ -158,6 +176,7 @@ int kq_prepare(int fmt, const void* d_blocks, int64_t n, int64_t k, void* d_code
 int kq_quantize_q8_0_device(const float* d_w, int64_t n, int64_t k, void* d_codes, void* d_scales, void* stream);
 int kq_quantize_pq2_0_device(const float* d_w_rot, int64_t n, int64_t k, void* d_codes, void* d_scales,
                              void* stream);
+int kq_quantize_scale4_device(const float* d_w, int64_t n, int64_t k, void* d_codes, void* d_scales, void* stream);
 
 /* Debug: write the dequantized n x k fp32 matrix (d*q or (q-1)*d, exact). */
 int kq_dequantize(const kq_qmat* W, float* d_out, void* stream);
@@ -189,6 +208,9 @@ size_t kq_gemv_workspace_bytes(const kq_qmat* W, int64_t m);
 
 /* y[n] = W x for a Q8_0 matrix: d_x fp32 [k], d_y fp32 [n]. */
 int kq_gemv_q8_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
+
+/* y[n] = W x for a SCALE4 matrix: d_x fp32 [k], d_y fp32 [n]. */
+int kq_gemv_scale4(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
 
 /* y[n] = W' (R x) for a PQ2_0 matrix: d_x is the UNROTATED fp32 activation
  * [k]; the blockwise transform runs in the kernel's activation prologue. */

@@ -39,7 +39,8 @@ KQ_ERR_UNSUPPORTED = 9
 KQ_Q8_0 = 0
 KQ_PQ2_0 = 1
 KQ_PTQ1_0 = 2  # storage format: kq_prepare transcodes it to PQ2_0 planes
-FORMATS = {"q8_0": KQ_Q8_0, "pq2_0": KQ_PQ2_0, "ptq1_0": KQ_PTQ1_0}
+KQ_SCALE4 = 3  # scale4_gs32
+FORMATS = {"q8_0": KQ_Q8_0, "pq2_0": KQ_PQ2_0, "ptq1_0": KQ_PTQ1_0, "scale4": KQ_SCALE4}
 
 
 class KQError(RuntimeError):
@@ -84,6 +85,9 @@ SIGNATURES = {
     "kq_quantize_q8_0": (ctypes.c_int, [_P, _I64, _I64, _P]),
     "kq_quantize_pq2_0": (ctypes.c_int, [_P, _I64, _I64, _P]),
     "kq_quantize_ptq1_0": (ctypes.c_int, [_P, _I64, _I64, _P]),
+    "kq_quantize_scale4": (ctypes.c_int, [_P, _I64, _I64, _P]),
+    "kq_quantize_scale4_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
+    "kq_gemv_scale4": (ctypes.c_int, [_QP, _P, _P, _P, _SZ, _P]),
     "kq_hadamard_blockwise_host": (ctypes.c_int, [_P, _P, _I64, _I64, _I32]),
     "kq_prepare": (ctypes.c_int, [ctypes.c_int, _P, _I64, _I64, _P, _P, _P]),
     "kq_quantize_q8_0_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
@@ -194,6 +198,14 @@ def kq_quantize_pq2_0(w_rot):
     return out[: n * (k // 128) * 34].reshape(n, k // 128, 34)
 
 
+def kq_quantize_scale4(w):
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    n, k = w.shape
+    out = np.zeros(max(kq_blocks_bytes("scale4", n, k), 1), dtype=np.uint8)
+    _check(_lib.kq_quantize_scale4(w.ctypes.data, n, k, out.ctypes.data), "kq_quantize_scale4")
+    return out[: n * (k // 32) * 18].reshape(n, k // 32, 18)
+
+
 def kq_quantize_ptq1_0(w_rot):
     w = np.ascontiguousarray(w_rot, dtype=np.float32)
     n, k = w.shape
@@ -265,6 +277,11 @@ def kq_quantize_pq2_0_device(W, d_w_rot, stream=None):
                                          _stream(stream)), "kq_quantize_pq2_0_device")
 
 
+def kq_quantize_scale4_device(W, d_w, stream=None):
+    _check(_lib.kq_quantize_scale4_device(_ptr(d_w), W.n, W.k, W.codes.data_ptr(), W.scales.data_ptr(),
+                                          _stream(stream)), "kq_quantize_scale4_device")
+
+
 def kq_dequantize(W, d_out, stream=None):
     _check(_lib.kq_dequantize(ctypes.byref(W.desc), _ptr(d_out), _stream(stream)), "kq_dequantize")
 
@@ -306,6 +323,11 @@ def _ws(ws):
 def kq_gemv_q8_0(W, d_x, d_y, ws=None, stream=None):
     p, nb = _ws(ws)
     _check(_lib.kq_gemv_q8_0(ctypes.byref(W.desc), _ptr(d_x), _ptr(d_y), p, nb, _stream(stream)), "kq_gemv_q8_0")
+
+
+def kq_gemv_scale4(W, d_x, d_y, ws=None, stream=None):
+    p, nb = _ws(ws)
+    _check(_lib.kq_gemv_scale4(ctypes.byref(W.desc), _ptr(d_x), _ptr(d_y), p, nb, _stream(stream)), "kq_gemv_scale4")
 
 
 def kq_gemv_pq2_0(W, d_x, d_y, ws=None, stream=None):

@@ -32,7 +32,8 @@ void clear_error() { g_last_error[0] = 0; }
 
 int check_qmat(const kq_qmat* W, int expect_fmt) {
   if (!W) return fail(KQ_ERR_INVALID_ARG, "W is NULL");
-  if (W->fmt != KQ_Q8_0 && W->fmt != KQ_PQ2_0) return fail(KQ_ERR_INVALID_ARG, "unknown format %d", W->fmt);
+  if (W->fmt != KQ_Q8_0 && W->fmt != KQ_PQ2_0 && W->fmt != KQ_SCALE4)
+    return fail(KQ_ERR_INVALID_ARG, "unknown matrix format %d", W->fmt);
   if (expect_fmt >= 0 && W->fmt != expect_fmt)
     return fail(KQ_ERR_INVALID_ARG, "format %d given to an entry point for format %d", W->fmt, expect_fmt);
   if (W->n < 1) return fail(KQ_ERR_SHAPE, "n = %lld < 1", (long long)W->n);
@@ -45,8 +46,8 @@ int check_qmat(const kq_qmat* W, int expect_fmt) {
     if (W->k % W->had_block != 0)
       return fail(KQ_ERR_SHAPE, "k = %lld is not a multiple of had_block = %d", (long long)W->k, W->had_block);
   } else {
-    if (W->had_block != 0) return fail(KQ_ERR_UNSUPPORTED, "had_block = %d (Q8_0 takes 0)", W->had_block);
-    if (W->signs) return fail(KQ_ERR_UNSUPPORTED, "signs given for a Q8_0 matrix");
+    if (W->had_block != 0) return fail(KQ_ERR_UNSUPPORTED, "had_block = %d (this format takes 0)", W->had_block);
+    if (W->signs) return fail(KQ_ERR_UNSUPPORTED, "signs given for a matrix without rotation");
   }
   if (!W->codes || !W->scales) return fail(KQ_ERR_INVALID_ARG, "NULL plane pointer");
   if (!aligned16(W->codes) || !aligned16(W->scales)) return fail(KQ_ERR_ALIGNMENT, "plane not 16-byte aligned");
@@ -193,6 +194,46 @@ int kq_quantize_pq2_0(const float* w_rot, int64_t n, int64_t k, void* blocks) {
         if (d != 0.0) t = std::lround(static_cast<double>(src[j]) / d);
         t = t > 1 ? 1 : (t < -1 ? -1 : t);
         blk[2 + j / 4] |= static_cast<uint8_t>((t + 1) << (2 * (j % 4)));
+      }
+    }
+  }
+  return KQ_OK;
+}
+
+int kq_quantize_scale4(const float* w, int64_t n, int64_t k, void* blocks) {
+  clear_error();
+  if (int s = check_host_weights(w, n, k, 32, blocks)) return s;
+  const int64_t nb = k / 32;
+  // First pass: scales only, so that a range error leaves the output untouched.
+  std::vector<uint16_t> dh(static_cast<size_t>(n * nb));
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* src = w + r * k + b * 32;
+      float m = 0.f;  // the weight of largest magnitude, with its sign, the first on a tie
+      for (int j = 0; j < 32; ++j)
+        if (std::fabs(src[j]) > std::fabs(m)) m = src[j];
+      uint16_t h = half_bits_rn(m / -8.0f);
+      if ((h & 0x7C00u) == 0x7C00u)
+        return fail(KQ_ERR_RANGE, "row %lld block %lld: scale %g overflows fp16", (long long)r, (long long)b,
+                    (double)(m / -8.0f));
+      dh[static_cast<size_t>(r * nb + b)] = h;
+    }
+  }
+  uint8_t* out = static_cast<uint8_t*>(blocks);
+  for (int64_t r = 0; r < n; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* src = w + r * k + b * 32;
+      uint8_t* blk = out + (r * nb + b) * 18;
+      const uint16_t h = dh[static_cast<size_t>(r * nb + b)];
+      const double d = half_to_float(h);
+      blk[0] = static_cast<uint8_t>(h & 0xFF);
+      blk[1] = static_cast<uint8_t>(h >> 8);
+      std::memset(blk + 2, 0, 16);
+      for (int j = 0; j < 32; ++j) {
+        long q = 8;
+        if (d != 0.0) q = std::lround(static_cast<double>(src[j]) / d) + 8;
+        q = q > 15 ? 15 : (q < 0 ? 0 : q);
+        blk[2 + j / 2] |= static_cast<uint8_t>(q << (4 * (j % 2)));
       }
     }
   }

@@ -18,13 +18,13 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // Weights per block; PTQ1_0 (a storage format) has the PQ2_0 planes.
 inline int64_t block_of(int fmt) {
-  return fmt == KQ_Q8_0 ? 32 : ((fmt == KQ_PQ2_0 || fmt == KQ_PTQ1_0) ? 128 : 0);
+  return (fmt == KQ_Q8_0 || fmt == KQ_SCALE4) ? 32 : ((fmt == KQ_PQ2_0 || fmt == KQ_PTQ1_0) ? 128 : 0);
 }
 inline int plane_format(int fmt) { return fmt == KQ_PTQ1_0 ? KQ_PQ2_0 : fmt; }
-inline int64_t block_bytes(int fmt) { return fmt == KQ_PTQ1_0 ? 28 : 34; }
+inline int64_t block_bytes(int fmt) { return fmt == KQ_PTQ1_0 ? 28 : (fmt == KQ_SCALE4 ? 18 : 34); }
 inline int64_t round_up(int64_t v, int64_t m) { return (v + m - 1) / m * m; }
 inline int64_t scale_stride(int fmt, int64_t k) { return round_up(k / block_of(fmt), 8); }
-inline int64_t code_row_bytes(int fmt, int64_t k) { return fmt == KQ_Q8_0 ? k : k / 4; }
+inline int64_t code_row_bytes(int fmt, int64_t k) { return fmt == KQ_Q8_0 ? k : (fmt == KQ_SCALE4 ? k / 2 : k / 4); }
 
 // Checks a kq_qmat descriptor (format, shape, plane pointers and alignment).
 int check_qmat(const kq_qmat* W, int expect_fmt);

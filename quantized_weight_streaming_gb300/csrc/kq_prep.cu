@@ -22,16 +22,17 @@ __device__ __forceinline__ void prep_flag(int status) { atomicOr(&g_prep_status,
 // AoS 34-byte blocks -> planes.  Both formats keep the code bytes in block
 // order, so the codes plane is the concatenation of the blocks' code bytes.
 // --------------------------------------------------------------------------
-__global__ void prepare_kernel(const uint8_t* __restrict__ blocks, int64_t n, int64_t nb, int64_t sstride,
+// A block is the fp16 scale then cb code bytes (32 for Q8_0 and PQ2_0, 16 for
+// SCALE4); the code bytes of a row's blocks are concatenated in the plane.
+__global__ void prepare_kernel(const uint8_t* __restrict__ blocks, int64_t n, int64_t nb, int64_t sstride, int cb,
                                uint8_t* __restrict__ codes, uint16_t* __restrict__ scales) {
   int64_t total = n * nb;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     int64_t r = i / nb, b = i % nb;
-    const uint8_t* blk = blocks + i * 34;
+    const uint8_t* blk = blocks + i * (2 + cb);
     scales[r * sstride + b] = (uint16_t)(blk[0] | (blk[1] << 8));
-    uint8_t* dst = codes + i * 32;  // row r, bytes b*32 .. b*32+31 (row stride nb*32)
-#pragma unroll
-    for (int j = 0; j < 32; ++j) dst[j] = blk[2 + j];
+    uint8_t* dst = codes + i * cb;  // row r, bytes b*cb .. (row stride nb*cb)
+    for (int j = 0; j < cb; ++j) dst[j] = blk[2 + j];
   }
 }
 
@@ -100,6 +101,43 @@ __global__ void quantize_q8_0_kernel(const float* __restrict__ w, int64_t n, int
     double q = 0.0;
     if (d != 0.0) q = fmin(127.0, fmax(-127.0, round((double)v / d)));
     codes[r * k + b * 32 + lane] = (int8_t)q;
+    if (lane == 0) scales[r * sstride + b] = __half_as_ushort(dh);
+  }
+}
+
+// SCALE4: lane j of the warp holds weight j of the 32-block; the signed
+// weight of largest magnitude (the first on a tie) by a warp reduction on
+// (magnitude, -index).
+__global__ void quantize_scale4_kernel(const float* __restrict__ w, int64_t n, int64_t k, int64_t sstride,
+                                       uint8_t* __restrict__ codes, uint16_t* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nb = k / 32;
+  const int64_t total = n * nb;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t i = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; i < total; i += warps) {
+    int64_t r = i / nb, b = i % nb;
+    const float v = w[r * k + b * 32 + lane];
+    if (!isfinite(v)) prep_flag(KQ_ERR_NONFINITE);
+    float a = fabsf(v);
+    int at = lane;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float a2 = __shfl_xor_sync(0xffffffffu, a, o);
+      const int at2 = __shfl_xor_sync(0xffffffffu, at, o);
+      if (a2 > a || (a2 == a && at2 < at)) {
+        a = a2;
+        at = at2;
+      }
+    }
+    const float m = __shfl_sync(0xffffffffu, v, at);
+    const __half dh = __float2half_rn(m / -8.0f);
+    if (__hisinf(dh)) prep_flag(KQ_ERR_RANGE);
+    const double d = (double)__half2float(dh);
+    int q = 8;
+    if (d != 0.0) q = (int)fmin(15.0, fmax(0.0, round((double)v / d) + 8.0));
+    // two lanes per byte: the even lane's nibble low, the odd lane's high
+    const int other = __shfl_xor_sync(0xffffffffu, q, 1);
+    if (!(lane & 1)) codes[r * (k / 2) + b * 16 + lane / 2] = (uint8_t)(q | (other << 4));
     if (lane == 0) scales[r * sstride + b] = __half_as_ushort(dh);
   }
 }
@@ -214,6 +252,10 @@ __global__ void dequant_kernel(int fmt, const uint8_t* __restrict__ codes, const
     if (fmt == KQ_Q8_0) {
       float d = __half2float(__ushort_as_half(scales[r * sstride + c / 32]));
       out[i] = (float)(int8_t)codes[i] * d;
+    } else if (fmt == KQ_SCALE4) {
+      float d = __half2float(__ushort_as_half(scales[r * sstride + c / 32]));
+      int q = (codes[r * (k / 2) + c / 2] >> (4 * (c % 2))) & 15;
+      out[i] = (float)(q - 8) * d;
     } else {
       float d = __half2float(__ushort_as_half(scales[r * sstride + c / 128]));
       int code = (codes[r * (k / 4) + c / 4] >> (2 * (c % 4))) & 3;
@@ -269,7 +311,8 @@ int kq_prepare(int fmt, const void* d_blocks, int64_t n, int64_t k, void* d_code
     prepare_ptq1_0_kernel<<<grid_for(n * nb, 256), 256, 0, st>>>((const uint8_t*)d_blocks, n, nb, ss,
                                                                  (uint8_t*)d_codes, (uint16_t*)d_scales);
   else
-    prepare_kernel<<<grid_for(n * nb, 256), 256, 0, st>>>((const uint8_t*)d_blocks, n, nb, ss, (uint8_t*)d_codes,
+    prepare_kernel<<<grid_for(n * nb, 256), 256, 0, st>>>((const uint8_t*)d_blocks, n, nb, ss,
+                                                          (int)(block_bytes(fmt) - 2), (uint8_t*)d_codes,
                                                           (uint16_t*)d_scales);
   KQ_CUDA_TRY(cudaGetLastError());
   if (ss > nb) {
@@ -294,6 +337,8 @@ static int quantize_device(int fmt, const float* d_w, int64_t n, int64_t k, void
   int grid = grid_for(n * nb * 32, 256);
   if (fmt == KQ_Q8_0)
     quantize_q8_0_kernel<<<grid, 256, 0, st>>>(d_w, n, k, ss, (int8_t*)d_codes, (uint16_t*)d_scales);
+  else if (fmt == KQ_SCALE4)
+    quantize_scale4_kernel<<<grid, 256, 0, st>>>(d_w, n, k, ss, (uint8_t*)d_codes, (uint16_t*)d_scales);
   else
     quantize_pq2_0_kernel<<<grid, 256, 0, st>>>(d_w, n, k, ss, (uint8_t*)d_codes, (uint16_t*)d_scales);
   KQ_CUDA_TRY(cudaGetLastError());
@@ -307,6 +352,10 @@ int kq_quantize_q8_0_device(const float* d_w, int64_t n, int64_t k, void* d_code
 int kq_quantize_pq2_0_device(const float* d_w_rot, int64_t n, int64_t k, void* d_codes, void* d_scales,
                              void* stream) {
   return quantize_device(KQ_PQ2_0, d_w_rot, n, k, d_codes, d_scales, stream);
+}
+
+int kq_quantize_scale4_device(const float* d_w, int64_t n, int64_t k, void* d_codes, void* d_scales, void* stream) {
+  return quantize_device(KQ_SCALE4, d_w, n, k, d_codes, d_scales, stream);
 }
 
 int kq_dequantize(const kq_qmat* W, float* d_out, void* stream) {

@@ -61,7 +61,8 @@ constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr int kRowsPerWarp = 8;   // Q8_0 rows per consumer warp
 constexpr int kChunkBytes = 256;  // code bytes per row per tile (32 lanes x 8 B)
 constexpr int kXMax = 18432;          // activation floats (or B-fragment words) staged per item (all m)
-constexpr int kBlkMax = kXMax / 128;  // PQ2_0 per-block side arrays
+constexpr int kXMaxScale4 = 16384;    // the same for SCALE4, whose larger ring leaves less room
+__host__ __device__ constexpr int xmax_of(int fmt) { return fmt == KQ_SCALE4 ? kXMaxScale4 : kXMax; }
 constexpr int kScratchFloats = 128;   // per-warp scratch (one Hadamard block)
 
 // Per-format tile geometry.  Q8_0: 128-row tiles (16 warps x 8 rows), a
@@ -71,20 +72,28 @@ constexpr int kScratchFloats = 128;   // per-warp scratch (one Hadamard block)
 // combine buffer shares its space with the staging scratch: the two are
 // never in use at the same time (staging runs between CTA-wide barriers,
 // after every warp has finished its handoffs).
+// SCALE4 has the PQ2_0 geometry with 32-weight blocks: 16 fp16 scales per
+// tile row and 512 weights (256 bytes) of codes.
 template <int FMT>
 struct Geo {
-  static constexpr int kTileRows = FMT == KQ_PQ2_0 ? 256 : 128;
+  static constexpr bool kMma = FMT != KQ_Q8_0;  // PQ2_0 and SCALE4 run on mma.sync
+  static constexpr int kTileRows = kMma ? 256 : 128;
   static constexpr int kTileCodeBytes = kTileRows * kChunkBytes;
-  static constexpr int kTileScaleBytes = kTileRows * 16;  // 8 fp16 scales per row per tile
+  static constexpr int kScalesPerRow = FMT == KQ_SCALE4 ? 16 : 8;  // fp16 scales per row per tile
+  static constexpr int kTileScaleBytes = kTileRows * kScalesPerRow * 2;
   static constexpr int kStageBytes = kTileCodeBytes + kTileScaleBytes;
-  static constexpr int kStages = FMT == KQ_PQ2_0 ? 2 : 4;
-  static constexpr int kCombineFloats = FMT == KQ_PQ2_0 ? 4 * 3 * 32 * 8 : 0;  // 4 row groups x 3 handing warps
+  static constexpr int kStages = kMma ? 2 : 4;
+  static constexpr int kXMaxF = xmax_of(FMT);
+  static constexpr int kBlkMax = kXMaxF / (FMT == KQ_SCALE4 ? 32 : 128);  // per-block side arrays (mma formats)
+  static constexpr int kCombineFloats = kMma ? 4 * 3 * 32 * 8 : 0;  // 4 row groups x 3 handing warps
   static constexpr int kScratchRegion =
       kConsumerWarps * kScratchFloats > kCombineFloats ? kConsumerWarps * kScratchFloats : kCombineFloats;
-  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kXMax * 4 + 2 * (size_t)kBlkMax * 4 +
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + (size_t)kXMaxF * 4 + 2 * (size_t)kBlkMax * 4 +
                                        (size_t)kScratchRegion * 4 + 2 * kStages * 8 + 8 * 8 + 16;
 };
-constexpr int tile_rows(int fmt) { return fmt == KQ_PQ2_0 ? Geo<KQ_PQ2_0>::kTileRows : Geo<KQ_Q8_0>::kTileRows; }
+constexpr int tile_rows(int fmt) { return fmt == KQ_Q8_0 ? Geo<KQ_Q8_0>::kTileRows : Geo<KQ_PQ2_0>::kTileRows; }
+static_assert(Geo<KQ_SCALE4>::kSmemBytes <= 232448, "SCALE4 shared memory");
+static_assert(Geo<KQ_PQ2_0>::kSmemBytes <= 232448, "PQ2_0 shared memory");
 
 __device__ unsigned int g_stream_status = 0;
 __device__ __forceinline__ void stream_flag(int status) { atomicOr(&g_stream_status, 1u << status); }
@@ -147,6 +156,13 @@ struct Fmt<KQ_PQ2_0> {
   static constexpr int kCodesPerByte = 4;
   static constexpr int kChunk = kChunkBytes * 4;  // 1024 weights per tile row
   static constexpr int kGran = 32;
+};
+template <>
+struct Fmt<KQ_SCALE4> {
+  static constexpr int kBlock = 32;
+  static constexpr int kCodesPerByte = 2;
+  static constexpr int kChunk = kChunkBytes * 2;  // 512 weights per tile row
+  static constexpr int kGran = 16;
 };
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
@@ -367,6 +383,13 @@ __device__ __forceinline__ int btab_index(int b, int q, int j, int n, int t) {
   return (((b * 2 + q) * 4 + j) * (2 * M) + n) * 4 + t;
 }
 
+// SCALE4 B table entry (uint2) of (32-block b of the slice, MMA j, column n,
+// thread t): 16 M entries of 8 bytes per block, again 4 M bytes per position.
+template <int M>
+__device__ __forceinline__ int btab4_index(int b, int j, int n, int t) {
+  return ((b * 2 + j) * (2 * M) + n) * 4 + t;
+}
+
 // Unnormalised 128-point Walsh-Hadamard transform, natural (Sylvester) order,
 // of a block held 4 consecutive elements per lane: strides 1 and 2 in
 // registers, 4 .. 64 across lanes.
@@ -402,6 +425,50 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
     for (int m = 0; m < M; ++m) {
       for (int i = cw * 32 + lane; i < len / 4; i += kT)
         xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] = load_x4(xs, m, kbeg + 4 * i);
+    }
+  } else if (FMT == KQ_SCALE4) {
+    // A warp takes 128 positions (four 32-blocks, eight lanes per block) at a
+    // time: per block the exponent E of its largest |x|, 8 * sum(x) (the
+    // implicit zero point) and the B table entries, x * 2^-E as fp16 high and
+    // low parts scaled by 2^(14-s) to match the code's bit offset s.
+    uint2* btab = reinterpret_cast<uint2*>(xbuf);
+    const int ngrp = (len + 127) / 128;  // the last group may hold fewer than four blocks
+    for (int tt = cw; tt < M * ngrp; tt += kConsumerWarps) {
+      const int m = tt / ngrp, q = tt % ngrp;
+      // len is a multiple of 32: a block's eight lanes are all inside or all past the slice
+      const bool inside = q * 128 + 4 * lane < len;
+      const float4 f = inside ? load_x4(xs, m, kbeg + q * 128 + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float amax = fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)));
+      float ssum = (f.x + f.y) + (f.z + f.w);
+#pragma unroll
+      for (int mk = 1; mk < 8; mk <<= 1) {
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, mk));
+        ssum += __shfl_xor_sync(0xffffffffu, ssum, mk);
+      }
+      int e = amax > 0.f ? ((__float_as_int(amax) >> 23) & 0xFF) - 127 : 0;
+      if (amax > 0.f && e == -127) e = -126;
+      e = max(-100, min(100, e));
+      const float unscale = pow2f(-e);
+      __syncwarp();
+      *reinterpret_cast<float4*>(scratch + 4 * lane) =
+          make_float4(f.x * unscale, f.y * unscale, f.z * unscale, f.w * unscale);
+      __syncwarp();
+      // lane (block bq, MMA j, thread t): word t of the block, elements 2j,
+      // 2j+4 (bit offset 0) and 2j+1, 2j+5 (bit offset 4) after the shift by 8j
+      const int bq = lane >> 3, j = (lane >> 2) & 1, t = lane & 3;
+      const float* xw = scratch + 32 * bq + 8 * t;
+      const float u0 = xw[2 * j] * 16384.f, u1 = xw[2 * j + 4] * 16384.f;
+      const float u2 = xw[2 * j + 1] * 1024.f, u3 = xw[2 * j + 5] * 1024.f;
+      const float h0 = __half2float(__float2half_rn(u0)), h1 = __half2float(__float2half_rn(u1));
+      const float h2 = __half2float(__float2half_rn(u2)), h3 = __half2float(__float2half_rn(u3));
+      const int gb = q * 4 + bq;  // block inside the slice
+      if (!inside) continue;       // (no further shuffle in this iteration)
+      btab[btab4_index<M>(gb, j, 2 * m, t)] = make_uint2(pack_half2(h0, h1), pack_half2(h2, h3));
+      btab[btab4_index<M>(gb, j, 2 * m + 1, t)] = make_uint2(pack_half2(u0 - h0, u1 - h1), pack_half2(u2 - h2, u3 - h3));
+      if ((lane & 7) == 0) {
+        fx[m * (xlen_pad / 32) + gb] = pow2f(10 + e);
+        sx[m * (xlen_pad / 32) + gb] = 8.f * ssum;
+      }
     }
   } else {
     const int nblk = len / 128;
@@ -502,6 +569,76 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
         const int gb = m * (xlen_pad / 128) + b;
         sx[gb] = s;
         fx[gb] = pow2f(10 + e);
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// SCALE4 consumer math for one 256-row tile (512 weights per row, sixteen
+// 32-blocks): warp cw takes the 64 rows of row group cw % 4 and the K quarter
+// cw / 4 (four blocks).  A block of a row is one 16-byte chunk, four code
+// words, word t for thread t; a 4-bit code masked in place at bit offset s of
+// an fp16 half is the exact subnormal q * 2^(s-24) (s = 0 or 4), so per word
+// one AND per two codes builds an A register: MMA j = 0 takes the words as
+// they are, j = 1 shifted right by 8.  Per block and row:
+//     y += d * (2^(10+E) * (C_hi + C_lo) - 8 * sum x)
+// ---------------------------------------------------------------------------
+template <int M>
+__device__ __forceinline__ void scale4_tile(const uint8_t* st_codes, const uint16_t* st_scales, int rows, int ci,
+                                            int nblk_valid, const float* xbuf, const float* fx, const float* sx,
+                                            int xlen_pad, int cw, int lane, float (&acc)[4][2]) {
+  constexpr int kRows = Geo<KQ_SCALE4>::kTileRows;
+  constexpr int kSpr = Geo<KQ_SCALE4>::kScalesPerRow;
+  const int rg = cw & 3, kq = cw >> 2;
+  if (rg * 64 >= rows) return;
+  const int g = lane >> 2, t = lane & 3;
+  const int kh = kq >> 1;
+  const uint8_t* base = st_codes + kh * (kRows * 128) + (rg * 64 + g) * 128 + 4 * t;
+  const int g16 = g << 4;
+  const bool has_b = g < 2 * M;
+  const uint2* bthread = reinterpret_cast<const uint2*>(xbuf) + (has_b ? g : 0) * 4 + t;
+  const int bt0 = 4 * kq;       // first block of the quarter inside the tile row
+  const int b0 = ci * 16 + bt0;  // first block inside the staged slice
+  const int tm = t < M ? t : 0;
+  const float4 F4 = *reinterpret_cast<const float4*>(fx + tm * (xlen_pad / 32) + b0);
+  const float4 S4 = *reinterpret_cast<const float4*>(sx + tm * (xlen_pad / 32) + b0);
+  const float Fv[4] = {F4.x, F4.y, F4.z, F4.w}, Sv[4] = {S4.x, S4.y, S4.z, S4.w};
+#pragma unroll
+  for (int bl = 0; bl < 4; ++bl) {
+    if (bt0 + bl >= nblk_valid) break;
+    const uint2* bb = bthread + (b0 + bl) * (2 * 2 * M * 4);
+    const int off = ((((kq & 1) * 4 + bl) << 4) ^ g16);
+    uint32_t w[4][2];
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4) {
+      w[s4][0] = *reinterpret_cast<const uint32_t*>(base + s4 * (16 * 128) + off);
+      w[s4][1] = *reinterpret_cast<const uint32_t*>(base + s4 * (16 * 128) + 8 * 128 + off);
+    }
+    float c[4][4];
+#pragma unroll
+    for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) c[s4][e] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint2 bf = make_uint2(0u, 0u);
+      if (has_b) bf = bb[j * (2 * M * 4)];
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const uint32_t xa = j ? w[s4][0] >> 8 : w[s4][0], xb = j ? w[s4][1] >> 8 : w[s4][1];
+        mma_16816(c[s4], xa & 0x000F000Fu, xb & 0x000F000Fu, xa & 0x00F000F0u, xb & 0x00F000F0u, bf.x, bf.y);
+      }
+    }
+    if (t < M) {
+      const float F = Fv[bl], S = Sv[bl];
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const int rA = rg * 64 + s4 * 16 + g;
+        const float dA = __half2float(__ushort_as_half(st_scales[rA * kSpr + bt0 + bl]));
+        const float dB = __half2float(__ushort_as_half(st_scales[(rA + 8) * kSpr + bt0 + bl]));
+        acc[s4][0] = fmaf(dA, fmaf(F, c[s4][0] + c[s4][1], -S), acc[s4][0]);
+        acc[s4][1] = fmaf(dB, fmaf(F, c[s4][2] + c[s4][3], -S), acc[s4][1]);
       }
     }
   }
@@ -630,7 +767,10 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
 // ---------------------------------------------------------------------------
 // The persistent streaming kernel.
 // ---------------------------------------------------------------------------
-template <int FMT, int M>
+// LINKED: a linked decode plan (stages, activation sources, stage counters,
+// split partials read by dependants).  The unlinked instantiation (single
+// GEMV / GEMM and plans without links) compiles none of that machinery.
+template <int FMT, int M, bool LINKED = false>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ Params p) {
   using F = Fmt<FMT>;
   using G = Geo<FMT>;
@@ -639,9 +779,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   extern __shared__ __align__(1024) uint8_t smem[];
   uint8_t* stages = smem;
   float* xbuf = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
-  float* fx = xbuf + kXMax;
-  float* sx = fx + kBlkMax;
-  float* scratch_all = sx + kBlkMax;
+  float* fx = xbuf + G::kXMaxF;
+  float* sx = fx + G::kBlkMax;
+  float* scratch_all = sx + G::kBlkMax;
   float* combine = scratch_all;  // shares the scratch region (see Geo)
   uint64_t* full = reinterpret_cast<uint64_t*>(scratch_all + G::kScratchRegion);
   uint64_t* empty = full + kStages;
@@ -664,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   }
   __syncthreads();
 
-  const int nst = p.nstages > 0 ? p.nstages : 1;
+  const int nst = LINKED ? p.nstages : 1;
 
   if (warp == 0) {
     // ------------------------------- producer -------------------------------
@@ -724,12 +864,13 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   const int cw = warp - 1;
   float* scratch = scratch_all + cw * kScratchFloats;
   ItemCursor cur;
-  // the staged activation slice: key of its activation and its K range
-  // (kbeg << 16 | kend, both below 2^15); a job sharing the activation and
-  // the range reuses it: the transform memo
+  // The staged activation slice.  Unlinked: keyed by (job, split).  Linked:
+  // by the activation's key and the K range (kbeg << 16 | kend, both below
+  // 2^15), so that a job sharing the activation and the range reuses it (the
+  // transform memo).
   int32_t cached_key = -1;
   uint32_t cached_range = 0xFFFFFFFFu;
-  int ready = -1;          // every stage up to this one has finished on all CTAs
+  int ready = -1;          // linked: every stage up to this one has finished on all CTAs
   int ring = 0;            // stage of the next tile
   uint32_t ring_par = 0;   // its phase parity
   uint32_t combines = 0;   // PQ2_0 slab-pair handoffs so far
@@ -745,12 +886,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     const int rows = min(kTileRows, (int)(job.n - row0));
     const int64_t kbeg = (int64_t)split * job.split_k;
     const int64_t kend = kbeg + min((int64_t)job.split_k, job.k - kbeg);
-    const int32_t key = p.links ? p.links[cur.j].x_key : cur.j;
-    const uint32_t range = ((uint32_t)kbeg << 16) | (uint32_t)kend;
+    const int32_t key = LINKED ? p.links[cur.j].x_key : cur.j;
+    const uint32_t range = LINKED ? ((uint32_t)kbeg << 16) | (uint32_t)kend : (uint32_t)split;
     if (key != cached_key || range != cached_range) {
-      const XLink lk = p.links ? p.links[cur.j] : XLink{-1, -1, cur.j, 1.f};
+      const XLink lk = LINKED ? p.links[cur.j] : XLink{-1, -1, cur.j, 1.f};
       xlen_pad = (int)(((kend - kbeg) + F::kChunk - 1) / F::kChunk * F::kChunk);
-      if (lk.dep_stage > ready) {  // the activation is an output of an earlier stage
+      if (LINKED && lk.dep_stage > ready) {  // the activation is an output of an earlier stage
         if (cw == 0 && lane == 0 && !*abort_flag && !wait_stage(p, lk.dep_stage)) {
           *abort_flag = 1;
           stream_flag(KQ_ERR_TIMEOUT);
@@ -794,6 +935,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         // lanes whose granule lies past k have nothing to do in this chunk
         if (k0 + (int64_t)(lane + 1) * F::kGran <= kend)
           q8_0_tile<M>(st, st_scales, rows, ci, xlen_pad, xbuf, cw, lane, acc8);
+      } else if constexpr (FMT == KQ_SCALE4) {
+        const int nblk_valid = min(16, (klen - ci * F::kChunk) / 32);
+        scale4_tile<M>(st, st_scales, rows, ci, nblk_valid, xbuf, fx, sx, xlen_pad, cw, lane, acc4);
       } else {
         const int nblk_valid = min(8, (klen - ci * F::kChunk) / 128);
         pq2_0_tile<M>(st, st_scales, rows, ci, nblk_valid, xbuf, fx, sx, xlen_pad, cw, lane, acc4);
@@ -894,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     }
   }
   // linked plan: this CTA has written every output of its items of stage st
-  if (p.stage_done) {
+  if (LINKED) {
     named_barrier(1, kConsumerWarps * 32);
     if (cw == 0 && lane == 0) {
       __threadfence();
@@ -906,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   // Linked plan: once every stage has finished everywhere, the outputs of the
   // split jobs are their partials added in split order (the order every
   // dependent activation used), each CTA a slice of the rows of every job.
-  if (p.n_split_jobs > 0) {
+  if (LINKED && p.n_split_jobs > 0) {
     if (cw == 0 && lane == 0 && !*abort_flag && !wait_stage(p, nst - 1)) {
       *abort_flag = 1;
       stream_flag(KQ_ERR_TIMEOUT);
@@ -943,7 +1087,9 @@ __global__ void reduce_splits_kernel(const float* __restrict__ ws, float* __rest
 // Host side
 // ---------------------------------------------------------------------------
 
-static int64_t chunk_of(int fmt) { return fmt == KQ_Q8_0 ? Fmt<KQ_Q8_0>::kChunk : Fmt<KQ_PQ2_0>::kChunk; }
+static int64_t chunk_of(int fmt) {
+  return fmt == KQ_Q8_0 ? Fmt<KQ_Q8_0>::kChunk : (fmt == KQ_SCALE4 ? Fmt<KQ_SCALE4>::kChunk : Fmt<KQ_PQ2_0>::kChunk);
+}
 
 struct Geometry {
   int32_t splits, split_k, row_blocks;
@@ -957,7 +1103,7 @@ struct Geometry {
 // The staged slice of m rows must fit kXMax floats, or half of it for the
 // n = 1024 rotation with m > 1 (its transform passes use the other half).
 static int64_t staging_floats(const kq_qmat* W, int64_t m) {
-  return W->fmt == KQ_PQ2_0 && W->had_block == 1024 && m > 1 ? kXMax / 2 : kXMax;
+  return W->fmt == KQ_PQ2_0 && W->had_block == 1024 && m > 1 ? kXMax / 2 : xmax_of(W->fmt);
 }
 
 static Geometry make_geometry(int fmt, int64_t n, int64_t k, int64_t m, int requested, int sms = 0,
@@ -970,7 +1116,7 @@ static Geometry make_geometry(int fmt, int64_t n, int64_t k, int64_t m, int requ
   int64_t splits = std::max<int64_t>(requested > 0 ? requested : 1, min_splits);
   if (requested == 0 && sms > 0) {
     const int64_t chunks = (k + unit - 1) / unit;
-    const double kTileUs = fmt == KQ_PQ2_0 ? 2.0 : 0.75, kReduceUs = 2.5;
+    const double kTileUs = fmt == KQ_PQ2_0 ? 2.0 : (fmt == KQ_SCALE4 ? 1.6 : 0.75), kReduceUs = 2.5;
     double best = 1e30;
     for (int64_t s = min_splits; s <= chunks; ++s) {
       const int64_t sk = round_up((k + s - 1) / s, unit);
@@ -1020,7 +1166,7 @@ static int make_maps(const kq_qmat* W, CUtensorMap* mc, CUtensorMap* ms) {
   cuuint64_t gstride[1] = {(cuuint64_t)rowbytes};
   // Q8_0: one 256-byte box per tile row; PQ2_0: two 128-byte boxes with the
   // 128-byte swizzle (the tensor-core consumer reads columns of 8 rows)
-  const bool swz = W->fmt == KQ_PQ2_0;
+  const bool swz = W->fmt != KQ_Q8_0;
   cuuint32_t box[2] = {swz ? 32u : (cuuint32_t)(kChunkBytes / 4), (cuuint32_t)tile_rows(W->fmt)};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(mc, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(W->codes), gdim, gstride, box, es,
@@ -1029,7 +1175,8 @@ static int make_maps(const kq_qmat* W, CUtensorMap* mc, CUtensorMap* ms) {
   if (r != CUDA_SUCCESS) return fail(KQ_ERR_CUDA, "tensor map of the codes plane: CUresult %d", (int)r);
   cuuint64_t sdim[2] = {(cuuint64_t)(sst / 2), (cuuint64_t)W->n};
   cuuint64_t sstr[1] = {(cuuint64_t)(sst * 2)};
-  cuuint32_t sbox[2] = {4, (cuuint32_t)tile_rows(W->fmt)};
+  // one tile row's scales: chunk / block fp16 values, as 32-bit elements
+  cuuint32_t sbox[2] = {(cuuint32_t)(chunk_of(W->fmt) / block_of(W->fmt) / 2), (cuuint32_t)tile_rows(W->fmt)};
   r = fn(ms, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(W->scales), sdim, sstr, sbox, es,
          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -1067,12 +1214,19 @@ static int launch_any(int fmt, int m, const Params& p, int grid, cudaStream_t st
       case 3: return launch_stream<KQ_Q8_0, 3>(p, grid, st);
       case 4: return launch_stream<KQ_Q8_0, 4>(p, grid, st);
     }
-  } else {
+  } else if (fmt == KQ_PQ2_0) {
     switch (m) {
       case 1: return launch_stream<KQ_PQ2_0, 1>(p, grid, st);
       case 2: return launch_stream<KQ_PQ2_0, 2>(p, grid, st);
       case 3: return launch_stream<KQ_PQ2_0, 3>(p, grid, st);
       case 4: return launch_stream<KQ_PQ2_0, 4>(p, grid, st);
+    }
+  } else if (fmt == KQ_SCALE4) {
+    switch (m) {
+      case 1: return launch_stream<KQ_SCALE4, 1>(p, grid, st);
+      case 2: return launch_stream<KQ_SCALE4, 2>(p, grid, st);
+      case 3: return launch_stream<KQ_SCALE4, 3>(p, grid, st);
+      case 4: return launch_stream<KQ_SCALE4, 4>(p, grid, st);
     }
   }
   return fail(KQ_ERR_UNSUPPORTED, "m = %d", m);
@@ -1241,8 +1395,9 @@ static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count,
   for (int64_t i = 0; i < count; ++i) {
     if (int s = check_qmat(&mats[i], -1)) return fail(s, "matrix %lld: %s", (long long)i, kq_last_error());
     if (mats[i].fmt != fmt) return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: mixed formats in one plan", (long long)i);
-    if (mats[i].k > kXMax)
-      return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: k = %lld > %d", (long long)i, (long long)mats[i].k, kXMax);
+    if (mats[i].k > xmax_of(fmt))
+      return fail(KQ_ERR_UNSUPPORTED, "matrix %lld: k = %lld > %d", (long long)i, (long long)mats[i].k,
+                  xmax_of(fmt));
   }
   if (links)
     if (int s = check_links(mats, links, count)) return s;
@@ -1385,7 +1540,7 @@ static int launch_plan(const Params& p, int grid, bool cooperative, cudaStream_t
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(stream_kernel<FMT, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(stream_kernel<FMT, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)Geo<FMT>::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return fail(KQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
@@ -1399,7 +1554,7 @@ static int launch_plan(const Params& p, int grid, bool cooperative, cudaStream_t
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  KQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, stream_kernel<FMT, 1>, p));
+  KQ_CUDA_TRY(cudaLaunchKernelEx(&cfg, stream_kernel<FMT, 1, true>, p));
   return KQ_OK;
 }
 
@@ -1407,7 +1562,9 @@ extern "C" {
 
 // kq_gemm_small_m runs on the tensor cores from kTcMinM activation rows on
 // (when k fits the tensor-core prologue), else on the streaming kernel.
-static bool small_m_uses_tc(const kq_qmat* W, int64_t m) { return m >= kTcMinM && m <= kTcMaxM && W->k <= kTcMaxK; }
+static bool small_m_uses_tc(const kq_qmat* W, int64_t m) {
+  return W->fmt != KQ_SCALE4 && m >= kTcMinM && m <= kTcMaxM && W->k <= kTcMaxK;
+}
 
 size_t kq_gemv_workspace_bytes(const kq_qmat* W, int64_t m) {
   if (check_qmat(W, -1) != KQ_OK || m < 1) return 0;
@@ -1423,6 +1580,11 @@ size_t kq_gemm_splitk_workspace_bytes(const kq_qmat* W, int64_t m, int32_t split
 int kq_gemv_q8_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream) {
   clear_error();
   return gemm_impl(W, d_x, 1, d_y, 0, d_ws, ws_bytes, stream, KQ_Q8_0);
+}
+
+int kq_gemv_scale4(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  return gemm_impl(W, d_x, 1, d_y, 0, d_ws, ws_bytes, stream, KQ_SCALE4);
 }
 
 int kq_gemv_pq2_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream) {
@@ -1519,6 +1681,7 @@ int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, vo
     KQ_CUDA_TRY(cudaMemsetAsync(d_ws, 0, (size_t)plan->nstages * sizeof(int32_t), st));
   }
   if (plan->fmt == KQ_Q8_0) return launch_plan<KQ_Q8_0>(p, plan->grid, plan->linked, st);
+  if (plan->fmt == KQ_SCALE4) return launch_plan<KQ_SCALE4>(p, plan->grid, plan->linked, st);
   return launch_plan<KQ_PQ2_0>(p, plan->grid, plan->linked, st);
 }
 

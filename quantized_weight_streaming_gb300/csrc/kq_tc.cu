@@ -768,6 +768,8 @@ int encode(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* map, CUtensorMapDa
 }  // namespace
 
 int tc_check(const kq_qmat* W, int64_t m) {
+  if (W->fmt != KQ_Q8_0 && W->fmt != KQ_PQ2_0)
+    return fail(KQ_ERR_UNSUPPORTED, "format %d has no tensor-core path (the streaming kernel serves it)", W->fmt);
   if (m < 1 || m > kTcMaxM) return fail(KQ_ERR_SHAPE, "m = %lld outside [1, %d]", (long long)m, kTcMaxM);
   if (W->k > kTcMaxK)
     return fail(KQ_ERR_SHAPE, "k = %lld above the tensor-core path's %d", (long long)W->k, kTcMaxK);

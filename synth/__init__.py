@@ -10,6 +10,7 @@ workload shapes:
 * ``pq2_0_gemv``    PQ2_0 GEMV with blockwise Hadamard, W 10240 x 5120, x 5120
 * ``qwen3_4b_q8_0_step``      Qwen3-4B-shaped list of 253 Q8_0 projections
 * ``bonsai_27b_pq2_0_step``   Bonsai-27B-shaped list of 401 PQ2_0 projections
+* ``qwen3_4b_scale4_step``    the same 253 projections in scale4_gs32
 * ``small_m``       M in {1, 4, 16, 64} activation rows against Q8_0 2560->9728
                     and PQ2_0 5120->17408
 
@@ -29,6 +30,7 @@ X_RANGE, X_EXP2 = 65536, 16
 
 ROLE_W = 0
 ROLE_X = 1
+ROLE_S = 2  # sign vectors of a rotation, indexed by K width
 
 CONFIG_IDS = {
     "q8_0_gemv": 0,
@@ -36,11 +38,13 @@ CONFIG_IDS = {
     "qwen3_4b_q8_0_step": 2,
     "bonsai_27b_pq2_0_step": 3,
     "small_m": 4,
+    "qwen3_4b_scale4_step": 5,
     "test": 7,
 }
 
 Q8_0 = "q8_0"
 PQ2_0 = "pq2_0"
+SCALE4 = "scale4"
 
 
 def stream_id(config, role, index=0):
@@ -100,7 +104,7 @@ def bonsai_27b_projections():
 SRC_PACKED = 0
 SRC_INPUT_OF = 1
 SRC_OUTPUT_OF = 2
-W_STD_EFF = {Q8_0: 0.0200, PQ2_0: 0.0222}  # std of the dequantized N(0, 0.02) weights of each format
+W_STD_EFF = {Q8_0: 0.0200, PQ2_0: 0.0222, SCALE4: 0.0200}  # std of the dequantized N(0, 0.02) weights
 
 
 def chain_alpha(fmt, k_src):
@@ -124,7 +128,7 @@ def decode_links(config):
 
     links = [None] * len(mats)
     prev = None  # index of the previous layer's down projection
-    if config == "qwen3_4b_q8_0_step":
+    if config in ("qwen3_4b_q8_0_step", "qwen3_4b_scale4_step"):
         layers, pre = 36, "layers."
         groups = lambda l: (("q_proj", "k_proj", "v_proj"), "q_proj", "o_proj", "gate_proj", "up_proj", "down_proj")
         head = "lm_head"
@@ -173,6 +177,8 @@ def workload(config):
         return bonsai_27b_projections()
     if config == "small_m":
         return list(SMALL_M_MATRICES)
+    if config == "qwen3_4b_scale4_step":  # the Qwen3-4B projections in scale4_gs32
+        return [(name, SCALE4, n, k) for name, _, n, k in qwen3_4b_projections()]
     raise KeyError(config)
 
 

@@ -91,6 +91,26 @@ def test_host_hadamard_matches_oracle(kq):
 
 
 @pytest.mark.parametrize("seed", [0, 1])
+def test_host_scale4_quantizer_matches_oracle_bytes(kq, seed):
+    w = synth.fill_host("w", 64 * 2560, seed, synth.stream_id("test", 0, 207)).reshape(64, 2560)
+    assert np.array_equal(kq.kq_quantize_scale4(w), oracle.scale4_quantize(w))
+    rng = np.random.default_rng(seed)
+    wide = (rng.standard_normal((32, 128)) * rng.uniform(1e-6, 50, size=(32, 1))).astype(np.float32)
+    wide[3, :32] = 0
+    wide[4, 5], wide[4, 6] = 7.0, -7.0  # a magnitude tie of opposite signs
+    wide[4, :5] = 0
+    assert np.array_equal(kq.kq_quantize_scale4(wide), oracle.scale4_quantize(wide))
+    assert kq.kq_blocks_bytes("scale4", 64, 2560) == 64 * 80 * 18
+    assert kq.kq_codes_bytes("scale4", 64, 2560) == 64 * 1280
+    assert kq.kq_scale_stride("scale4", 2560) == 80
+    lib = kq.lib()
+    big = np.full((1, 32), 6e5, dtype=np.float32)
+    out = np.full(18, 0xAB, dtype=np.uint8)
+    assert lib.kq_quantize_scale4(big.ctypes.data, 1, 32, out.ctypes.data) == kq.KQ_ERR_RANGE
+    assert np.all(out == 0xAB)
+
+
+@pytest.mark.parametrize("seed", [0, 1])
 def test_host_ptq1_0_quantizer_matches_oracle_bytes(kq, seed):
     w = synth.fill_host("w", 40 * 1024, seed, synth.stream_id("test", 0, 204)).reshape(40, 1024)
     _, w_rot = oracle.rotate_rows(w)
@@ -191,6 +211,13 @@ def test_device_entry_points_validate_before_any_cuda_call(kq):
     assert lib.kq_gemv_pq2_0(ctypes.byref(bad_signs), A, A, None, 0, None) == kq.KQ_ERR_ALIGNMENT
     assert lib.kq_rotate_blockwise(A, A, 1, 2048, 1024, A + 1, None) == kq.KQ_ERR_ALIGNMENT
     assert lib.kq_rotate_blockwise(A, A, 1, 1000, 1024, None, None) == kq.KQ_ERR_SHAPE
+    s4 = kq.kq_qmat(kq.KQ_SCALE4, 0, 8, 2560, A, A)
+    assert lib.kq_gemm_tc(ctypes.byref(s4), A, 16, A, 0, None, 0, None) == kq.KQ_ERR_UNSUPPORTED
+    assert lib.kq_gemv_scale4(ctypes.byref(good), A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG  # a Q8_0 matrix
+    s4_bad = kq.kq_qmat(kq.KQ_SCALE4, 0, 8, 48, A, A)
+    assert lib.kq_gemv_scale4(ctypes.byref(s4_bad), A, A, None, 0, None) == kq.KQ_ERR_SHAPE
+    ptq = kq.kq_qmat(kq.KQ_PTQ1_0, 128, 8, 128, A, A)  # a storage format is not a matrix format
+    assert lib.kq_gemv_pq2_0(ctypes.byref(ptq), A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
     assert lib.kq_stream_read(None, 1024, 4096, 4, A, None) == kq.KQ_ERR_INVALID_ARG
     assert lib.kq_stream_read(A, 1000, 4096, 4, A, None) == kq.KQ_ERR_SHAPE
     assert lib.kq_stream_read(A, 0, 4096, 4, A, None) == kq.KQ_ERR_SHAPE

@@ -45,14 +45,15 @@ def _sync_ok(kq):
 
 
 def _planes_as_blocks(kq, W):
-    """Device planes -> AoS 34-byte blocks (host), for byte comparison."""
+    """Device planes -> AoS blocks (host: fp16 scale, then the code bytes), for byte comparison."""
     bs = kq.kq_block_size(W.fmt)
     nb = W.k // bs
-    codes = W.codes.cpu().numpy().reshape(W.n, nb, 32)
+    cb = 16 if W.fmt == kq.KQ_SCALE4 else 32
+    codes = W.codes.cpu().numpy().reshape(W.n, nb, cb)
     ss = kq.kq_scale_stride(W.fmt, W.k)
     scales = W.scales.cpu().numpy().view(np.uint16).reshape(W.n, ss)
     assert not scales[:, nb:].any()  # padding is zero
-    out = np.empty((W.n, nb, 34), dtype=np.uint8)
+    out = np.empty((W.n, nb, 2 + cb), dtype=np.uint8)
     out[:, :, 0] = scales[:, :nb] & 0xFF
     out[:, :, 1] = scales[:, :nb] >> 8
     out[:, :, 2:] = codes
@@ -64,7 +65,7 @@ def _run_gemv(kq, W, x, splits=0, m=1):
     nbytes = kq.kq_gemm_splitk_workspace_bytes(W, m, splits)
     ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda") if nbytes else None
     if splits == 0 and m == 1:
-        (kq.kq_gemv_pq2_0 if W.fmt == kq.KQ_PQ2_0 else kq.kq_gemv_q8_0)(W, x, y, ws)
+        {kq.KQ_PQ2_0: kq.kq_gemv_pq2_0, kq.KQ_Q8_0: kq.kq_gemv_q8_0, kq.KQ_SCALE4: kq.kq_gemv_scale4}[W.fmt](W, x, y, ws)
     else:
         kq.kq_gemm_splitk(W, x, m, y, splits, ws)
     _sync_ok(kq)
@@ -107,19 +108,24 @@ def test_device_hadamard_bit_identical_to_host_and_oracle(kq):
 
 
 @pytest.mark.parametrize("fmt,n,k", [("q8_0", 1024, 2560), ("pq2_0", 10240, 5120), ("q8_0", 33, 96),
-                                     ("pq2_0", 17, 384)])
+                                     ("pq2_0", 17, 384), ("scale4", 9728, 2560), ("scale4", 33, 96)])
 def test_device_quantizer_and_prepare_bit_exact(kq, wl, fmt, n, k):
     s = synth.stream_id("test", 0, 302)
     W = wl.build_matrix(fmt, n, k, 3, s)
     _sync_ok(kq)
     w = synth.fill_host("w", n * k, 3, s).reshape(n, k)
-    ref = oracle.q8_0_quantize(w) if fmt == "q8_0" else oracle.pq2_0_quantize(oracle.rotate_rows(w)[1])
+    if fmt == "q8_0":
+        ref = oracle.q8_0_quantize(w)
+    elif fmt == "scale4":
+        ref = oracle.scale4_quantize(w)
+    else:
+        ref = oracle.pq2_0_quantize(oracle.rotate_rows(w)[1])
     assert np.array_equal(_planes_as_blocks(kq, W), ref)
     # debug dequantizer is bit-exact against the oracle's dequantizer
     deq = torch.empty(n * k, dtype=torch.float32, device="cuda")
     kq.kq_dequantize(W, deq)
     _sync_ok(kq)
-    ref_deq = (oracle.q8_0_dequant if fmt == "q8_0" else oracle.pq2_0_dequant)(ref, n, k)
+    ref_deq = {"q8_0": oracle.q8_0_dequant, "scale4": oracle.scale4_dequant, "pq2_0": oracle.pq2_0_dequant}[fmt](ref, n, k)
     assert np.array_equal(deq.cpu().numpy().reshape(n, k), ref_deq)
     # AoS blocks from the host quantizer, repacked on the device, give the same planes
     W2 = kq.QMatrix(fmt, n, k)
@@ -169,6 +175,8 @@ SHAPES = [
     ("pq2_0", 10240, 5120),  # PQ2_0 GEMV workload, full size
     ("q8_0", 1, 32), ("q8_0", 17, 96), ("q8_0", 72, 2592), ("q8_0", 33, 9728), ("q8_0", 5, 4096),
     ("pq2_0", 1, 128), ("pq2_0", 15, 384), ("pq2_0", 72, 5248), ("pq2_0", 31, 17408), ("pq2_0", 48, 6144),
+    ("scale4", 1024, 2560), ("scale4", 9728, 2560), ("scale4", 2560, 9728), ("scale4", 1, 32), ("scale4", 17, 96),
+    ("scale4", 300, 4128), ("scale4", 33, 16384),
 ]
 
 
@@ -202,6 +210,26 @@ def test_q8_0_exact_integer_case_tolerance_zero(kq):
     y = _run_gemv(kq, W, torch.from_numpy(x).cuda())
     assert np.array_equal(y.astype(np.float64), y_ref)
     assert np.array_equal(y_ref, (q @ x.astype(np.int64)) * 2.0**-5)
+
+
+def test_scale4_exact_integer_case_tolerance_zero(kq):
+    """Codes 0..15 with a 0 in every block (so d = 2^-5 exactly), small
+    integer activations: every product and partial sum is exact in fp32, the
+    zero point included, so the output must equal the oracle's exactly."""
+    rng = np.random.default_rng(14)
+    n, k = 300, 4128  # ragged rows, K not a multiple of the 512-weight tile row
+    q = rng.integers(0, 16, size=(n, k))
+    q[:, ::32] = 0
+    w = ((q - 8) * 2.0**-5).astype(np.float32)
+    x = rng.integers(-8, 9, size=k).astype(np.float32)
+    blocks, _, y_ref, _ = oracle.scale4_reference(w, x)
+    W = kq.QMatrix("scale4", n, k)
+    kq.kq_prepare(W, torch.from_numpy(blocks.reshape(-1)).cuda())
+    y = _run_gemv(kq, W, torch.from_numpy(x).cuda())
+    assert np.array_equal(y.astype(np.float64), y_ref)
+    assert np.array_equal(y_ref, ((q - 8) @ x.astype(np.int64)) * 2.0**-5)
+    y3 = _run_gemv(kq, W, torch.from_numpy(x).cuda(), splits=3)
+    assert np.array_equal(y3.astype(np.float64), y_ref)
 
 
 def test_pq2_0_nonzero_mean_activation(kq, wl):
@@ -269,7 +297,7 @@ def test_workspace_too_small_is_rejected(kq, wl):
 # ----------------------------------------------------------------------------
 
 @pytest.mark.parametrize("fmt,n,k", [("q8_0", 9728, 2560), ("pq2_0", 17408, 5120), ("q8_0", 40, 288),
-                                     ("pq2_0", 24, 1152)])
+                                     ("pq2_0", 24, 1152), ("scale4", 9728, 2560), ("scale4", 40, 544)])
 @pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 16, 64])
 def test_small_m_matches_oracle(kq, wl, fmt, n, k, m):
     if n * k > 50_000_000 and m not in (1, 4, 16, 64):
@@ -289,6 +317,9 @@ def test_small_m_matches_oracle(kq, wl, fmt, n, k, m):
     if fmt == "pq2_0":
         deq = oracle.pq2_0_dequant(oracle.pq2_0_quantize(oracle.rotate_rows(w)[1]), rows.size, k)
         X64 = oracle.rotate_rows(Xh)[0]
+    elif fmt == "scale4":
+        deq = oracle.scale4_dequant(oracle.scale4_quantize(w), rows.size, k)
+        X64 = Xh.astype(np.float64)
     else:
         deq = oracle.q8_0_dequant(oracle.q8_0_quantize(w), rows.size, k)
         X64 = Xh.astype(np.float64)
@@ -442,11 +473,11 @@ def test_stream_read_control_xor(kq, nbytes, stage_bytes, stages):
 
 def test_decode_plan_small_mixed_shapes(kq, wl):
     spec = [(16, 256), (33, 1024), (1, 5120), (300, 2048), (17, 17408), (64, 128)]
-    for fmt in ("q8_0", "pq2_0"):
+    for fmt in ("q8_0", "pq2_0", "scale4"):
         mats, xs, host = [], [], []
         for i, (n, k) in enumerate(spec):
-            if fmt == "q8_0" and k % 32:
-                continue
+            if fmt == "scale4" and k > 16384:
+                continue  # beyond the SCALE4 plan's staging limit
             sw, sx = synth.stream_id("test", 0, 340 + i), synth.stream_id("test", 1, 340 + i)
             mats.append(wl.build_matrix(fmt, n, k, 4, sw))
             xs.append(synth.fill_host("x", k, 4, sx))
@@ -599,7 +630,7 @@ _CHAIN = [((200, 4096), (0, 0, 0, 1.0)), ((64, 4096), (1, 0, 0, 1.0)), ((300, 40
           ((96, 128), (2, 6, 8, 3.0))]
 
 
-@pytest.mark.parametrize("fmt", ["q8_0", "pq2_0"])
+@pytest.mark.parametrize("fmt", ["q8_0", "pq2_0", "scale4"])
 def test_linked_plan_chain(kq, wl, fmt):
     mats, host, links = [], [], []
     for i, ((n, k), lk) in enumerate(_CHAIN):

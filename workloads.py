@@ -14,7 +14,9 @@ import synth
 
 
 def _fmt_name(fmt):
-    return fmt if isinstance(fmt, str) else ("q8_0" if fmt == kq.KQ_Q8_0 else "pq2_0")
+    if isinstance(fmt, str):
+        return fmt
+    return {kq.KQ_Q8_0: "q8_0", kq.KQ_PQ2_0: "pq2_0", kq.KQ_SCALE4: "scale4"}[fmt]
 
 
 def build_matrix(fmt, n, k, seed, stream, tmp=None, device="cuda", had_block=None, signs=None):
@@ -31,6 +33,8 @@ def build_matrix(fmt, n, k, seed, stream, tmp=None, device="cuda", had_block=Non
     if _fmt_name(fmt) == "pq2_0":
         kq.kq_rotate_blockwise(w, w, n, k, W.had_block, signs)
         kq.kq_quantize_pq2_0_device(W, w)
+    elif _fmt_name(fmt) == "scale4":
+        kq.kq_quantize_scale4_device(W, w)
     else:
         kq.kq_quantize_q8_0_device(W, w)
     return W
@@ -57,10 +61,14 @@ class DecodeWorkload:
     every later one reads its group's input or alpha times an earlier output,
     stage by stage, in one cooperative launch per step."""
 
-    def __init__(self, config, seed=0, device="cuda", limit=None, linked=False):
+    def __init__(self, config, seed=0, device="cuda", limit=None, linked=False, rotation=None):
+        """rotation="page": PQ2_0 matrices use the page's rotation, 1024-point
+        blocks with one seeded sign vector per K width (shared by every matrix
+        of that width)."""
         self.config = config
         self.seed = seed
         self.linked = linked
+        self.rotation = rotation
         self.mats_spec = synth.workload(config)
         if limit:
             self.mats_spec = self.mats_spec[:limit]
@@ -68,8 +76,15 @@ class DecodeWorkload:
         big = max(n * k for _, _, n, k in self.mats_spec)
         tmp = torch.empty(big, dtype=torch.float32, device=device)
         self.mats = []
+        self.signs = {}  # K width -> (host, device) signs of the page's rotation
         for i, (_, fmt, n, k) in enumerate(self.mats_spec):
-            self.mats.append(build_matrix(fmt, n, k, seed, synth.stream_id(config, synth.ROLE_W, i), tmp, device))
+            had, sd = None, None
+            if rotation == "page" and fmt == synth.PQ2_0:
+                if k not in self.signs:
+                    self.signs[k] = build_signs(k, seed, synth.stream_id(config, synth.ROLE_S, k), device)
+                had, sd = 1024, self.signs[k][1]
+            self.mats.append(build_matrix(fmt, n, k, seed, synth.stream_id(config, synth.ROLE_W, i), tmp, device,
+                                          had_block=had, signs=sd))
         del tmp
         # packed inputs: every projection's own (unlinked), or those of the
         # projections whose link is SRC_PACKED (linked), in list order
