@@ -307,6 +307,40 @@ def reference(fmt, w, x):
     raise OracleError(fmt)
 
 
+def f16_chain_reference(fmt, w, x16, had=HADAMARD_N, signs=None):
+    """The fp16 activation chain of the Bonsai page, section 4.4: activation
+    fp16 -> fp32 (sign flip and) transform -> fp16 -> product accumulated in
+    fp32 -> fp16 output.  Reading: the transformed activation is the exact
+    (FP64) R x rounded once to fp16; an fp32 transform may land on the other
+    fp16 neighbour when R x lies within the fp32 transform's error bound
+    ((log2 n + 3) 2^-24 sum_blk |x| / sqrt(n)) of a rounding midpoint, and
+    `slack` bounds that: sum_j |w_ij| * (the fp16 step at x'_j) over those j.
+    x16: fp16 values (numpy float16).  Returns (y FP64, absdot, slack, x'16)."""
+    w = _f32(w)
+    n, k = w.shape
+    x = np.asarray(x16, dtype=np.float16).astype(np.float32)
+    if fmt == "pq2_0":
+        _, w_rot = rotate_rows(w, had, signs)
+        deq = pq2_0_dequant(pq2_0_quantize(w_rot), n, k)
+        xr64, _ = rotate_rows(x, had, signs)
+        xp16 = xr64.astype(np.float16)  # one rounding of the exact value (to nearest even)
+        # where an fp32 transform could have rounded to the other neighbour
+        blk_abs = np.abs(x.astype(np.float64)).reshape(-1, had).sum(axis=1).repeat(had)
+        eps = (np.log2(had) + 3) * 2.0 ** -24 * blk_abs / np.sqrt(had)
+        lo = np.nextafter(xp16, np.float16(-np.inf)).astype(np.float64)
+        hi = np.nextafter(xp16, np.float16(np.inf)).astype(np.float64)
+        c = xp16.astype(np.float64)
+        near = np.minimum(np.abs(xr64 - (c + lo) / 2), np.abs(xr64 - (c + hi) / 2)) <= eps
+        step = np.where(near, np.maximum(c - lo, hi - c), 0.0)
+    else:
+        deq = (q8_0_dequant(q8_0_quantize(w), n, k) if fmt == "q8_0" else scale4_dequant(scale4_quantize(w), n, k))
+        xp16 = x.astype(np.float16)
+        step = np.zeros(k)
+    y, a = gemv(deq, xp16.astype(np.float64))
+    slack = np.abs(deq.astype(np.float64)) @ step
+    return y, a, slack, xp16
+
+
 def within_bound(y, y_ref, absdot, tol=TOLERANCE):
     """Per-row acceptance: |y - y_ref| <= tol * absdot.  Returns (ok, worst
     ratio of error to bound)."""

@@ -484,6 +484,39 @@ def test_gemv_brute_force_4x128_scale4():
         assert abs(a[i] - sum(abs(float(deq[i, j]) * float(x[j])) for j in range(128))) <= 1e-12 * a[i]
 
 
+def test_f16_chain_of_a_scaled_unit_vector():
+    """x = c e_j in fp16: R x = (c / sqrt(128)) H[:, j] exactly, so x'16 is
+    fp16(+-c / sqrt(128)) everywhere in the block, worked by hand: for
+    c = 3, 3 / sqrt(128) = 0.26516504... -> fp16 0.2651367 (0x343E)."""
+    w = np.zeros((2, 256), dtype=np.float32)
+    w[0, :128] = 0.5  # some block scale; the y check below only needs x'
+    x16 = np.zeros(256, dtype=np.float16)
+    x16[5] = 3.0
+    _, _, slack, xp16 = oracle.f16_chain_reference("pq2_0", w, x16)
+    h = scipy.linalg.hadamard(128)[:, 5]
+    want = np.float16(0.2651367)
+    assert want.view(np.uint16) == 0x343E
+    assert np.array_equal(xp16[:128], (h * want).astype(np.float16))
+    assert not xp16[128:].any()
+    assert np.all(slack == 0)
+
+
+def test_f16_chain_exact_integer_case():
+    """Q8_0 with integer codes, power-of-two scales and small integer fp16
+    activations: the FP64 y is an exact integer multiple of 2^-5 that fp16
+    holds exactly, so the chain's fp16 output equals it."""
+    rng = np.random.default_rng(15)
+    q = rng.integers(-127, 128, size=(6, 256))
+    q[:, ::32] = 127
+    w = (q * 2.0 ** -5).astype(np.float32)
+    x16 = np.zeros(256, dtype=np.float16)  # eight nonzero activations: |y 2^5| <= 8 * 127 * 2 < 2^11
+    x16[rng.choice(256, size=8, replace=False)] = rng.choice([-2, -1, 1, 2], size=8)
+    y, _, slack, _ = oracle.f16_chain_reference("q8_0", w, x16)
+    assert np.array_equal(y, (q @ x16.astype(np.int64)) * 2.0 ** -5)
+    assert np.array_equal(y.astype(np.float16).astype(np.float64), y)  # 11 significant bits suffice
+    assert not slack.any()
+
+
 def test_gemv_brute_force_4x128_pq2_0():
     w = synth.fill_host("w", 4 * 128, 9, synth.stream_id("test", 0, 9)).reshape(4, 128)
     x = synth.fill_host("x", 128, 9, synth.stream_id("test", 1, 9))
