@@ -216,6 +216,15 @@ int kq_gemv_scale4(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, s
  * [k]; the blockwise transform runs in the kernel's activation prologue. */
 int kq_gemv_pq2_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
 
+/* The fp16 chain of the Bonsai page, section 4.4 (its token-identity
+ * yardstick): d_x is an fp16 activation [k], d_y an fp16 output [n], any
+ * matrix format.  For PQ2_0 the (sign flip and) transform runs in fp32 and
+ * its result is rounded to fp16 before the product; the product accumulates
+ * in fp32 and is rounded once to fp16 at the end (after the split second
+ * pass, if any).  Same workspace as the fp32 GEMV of W; d_x and d_y 16-byte
+ * aligned. */
+int kq_gemv_f16(const kq_qmat* W, const void* d_x, void* d_y, void* d_ws, size_t ws_bytes, void* stream);
+
 /* Y[m][n] = X[m][k] W^T (rotated per row for PQ2_0), X and Y row-major fp32,
  * 1 <= m <= 64.  From m = 16 on (and k <= 32768) this is kq_gemm_tc with an
  * automatic split; below, the streaming kernel applies each weight tile to

@@ -88,6 +88,7 @@ SIGNATURES = {
     "kq_quantize_scale4": (ctypes.c_int, [_P, _I64, _I64, _P]),
     "kq_quantize_scale4_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "kq_gemv_scale4": (ctypes.c_int, [_QP, _P, _P, _P, _SZ, _P]),
+    "kq_gemv_f16": (ctypes.c_int, [_QP, _P, _P, _P, _SZ, _P]),
     "kq_hadamard_blockwise_host": (ctypes.c_int, [_P, _P, _I64, _I64, _I32]),
     "kq_prepare": (ctypes.c_int, [ctypes.c_int, _P, _I64, _I64, _P, _P, _P]),
     "kq_quantize_q8_0_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
@@ -328,6 +329,12 @@ def kq_gemv_q8_0(W, d_x, d_y, ws=None, stream=None):
 def kq_gemv_scale4(W, d_x, d_y, ws=None, stream=None):
     p, nb = _ws(ws)
     _check(_lib.kq_gemv_scale4(ctypes.byref(W.desc), _ptr(d_x), _ptr(d_y), p, nb, _stream(stream)), "kq_gemv_scale4")
+
+
+def kq_gemv_f16(W, d_x16, d_y16, ws=None, stream=None):
+    """The fp16 chain: fp16 activation in, fp16 output (any format)."""
+    p, nb = _ws(ws)
+    _check(_lib.kq_gemv_f16(ctypes.byref(W.desc), _ptr(d_x16), _ptr(d_y16), p, nb, _stream(stream)), "kq_gemv_f16")
 
 
 def kq_gemv_pq2_0(W, d_x, d_y, ws=None, stream=None):

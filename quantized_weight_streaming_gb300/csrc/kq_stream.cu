@@ -255,7 +255,15 @@ struct XSrc {
 // x[i..i+3] of activation row m; loads bypass L1 (the source may have been
 // written by other CTAs of this launch).  The partials are added in split
 // order, exactly as the final write of the source's output adds them.
+template <bool IO16 = false>
 __device__ __forceinline__ float4 load_x4(const XSrc& xs, int m, int64_t i) {
+  if constexpr (IO16) {  // fp16 activations (the fp16 chain): four halves, exact in fp32
+    const __half* h = reinterpret_cast<const __half*>(xs.base) + (int64_t)m * xs.row_stride + i;
+    const uint2 u = __ldcg(reinterpret_cast<const uint2*>(h));
+    const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&u.x));
+    const float2 c = __half22float2(*reinterpret_cast<const __half2*>(&u.y));
+    return make_float4(a.x, a.y, c.x, c.y);
+  }
   const float* b = xs.base + (int64_t)m * xs.row_stride + i;
   float4 v;
   if (xs.vec4) {
@@ -415,7 +423,11 @@ __device__ __forceinline__ void fwht128_lane4(float (&v)[4], int lane) {
 //  PQ2_0: blockwise Walsh-Hadamard transform, then the B table of every
 //  block, plus per block the factor 2^(10+E) and the sum of x'.
 // ---------------------------------------------------------------------------
-template <int FMT, int M>
+// IO16: the activation is fp16, and for PQ2_0 the transformed activation is
+// rounded to fp16 right after the transform (the fp16 chain).
+__device__ __forceinline__ float round_f16(float v) { return __half2float(__float2half_rn(v)); }
+
+template <int FMT, int M, bool IO16 = false>
 __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int xlen_pad, float* xbuf, float* fx,
                                  float* sx, float* scratch, int cw, int lane) {
   const int len = (int)(kend - kbeg);
@@ -424,7 +436,7 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
     float4* xb4 = reinterpret_cast<float4*>(xbuf);
     for (int m = 0; m < M; ++m) {
       for (int i = cw * 32 + lane; i < len / 4; i += kT)
-        xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] = load_x4(xs, m, kbeg + 4 * i);
+        xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] = load_x4<IO16>(xs, m, kbeg + 4 * i);
     }
   } else if (FMT == KQ_SCALE4) {
     // A warp takes 128 positions (four 32-blocks, eight lanes per block) at a
@@ -437,7 +449,7 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
       const int m = tt / ngrp, q = tt % ngrp;
       // len is a multiple of 32: a block's eight lanes are all inside or all past the slice
       const bool inside = q * 128 + 4 * lane < len;
-      const float4 f = inside ? load_x4(xs, m, kbeg + q * 128 + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 f = inside ? load_x4<IO16>(xs, m, kbeg + q * 128 + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
       float amax = fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)));
       float ssum = (f.x + f.y) + (f.z + f.w);
 #pragma unroll
@@ -485,7 +497,7 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
     if (h1024) {
       for (int tt = cw; tt < M * nblk; tt += kConsumerWarps) {
         const int m = tt / nblk, b = tt % nblk;
-        float4 f = load_x4(xs, m, kbeg + b * 128 + 4 * lane);
+        float4 f = load_x4<IO16>(xs, m, kbeg + b * 128 + 4 * lane);
         float v[4] = {f.x, f.y, f.z, f.w};
         if (xs.signs) {
           const char4 s4 = *reinterpret_cast<const char4*>(xs.signs + kbeg + b * 128 + 4 * lane);
@@ -514,7 +526,10 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
               v[a + h] = x0 - x1;
             }
 #pragma unroll
-        for (int a = 0; a < 8; ++a) raw[((int64_t)(bb * 8 + a) * M + mm) * 128 + e] = v[a] * 0.03125f;
+        for (int a = 0; a < 8; ++a) {
+          const float r = v[a] * 0.03125f;
+          raw[((int64_t)(bb * 8 + a) * M + mm) * 128 + e] = IO16 ? round_f16(r) : r;
+        }
       }
       named_barrier(1, kConsumerWarps * 32);
     }
@@ -528,14 +543,14 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
         v[2] = f.z;
         v[3] = f.w;
       } else {
-        const float4 f = load_x4(xs, m, kbeg + b * 128 + 4 * lane);
+        const float4 f = load_x4<IO16>(xs, m, kbeg + b * 128 + 4 * lane);
         v[0] = f.x;
         v[1] = f.y;
         v[2] = f.z;
         v[3] = f.w;
         fwht128_lane4(v, lane);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] *= inv_sqrt128;
+        for (int i = 0; i < 4; ++i) v[i] = IO16 ? round_f16(v[i] * inv_sqrt128) : v[i] * inv_sqrt128;
       }
       float amax = 0.f;
 #pragma unroll
@@ -770,7 +785,8 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
 // LINKED: a linked decode plan (stages, activation sources, stage counters,
 // split partials read by dependants).  The unlinked instantiation (single
 // GEMV / GEMM and plans without links) compiles none of that machinery.
-template <int FMT, int M, bool LINKED = false>
+// IO16: the fp16 chain (fp16 activation in, fp16 output; unlinked GEMVs only).
+template <int FMT, int M, bool LINKED = false, bool IO16 = false>
 __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_constant__ Params p) {
   using F = Fmt<FMT>;
   using G = Geo<FMT>;
@@ -899,7 +915,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         ready = lk.dep_stage;
       }
       named_barrier(1, kConsumerWarps * 32);  // everyone is done with the previous slice
-      stage_activation<FMT, M>(make_xsrc(p, cur.j, job, lk), kbeg, kend, xlen_pad, xbuf, fx, sx, scratch, cw, lane);
+      stage_activation<FMT, M, IO16>(make_xsrc(p, cur.j, job, lk), kbeg, kend, xlen_pad, xbuf, fx, sx, scratch, cw,
+                                     lane);
       named_barrier(1, kConsumerWarps * 32);
       cached_key = key;
       cached_range = range;
@@ -972,10 +989,14 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
           }
 #pragma unroll
           for (int m = 0; m < M; ++m) {
-            if (job.splits == 1)
-              job.y[(int64_t)m * job.ldy + row0 + row] = v[m];
-            else
+            if (job.splits == 1) {
+              if constexpr (IO16)
+                reinterpret_cast<__half*>(job.y)[(int64_t)m * job.ldy + row0 + row] = __float2half_rn(v[m]);
+              else
+                job.y[(int64_t)m * job.ldy + row0 + row] = v[m];
+            } else {
               job.ws[((int64_t)split * M + m) * job.n + row0 + row] = v[m];
+            }
           }
         }
       }
@@ -1028,11 +1049,20 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&cfree[sp]);
-        float* yl = yout + sp * 64 + g;
+        if (IO16 && job.splits == 1) {  // the final output, in fp16
+          __half* yh = reinterpret_cast<__half*>(job.y) + (int64_t)t * job.ldy + row0 + sp * 64 + g;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int dr = (e >> 1) * 16 + (e & 1) * 8;  // slab e/2, row g or g+8
-          if (dr < rmax) yl[dr] = y8[e];
+          for (int e = 0; e < 8; ++e) {
+            const int dr = (e >> 1) * 16 + (e & 1) * 8;
+            if (dr < rmax) yh[dr] = __float2half_rn(y8[e]);
+          }
+        } else {
+          float* yl = yout + sp * 64 + g;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int dr = (e >> 1) * 16 + (e & 1) * 8;  // slab e/2, row g or g+8
+            if (dr < rmax) yl[dr] = y8[e];
+          }
         }
       }
     }
@@ -1071,7 +1101,9 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   }
 }
 
-// Second pass of split-K: y[m][row] = sum over splits in split order.
+// Second pass of split-K: y[m][row] = sum over splits in split order (OUT16:
+// the sum rounded once to fp16).
+template <bool OUT16 = false>
 __global__ void reduce_splits_kernel(const float* __restrict__ ws, float* __restrict__ y, int64_t n, int64_t ldy,
                                      int m, int splits) {
   const int64_t total = (int64_t)m * n;
@@ -1079,7 +1111,10 @@ __global__ void reduce_splits_kernel(const float* __restrict__ ws, float* __rest
     const int64_t mm = i / n, row = i % n;
     float s = ws[mm * n + row];
     for (int sp = 1; sp < splits; ++sp) s += ws[((int64_t)sp * m + mm) * n + row];
-    y[mm * ldy + row] = s;
+    if constexpr (OUT16)
+      reinterpret_cast<__half*>(y)[mm * ldy + row] = __float2half_rn(s);
+    else
+      y[mm * ldy + row] = s;
   }
 }
 
@@ -1192,21 +1227,28 @@ static int device_sms(int* sms) {
   return KQ_OK;
 }
 
-template <int FMT, int M>
+template <int FMT, int M, bool IO16 = false>
 static int launch_stream(const Params& p, int grid, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(stream_kernel<FMT, M>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(stream_kernel<FMT, M, false, IO16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)Geo<FMT>::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return fail(KQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
-  stream_kernel<FMT, M><<<grid, kThreads, Geo<FMT>::kSmemBytes, st>>>(p);
+  stream_kernel<FMT, M, false, IO16><<<grid, kThreads, Geo<FMT>::kSmemBytes, st>>>(p);
   KQ_CUDA_TRY(cudaGetLastError());
   return KQ_OK;
 }
 
-static int launch_any(int fmt, int m, const Params& p, int grid, cudaStream_t st) {
+static int launch_any(int fmt, int m, const Params& p, int grid, cudaStream_t st, bool io16 = false) {
+  if (io16) {  // the fp16 chain: one activation row
+    if (m != 1) return fail(KQ_ERR_UNSUPPORTED, "fp16 activations with m = %d", m);
+    if (fmt == KQ_Q8_0) return launch_stream<KQ_Q8_0, 1, true>(p, grid, st);
+    if (fmt == KQ_PQ2_0) return launch_stream<KQ_PQ2_0, 1, true>(p, grid, st);
+    if (fmt == KQ_SCALE4) return launch_stream<KQ_SCALE4, 1, true>(p, grid, st);
+    return fail(KQ_ERR_UNSUPPORTED, "format %d", fmt);
+  }
   if (fmt == KQ_Q8_0) {
     switch (m) {
       case 1: return launch_stream<KQ_Q8_0, 1>(p, grid, st);
@@ -1252,7 +1294,7 @@ static size_t splitk_ws_bytes(const kq_qmat* W, int64_t m, int splits) {
 }
 
 static int gemm_impl(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int splits, void* d_ws,
-                     size_t ws_bytes, void* stream, int expect_fmt) {
+                     size_t ws_bytes, void* stream, int expect_fmt, bool io16 = false) {
   if (int s = check_qmat(W, expect_fmt)) return s;
   if (m < 1 || m > kMaxM) return fail(KQ_ERR_SHAPE, "m = %lld outside [1, %lld]", (long long)m, (long long)kMaxM);
   if (splits < 0) return fail(KQ_ERR_INVALID_ARG, "splits = %d", splits);
@@ -1293,11 +1335,14 @@ static int gemm_impl(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, 
     p.bounds = nullptr;
     p.total_items = j.items;
     const int grid = (int)std::min<int64_t>(j.items, sms);
-    if (int s = launch_any(W->fmt, mm, p, grid, st)) return s;
+    if (int s = launch_any(W->fmt, mm, p, grid, st, io16)) return s;
     if (g.splits > 1) {
       const int64_t tot = (int64_t)mm * W->n;
       const int rgrid = (int)std::min<int64_t>((tot + 255) / 256, (int64_t)sms * 8);
-      reduce_splits_kernel<<<rgrid, 256, 0, st>>>((const float*)d_ws, d_Y + m0 * W->n, W->n, W->n, mm, g.splits);
+      if (io16)
+        reduce_splits_kernel<true><<<rgrid, 256, 0, st>>>((const float*)d_ws, d_Y, W->n, W->n, mm, g.splits);
+      else
+        reduce_splits_kernel<<<rgrid, 256, 0, st>>>((const float*)d_ws, d_Y + m0 * W->n, W->n, W->n, mm, g.splits);
       KQ_CUDA_TRY(cudaGetLastError());
     }
   }
@@ -1580,6 +1625,12 @@ size_t kq_gemm_splitk_workspace_bytes(const kq_qmat* W, int64_t m, int32_t split
 int kq_gemv_q8_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream) {
   clear_error();
   return gemm_impl(W, d_x, 1, d_y, 0, d_ws, ws_bytes, stream, KQ_Q8_0);
+}
+
+int kq_gemv_f16(const kq_qmat* W, const void* d_x, void* d_y, void* d_ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  return gemm_impl(W, static_cast<const float*>(d_x), 1, static_cast<float*>(d_y), 0, d_ws, ws_bytes, stream, -1,
+                   true);
 }
 
 int kq_gemv_scale4(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream) {

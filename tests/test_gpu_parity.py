@@ -504,6 +504,39 @@ def test_decode_plan_small_mixed_shapes(kq, wl):
 
 
 # ----------------------------------------------------------------------------
+# the fp16 chain (fp16 activation in, fp16 output)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,n,k,had", [("pq2_0", 10240, 5120, 128), ("pq2_0", 300, 5120, 1024),
+                                         ("pq2_0", 64, 17408, 128), ("pq2_0", 33, 1152, 128),
+                                         ("q8_0", 1024, 2560, 0), ("q8_0", 40, 9728, 0), ("scale4", 300, 4128, 0)])
+def test_f16_chain_matches_oracle(kq, wl, fmt, n, k, had):
+    """fp16 x -> (sign flip and) transform in fp32 -> fp16 -> product in fp32 ->
+    fp16 y (the Bonsai page, section 4.4).  Bound per row: the fp32 bound, the
+    oracle's slack for transformed values next to an fp16 rounding midpoint,
+    and half an fp16 step of the output."""
+    sid = synth.stream_id("test", 0, 470 + n % 97)
+    sh, sd = (wl.build_signs(k, 3, synth.stream_id("test", 1, 471)) if had == 1024 else (None, None))
+    W = wl.build_matrix(fmt, n, k, 9, sid, had_block=(1024 if had == 1024 else None), signs=sd)
+    x16 = synth.fill_host("x", k, 9, synth.stream_id("test", 1, 472)).astype(np.float16)
+    y16 = torch.empty(n, dtype=torch.float16, device="cuda")
+    nb = kq.kq_gemv_workspace_bytes(W, 1)
+    ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+    kq.kq_gemv_f16(W, torch.from_numpy(x16).cuda(), y16, ws)
+    _sync_ok(kq)
+    w = synth.fill_host("w", n * k, 9, sid).reshape(n, k)
+    y_ref, absdot, slack, _ = oracle.f16_chain_reference(fmt, w, x16, had if had else 128, sh)
+    got = y16.cpu().numpy().astype(np.float64)
+    mag = np.abs(y_ref) + TOL * absdot + slack
+    bound = TOL * absdot + slack + 0.5 * np.spacing(mag.astype(np.float16)).astype(np.float64) * (1 + 2.0**-10)
+    err = np.abs(got - y_ref)
+    assert np.all(err <= bound), float(np.max(err / np.maximum(bound, 1e-300)))
+    if fmt != "pq2_0":  # no transform: the fp32 GEMV of the same input, rounded once
+        y32 = _run_gemv(kq, W, torch.from_numpy(x16.astype(np.float32)).cuda())
+        assert np.array_equal(got, y32.astype(np.float16).astype(np.float64))
+
+
+# ----------------------------------------------------------------------------
 # the page's rotation: n = 1024 blocks with a sign vector
 # ----------------------------------------------------------------------------
 
