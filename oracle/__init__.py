@@ -69,6 +69,8 @@ def lib():
         L.orc_rotate_rows.restype = ctypes.c_int
         L.orc_rotate_rows_signed.argtypes = [P, I64, I64, ctypes.c_int32, P, P, P]
         L.orc_rotate_rows_signed.restype = ctypes.c_int
+        L.orc_rotate_rows_inverse.argtypes = [P, I64, I64, ctypes.c_int32, P, P]
+        L.orc_rotate_rows_inverse.restype = ctypes.c_int
         L.orc_gemv_f64.argtypes = [P, I64, I64, P, P, I64, ctypes.c_int32, P, P]
         L.orc_gemv_f64.restype = ctypes.c_int
         L.orc_max_threads.restype = ctypes.c_int
@@ -226,6 +228,36 @@ def rotate_rows(x, n=HADAMARD_N, signs=None):
     _check(lib().orc_rotate_rows_signed(x2.ctypes.data, rows, k, int(n), sp, o64.ctypes.data, o32.ctypes.data),
            "rotate_rows")
     return o64.reshape(shape), o32.reshape(shape)
+
+
+def rotate_rows_inverse(z, n=HADAMARD_N, signs=None):
+    """e = R^T z = S (H_n z) / sqrt(n) per n-block along the last axis (FP64)."""
+    z = _f32(z)
+    shape = z.shape
+    z2 = z.reshape(-1, shape[-1])
+    rows, k = z2.shape
+    out = np.empty((rows, k), dtype=np.float64)
+    sp = None
+    if signs is not None:
+        sg = np.ascontiguousarray(signs, dtype=np.int8)
+        if sg.shape != (k,):
+            raise OracleError("signs length mismatch")
+        sp = sg.ctypes.data
+    _check(lib().orc_rotate_rows_inverse(z2.ctypes.data, rows, k, int(n), sp, out.ctypes.data), "rotate_rows_inverse")
+    return out.reshape(shape)
+
+
+def embed_reference(fmt, blocks, vocab, dim, ids, had=HADAMARD_N, signs=None):
+    """Rows `ids` of a quantized table (blocks of the stored rows), dequantized;
+    for PQ2_0 the stored rows are R e, so e = R^T z (transform, then signs).
+    Returns (FP64 rows, per-row-block sum |z| for the error bound)."""
+    deq = {"q8_0": q8_0_dequant, "pq2_0": pq2_0_dequant, "scale4": scale4_dequant}[fmt](blocks, vocab, dim)
+    z = deq[np.asarray(ids)]
+    if fmt != "pq2_0":
+        return z.astype(np.float64), None
+    e = rotate_rows_inverse(z, had, signs)
+    blk = np.abs(z.astype(np.float64)).reshape(len(ids), -1, had).sum(axis=2).repeat(had, axis=1)
+    return e, blk
 
 
 # -- GEMV ---------------------------------------------------------------------

@@ -422,6 +422,35 @@ int orc_rotate_rows_signed(const float* in, int64_t rows, int64_t k, int32_t n, 
   return ORC_OK;
 }
 
+/* The inverse of the signed rotation, e = R^T z = S (H_n z) / sqrt(n) per
+ * n-block: the transform first, then the sign flip (the Bonsai page, section
+ * 4.2, embedding inverse), with the explicit FP64 matrix. */
+int orc_rotate_rows_inverse(const float* in, int64_t rows, int64_t k, int32_t n, const int8_t* signs, double* out64) {
+  if (!is_pow2(n) || rows < 0 || k <= 0 || k % n != 0) return ORC_ERR_SHAPE;
+  if (signs)
+    for (int64_t c = 0; c < k; ++c)
+      if (signs[c] != 1 && signs[c] != -1) return ORC_ERR_SHAPE;
+  const double inv_sqrt_n = 1.0 / sqrt((double)n);
+  int64_t nblk = k / n;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t b = 0; b < nblk; ++b) {
+      const float* v = in + r * k + b * n;
+      for (int32_t i = 0; i < n; ++i) {
+        double s = 0.0;
+        for (int32_t c = 0; c < n; ++c) {
+          double h = (popcount64((uint64_t)(i & c)) & 1) ? -1.0 : 1.0;
+          s += h * (double)v[c];
+        }
+        double o = inv_sqrt_n * s;
+        if (signs) o *= (double)signs[b * n + i];
+        out64[r * k + b * n + i] = o;
+      }
+    }
+  }
+  return ORC_OK;
+}
+
 /* ------------------------------------------------------------------------ */
 /* GEMV in FP64                                                               */
 /* ------------------------------------------------------------------------ */

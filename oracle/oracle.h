@@ -106,6 +106,11 @@ int orc_rotate_rows(const float* in, int64_t rows, int64_t k, int32_t n, double*
 int orc_rotate_rows_signed(const float* in, int64_t rows, int64_t k, int32_t n, const int8_t* signs, double* out64,
                            float* out32);
 
+/* The inverse rotation e = R^T z = S (H_n z) / sqrt(n) per n-block (the
+ * Bonsai page, section 4.2: the embedding table stores R e per row; after
+ * the gather, transform first, then the sign flip).  FP64 out. */
+int orc_rotate_rows_inverse(const float* in, int64_t rows, int64_t k, int32_t n, const int8_t* signs, double* out64);
+
 /* y_i = sum_j w_ij x_j and absdot_i = sum_j |w_ij x_j| in FP64 for the listed
  * rows (rows == NULL: all n rows, in order); w holds the n x k matrix (or
  * just the listed rows when rows_are_packed != 0). */

@@ -154,6 +154,23 @@ def test_signed_rotation_of_a_signed_unit_vector():
         assert np.array_equal(got[0], want)
 
 
+def test_inverse_rotation_undoes_the_rotation_and_matches_scipy():
+    """R^T R = I (orthogonality) through the two independent oracle routines,
+    and the inverse against scipy's Hadamard matrix with the sign flip last."""
+    k = 3072
+    s = _signs(k, 21)
+    x = np.random.default_rng(22).standard_normal((3, k)).astype(np.float32)
+    for n, sg in ((128, None), (1024, s), (1024, None)):
+        _, z32 = oracle.rotate_rows(x, n, signs=sg)
+        back = oracle.rotate_rows_inverse(z32, n, signs=sg)
+        assert np.max(np.abs(back - x)) <= 4e-6 * np.max(np.abs(x))  # z rounded to fp32 once
+    z = np.random.default_rng(23).standard_normal((2, k)).astype(np.float32)
+    H = scipy.linalg.hadamard(1024).astype(np.float64)
+    want = np.concatenate([s[b * 1024:(b + 1) * 1024] * (H @ z[:, b * 1024:(b + 1) * 1024].astype(np.float64).T).T
+                           for b in range(3)], axis=1) / 32.0
+    assert np.allclose(oracle.rotate_rows_inverse(z, 1024, signs=s), want, rtol=0, atol=1e-12 * np.abs(z).sum())
+
+
 def test_signed_rotation_rejects_bad_signs():
     x = np.zeros((1, 1024), dtype=np.float32)
     bad = np.ones(1024, dtype=np.int8)
