@@ -178,6 +178,16 @@ int kq_quantize_pq2_0_device(const float* d_w_rot, int64_t n, int64_t k, void* d
                              void* stream);
 int kq_quantize_scale4_device(const float* d_w, int64_t n, int64_t k, void* d_codes, void* d_scales, void* stream);
 
+/* Embedding lookup: d_out[t][0..k) = row d_ids[t] of the n x k table E,
+ * dequantized; for a PQ2_0 table (stored rotated, R e per row, as the Bonsai
+ * page's token_embd) the inverse rotation e = R^T z = S (H_n z)/sqrt(n) per
+ * n-block follows, the transform first, then the sign flip (section 4.2), in
+ * fp32.  d_ids int32 [count], d_out fp32 [count][k], both 16-byte aligned
+ * device memory.  An id outside [0, n) yields a zero row and sets KQ_ERR_RANGE
+ * in the device status word (kq_device_status).  PQ2_0 tables up to k =
+ * 32768. */
+int kq_embed(const kq_qmat* E, const int32_t* d_ids, int64_t count, float* d_out, void* stream);
+
 /* Debug: write the dequantized n x k fp32 matrix (d*q or (q-1)*d, exact). */
 int kq_dequantize(const kq_qmat* W, float* d_out, void* stream);
 

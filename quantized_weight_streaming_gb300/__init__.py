@@ -94,6 +94,7 @@ SIGNATURES = {
     "kq_quantize_q8_0_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "kq_quantize_pq2_0_device": (ctypes.c_int, [_P, _I64, _I64, _P, _P, _P]),
     "kq_dequantize": (ctypes.c_int, [_QP, _P, _P]),
+    "kq_embed": (ctypes.c_int, [_QP, _P, _I64, _P, _P]),
     "kq_hadamard_blockwise": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _P]),
     "kq_rotate_blockwise_host": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _P]),
     "kq_rotate_blockwise": (ctypes.c_int, [_P, _P, _I64, _I64, _I32, _P, _P]),
@@ -281,6 +282,11 @@ def kq_quantize_pq2_0_device(W, d_w_rot, stream=None):
 def kq_quantize_scale4_device(W, d_w, stream=None):
     _check(_lib.kq_quantize_scale4_device(_ptr(d_w), W.n, W.k, W.codes.data_ptr(), W.scales.data_ptr(),
                                           _stream(stream)), "kq_quantize_scale4_device")
+
+
+def kq_embed(E, d_ids, count, d_out, stream=None):
+    """Rows d_ids of the quantized table E, dequantized (and inverse-rotated for PQ2_0)."""
+    _check(_lib.kq_embed(ctypes.byref(E.desc), _ptr(d_ids), count, _ptr(d_out), _stream(stream)), "kq_embed")
 
 
 def kq_dequantize(W, d_out, stream=None):

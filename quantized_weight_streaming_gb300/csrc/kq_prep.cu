@@ -6,6 +6,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include "kq_device.cuh"
@@ -242,6 +243,94 @@ __global__ void hadamard_f64_smem_kernel(const float* __restrict__ in, float* __
 }
 
 // --------------------------------------------------------------------------
+// Embedding lookup: rows of a quantized table, dequantized; a rotated PQ2_0
+// table stores R e per row, so the lookup returns e = R^T z = S (H z)/sqrt(n)
+// per n-block, the transform first, then the sign flip (the Bonsai page,
+// section 4.2).  One CTA per token; PQ2_0 rows go through shared memory
+// (k floats): each warp dequantizes and transforms 128-blocks (4 elements per
+// lane), an 8-point pass joins them into 1024-blocks (H_1024 = H_8 (x)
+// H_128), then the scale, the signs and the store.
+// --------------------------------------------------------------------------
+__global__ void embed_kernel(int fmt, const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                             int64_t n, int64_t k, int64_t sstride, const int32_t* __restrict__ ids, int64_t count,
+                             int had, const int8_t* __restrict__ signs, float* __restrict__ out) {
+  extern __shared__ float zrow[];  // k floats (PQ2_0)
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int64_t t = blockIdx.x; t < count; t += gridDim.x) {
+    const int64_t id = ids[t];
+    float* o = out + t * k;
+    if (id < 0 || id >= n) {
+      if (threadIdx.x == 0) prep_flag(KQ_ERR_RANGE);
+      for (int64_t c = threadIdx.x; c < k; c += blockDim.x) o[c] = 0.f;
+      continue;
+    }
+    const uint16_t* srow = scales + id * sstride;
+    if (fmt == KQ_Q8_0) {
+      const int8_t* q = reinterpret_cast<const int8_t*>(codes) + id * k;
+      for (int64_t c = threadIdx.x; c < k; c += blockDim.x)
+        o[c] = (float)q[c] * __half2float(__ushort_as_half(srow[c / 32]));
+      continue;
+    }
+    if (fmt == KQ_SCALE4) {
+      const uint8_t* q = codes + id * (k / 2);
+      for (int64_t c = threadIdx.x; c < k; c += blockDim.x)
+        o[c] = (float)((int)((q[c / 2] >> (4 * (c % 2))) & 15) - 8) * __half2float(__ushort_as_half(srow[c / 32]));
+      continue;
+    }
+    // PQ2_0: words of 16 codes, element 16i + j at bits 2j of word i
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(codes + id * (k / 4));
+    for (int64_t b = warp; b < k / 128; b += nwarps) {
+      const float d = __half2float(__ushort_as_half(srow[b]));
+      const uint32_t word = w[b * 8 + lane / 4];
+      float v[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = (float)((int)((word >> (2 * (4 * (lane & 3) + e))) & 3u) - 1) * d;
+      float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+      v[0] = a0 + a2;
+      v[2] = a0 - a2;
+      v[1] = a1 + a3;
+      v[3] = a1 - a3;
+#pragma unroll
+      for (int mk = 1; mk < 32; mk <<= 1) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float q = __shfl_xor_sync(0xffffffffu, v[e], mk);
+          v[e] = (lane & mk) ? (q - v[e]) : (v[e] + q);
+        }
+      }
+      *reinterpret_cast<float4*>(zrow + b * 128 + 4 * lane) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    __syncthreads();
+    if (had == 1024) {
+      for (int64_t c = threadIdx.x; c < (k / 1024) * 128; c += blockDim.x) {
+        float* col = zrow + (c / 128) * 1024 + (c % 128);
+        float v[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) v[a] = col[a * 128];
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+          for (int a = 0; a < 8; ++a)
+            if (!(a & h)) {
+              const float x0 = v[a], x1 = v[a + h];
+              v[a] = x0 + x1;
+              v[a + h] = x0 - x1;
+            }
+#pragma unroll
+        for (int a = 0; a < 8; ++a) col[a * 128] = v[a];
+      }
+      __syncthreads();
+    }
+    const float scale = had == 1024 ? 0.03125f : 0.08838834764831845f;
+    for (int64_t c = threadIdx.x; c < k; c += blockDim.x) {
+      const float e = zrow[c] * scale;
+      o[c] = signs ? e * (float)signs[c] : e;
+    }
+    __syncthreads();  // zrow is reused by the next token
+  }
+}
+
+// --------------------------------------------------------------------------
 // Debug dequantizer.
 // --------------------------------------------------------------------------
 __global__ void dequant_kernel(int fmt, const uint8_t* __restrict__ codes, const uint16_t* __restrict__ scales,
@@ -365,6 +454,33 @@ int kq_dequantize(const kq_qmat* W, float* d_out, void* stream) {
   const int64_t ss = scale_stride(W->fmt, W->k);
   dequant_kernel<<<grid_for(W->n * W->k, 256), 256, 0, (cudaStream_t)stream>>>(
       W->fmt, (const uint8_t*)W->codes, (const uint16_t*)W->scales, W->n, W->k, ss, d_out);
+  KQ_CUDA_TRY(cudaGetLastError());
+  return KQ_OK;
+}
+
+int kq_embed(const kq_qmat* E, const int32_t* d_ids, int64_t count, float* d_out, void* stream) {
+  clear_error();
+  if (int s = check_qmat(E, -1)) return s;
+  if (count < 0) return fail(KQ_ERR_SHAPE, "count = %lld", (long long)count);
+  if (count == 0) return KQ_OK;
+  if (!d_ids || !d_out) return fail(KQ_ERR_INVALID_ARG, "NULL ids or output");
+  if (!aligned16(d_ids) || !aligned16(d_out)) return fail(KQ_ERR_ALIGNMENT, "ids or output not 16-byte aligned");
+  if (E->fmt == KQ_PQ2_0 && E->k > 32768)
+    return fail(KQ_ERR_UNSUPPORTED, "k = %lld above the 32768 a PQ2_0 lookup transforms in shared memory",
+                (long long)E->k);
+  const size_t smem = E->fmt == KQ_PQ2_0 ? (size_t)E->k * sizeof(float) : 0;
+  static bool attr_set = false;
+  if (!attr_set) {
+    KQ_CUDA_TRY(cudaFuncSetAttribute(embed_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 32768 * 4));
+    attr_set = true;
+  }
+  int dev = 0, sms = 0;
+  KQ_CUDA_TRY(cudaGetDevice(&dev));
+  KQ_CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int grid = (int)std::min<int64_t>(count, (int64_t)sms * 8);
+  embed_kernel<<<grid, 256, smem, (cudaStream_t)stream>>>(E->fmt, (const uint8_t*)E->codes, (const uint16_t*)E->scales,
+                                                          E->n, E->k, scale_stride(E->fmt, E->k), d_ids, count,
+                                                          E->had_block, E->signs, d_out);
   KQ_CUDA_TRY(cudaGetLastError());
   return KQ_OK;
 }

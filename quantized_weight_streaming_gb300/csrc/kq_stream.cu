@@ -57,7 +57,18 @@ namespace kq {
 
 // ---- geometry ---------------------------------------------------------------
 constexpr int kConsumerWarps = 16;
-constexpr int kThreads = 32 * (kConsumerWarps + 1);
+// Warp roles: one producer warpgroup (warp 0 issues the copies, warps 1-3
+// hold no role) gives registers to the sixteen consumer warps with
+// setmaxnreg.  The launch allocates kThreads x kLaunchRegs registers (every
+// instantiation compiles to exactly kLaunchRegs, checked before the first
+// launch); the split below must not exceed it, or setmaxnreg.inc would wait
+// for registers that never come.
+constexpr int kProducerWarps = 4;
+constexpr int kThreads = 32 * (kConsumerWarps + kProducerWarps);
+constexpr int kLaunchRegs = 96;
+constexpr int kProducerRegs = 32, kConsumerRegs = 112;
+static_assert(32 * (kProducerWarps * kProducerRegs + kConsumerWarps * kConsumerRegs) <= kThreads * kLaunchRegs,
+              "register split above the launch allocation");
 constexpr int kRowsPerWarp = 8;   // Q8_0 rows per consumer warp
 constexpr int kChunkBytes = 256;  // code bytes per row per tile (32 lanes x 8 B)
 constexpr int kXMax = 18432;          // activation floats (or B-fragment words) staged per item (all m)
@@ -822,6 +833,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 
   const int nst = LINKED ? p.nstages : 1;
 
+  if (warp < kProducerWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kProducerRegs) : "memory");
+    if (warp != 0) return;
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kConsumerRegs) : "memory");
+  }
   if (warp == 0) {
     // ------------------------------- producer -------------------------------
     // The weight stream never waits for a stage: it runs ahead into the next
@@ -877,7 +894,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   }
 
   // -------------------------------- consumers --------------------------------
-  const int cw = warp - 1;
+  const int cw = warp - kProducerWarps;
   float* scratch = scratch_all + cw * kScratchFloats;
   ItemCursor cur;
   // The staged activation slice.  Unlinked: keyed by (job, split).  Linked:
@@ -1227,15 +1244,33 @@ static int device_sms(int* sms) {
   return KQ_OK;
 }
 
+// Sets the kernel's shared-memory limit and checks that it was compiled to
+// the register count the setmaxnreg split assumes (once per kernel).
+template <typename K>
+static int prepare_kernel_once(K kernel, size_t smem, std::once_flag& once, int& status, char (&msg)[160]) {
+  std::call_once(once, [&] {
+    cudaFuncAttributes a{};
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&a, kernel);
+    if (e != cudaSuccess) {
+      status = KQ_ERR_CUDA;
+      snprintf(msg, sizeof(msg), "kernel attributes: %s", cudaGetErrorString(e));
+    } else if (a.numRegs != kLaunchRegs) {
+      status = KQ_ERR_UNSUPPORTED;
+      snprintf(msg, sizeof(msg), "stream kernel built with %d registers per thread, not %d: its register split "
+               "would not fit", a.numRegs, kLaunchRegs);
+    }
+  });
+  return status == KQ_OK ? KQ_OK : fail(status, "%s", msg);
+}
+
 template <int FMT, int M, bool IO16 = false>
 static int launch_stream(const Params& p, int grid, cudaStream_t st) {
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(stream_kernel<FMT, M, false, IO16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)Geo<FMT>::kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return fail(KQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  static int status = KQ_OK;
+  static char msg[160];
+  if (int s = prepare_kernel_once(stream_kernel<FMT, M, false, IO16>, Geo<FMT>::kSmemBytes, once, status, msg))
+    return s;
   stream_kernel<FMT, M, false, IO16><<<grid, kThreads, Geo<FMT>::kSmemBytes, st>>>(p);
   KQ_CUDA_TRY(cudaGetLastError());
   return KQ_OK;
@@ -1583,12 +1618,9 @@ static int launch_plan(const Params& p, int grid, bool cooperative, cudaStream_t
   // The CTAs of a linked plan wait for one another (stage counters): the
   // cooperative launch guarantees that all of them are resident at once.
   static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(stream_kernel<FMT, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)Geo<FMT>::kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return fail(KQ_ERR_CUDA, "cudaFuncSetAttribute: %s", cudaGetErrorString(attr_err));
+  static int status = KQ_OK;
+  static char msg[160];
+  if (int s = prepare_kernel_once(stream_kernel<FMT, 1, true>, Geo<FMT>::kSmemBytes, once, status, msg)) return s;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kThreads);

@@ -216,6 +216,12 @@ def test_device_entry_points_validate_before_any_cuda_call(kq):
     assert lib.kq_gemv_scale4(ctypes.byref(good), A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG  # a Q8_0 matrix
     s4_bad = kq.kq_qmat(kq.KQ_SCALE4, 0, 8, 48, A, A)
     assert lib.kq_gemv_scale4(ctypes.byref(s4_bad), A, A, None, 0, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_embed(ctypes.byref(good), None, 4, A, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_embed(ctypes.byref(good), A + 4, 4, A, None) == kq.KQ_ERR_ALIGNMENT
+    assert lib.kq_embed(ctypes.byref(good), A, -1, A, None) == kq.KQ_ERR_SHAPE
+    assert lib.kq_embed(ctypes.byref(good), A, 0, A, None) == kq.KQ_OK  # nothing to do
+    wide_pq = kq.kq_qmat(kq.KQ_PQ2_0, 128, 8, 65536, A, A)
+    assert lib.kq_embed(ctypes.byref(wide_pq), A, 4, A, None) == kq.KQ_ERR_UNSUPPORTED
     ptq = kq.kq_qmat(kq.KQ_PTQ1_0, 128, 8, 128, A, A)  # a storage format is not a matrix format
     assert lib.kq_gemv_pq2_0(ctypes.byref(ptq), A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
     assert lib.kq_stream_read(None, 1024, 4096, 4, A, None) == kq.KQ_ERR_INVALID_ARG

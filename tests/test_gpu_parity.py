@@ -504,6 +504,48 @@ def test_decode_plan_small_mixed_shapes(kq, wl):
 
 
 # ----------------------------------------------------------------------------
+# embedding lookup (gather + dequantize + inverse rotation)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("fmt,vocab,dim,had", [("q8_0", 1000, 2560, 0), ("scale4", 700, 2080, 0),
+                                               ("pq2_0", 600, 5120, 128), ("pq2_0", 300, 5120, 1024)])
+def test_embed_matches_oracle(kq, wl, fmt, vocab, dim, had):
+    sid = synth.stream_id("test", 0, 480 + dim % 89)
+    sh, sd = (wl.build_signs(dim, 4, synth.stream_id("test", 1, 481)) if had == 1024 else (None, None))
+    E = wl.build_matrix(fmt, vocab, dim, 10, sid, had_block=(1024 if had == 1024 else None), signs=sd)
+    ids = np.array([0, vocab - 1, 5, 5, 123, 77, vocab // 2], dtype=np.int32)
+    out = torch.empty(len(ids) * dim, dtype=torch.float32, device="cuda")
+    kq.kq_embed(E, torch.from_numpy(ids).cuda(), len(ids), out)
+    _sync_ok(kq)
+    got = out.cpu().numpy().reshape(len(ids), dim).astype(np.float64)
+    e = synth.matrix_rows_host(vocab, dim, np.arange(vocab), 10, sid)
+    if fmt == "pq2_0":
+        blocks = oracle.pq2_0_quantize(oracle.rotate_rows(e, had, signs=sh)[1])
+    else:
+        blocks = (oracle.q8_0_quantize if fmt == "q8_0" else oracle.scale4_quantize)(e)
+    want, blk = oracle.embed_reference(fmt, blocks, vocab, dim, ids, had if had else 128, sh)
+    if fmt != "pq2_0":
+        assert np.array_equal(got, want)  # a dequantized row is exact
+    else:  # an fp32 transform: (log2 n + 3) 2^-24 sum_blk |z| / sqrt(n) per element
+        n = had
+        assert np.all(np.abs(got - want) <= (np.log2(n) + 3) * 2.0**-24 * blk / np.sqrt(n) + 1e-30)
+        # the rows are the original (unrotated) embeddings up to the quantization of R e
+        assert np.corrcoef(got[0], e[0])[0, 1] > 0.6  # ternary codes of Gaussian rows: about 0.73
+
+
+def test_embed_out_of_range_ids(kq, wl):
+    E = wl.build_matrix("q8_0", 10, 64, 1, synth.stream_id("test", 0, 485))
+    ids = torch.tensor([3, -1, 10, 9], dtype=torch.int32, device="cuda")
+    out = torch.full((4 * 64,), 7.0, dtype=torch.float32, device="cuda")
+    kq.kq_embed(E, ids, 4, out)
+    torch.cuda.synchronize()
+    assert kq.kq_device_status(True) == kq.KQ_ERR_RANGE
+    o = out.cpu().numpy().reshape(4, 64)
+    assert not o[1].any() and not o[2].any() and o[0].any() and o[3].any()
+    assert kq.kq_device_status(True) == kq.KQ_OK
+
+
+# ----------------------------------------------------------------------------
 # the fp16 chain (fp16 activation in, fp16 output)
 # ----------------------------------------------------------------------------
 
