@@ -267,9 +267,11 @@ def _gemv_graph_measure(kq, wl_mod, fmt, n, k, m, stream, replays=20):
     nb = kq.kq_gemv_workspace_bytes(W0, m)
     ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
 
+    gemv = {"pq2_0": kq.kq_gemv_pq2_0, "q8_0": kq.kq_gemv_q8_0, "scale4": kq.kq_gemv_scale4}[fmt]
+
     def launch(Wm, st):
         if m == 1:
-            (kq.kq_gemv_pq2_0 if fmt == "pq2_0" else kq.kq_gemv_q8_0)(Wm, X, Y, ws, stream=st)
+            gemv(Wm, X, Y, ws, stream=st)
         else:
             kq.kq_gemm_small_m(Wm, X, m, Y, ws, stream=st)
 
@@ -396,7 +398,8 @@ def run_kq(args):
         for fmt, n, k, m in (("q8_0", 1024, 2560, 1), ("pq2_0", 10240, 5120, 1), ("q8_0", 9728, 2560, 1),
                              ("q8_0", 9728, 2560, 4), ("q8_0", 9728, 2560, 16), ("q8_0", 9728, 2560, 64),
                              ("pq2_0", 17408, 5120, 1), ("pq2_0", 17408, 5120, 4), ("pq2_0", 17408, 5120, 16),
-                             ("pq2_0", 17408, 5120, 64)):
+                             ("pq2_0", 17408, 5120, 64), ("scale4", 9728, 2560, 1), ("scale4", 9728, 2560, 4),
+                             ("scale4", 9728, 2560, 16), ("scale4", 9728, 2560, 64)):
             r = _gemv_graph_measure(kq, workloads, fmt, n, k, m, stream)
             gemv.append({key: (round(v, 3) if isinstance(v, float) else v) for key, v in r.items()})
         extras["gemv_graph"] = gemv

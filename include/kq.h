@@ -248,11 +248,14 @@ int kq_gemm_small_m(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, v
  * 16-bit tile, then multiplied): Y[m][n] = X[m][k] W^T, X rotated per
  * 128-block for PQ2_0 (unrotated X in, as for kq_gemv_pq2_0).
  *  - 1 <= m <= 64, k <= 32768; X, Y row-major fp32, 16-byte aligned.
- *  - Weights enter the tensor core as fp16 tiles: (c-1)*d exactly for PQ2_0;
- *    for Q8_0 as fp16(q*d) plus the residual q*d - fp16(q*d) (exact but for
- *    fp16 subnormals: absolute error <= 2^-25 per weight).  Each activation
- *    row enters as two fp16 rows, high and low part of x * 2^-e (e its
- *    largest exponent), so x keeps ~22 bits; fp32 accumulation.  A Q8_0
+ *  - Weights enter the tensor core as exact fp16 code values, one fp32
+ *    accumulator per quantization block, the block scale applied in the
+ *    epilogue: q for Q8_0, (c-1) times a power of two for PQ2_0, (q-8) times
+ *    a power of two for SCALE4 (a 4-bit code masked in place in an fp16 half
+ *    is an exact subnormal; one fp16 subtraction applies the zero point).
+ *    Each activation row enters as two fp16 rows, high and low part of
+ *    x * 2^-e (e its largest exponent), so x keeps ~22 bits; fp32
+ *    accumulation.  A Q8_0
  *    scale above 65504/127 (q*d not a finite fp16) sets KQ_ERR_RANGE.
  *  - splits: K splits (0 = automatic); with splits > 1 the partial sums are
  *    added in split order by a second pass (deterministic).

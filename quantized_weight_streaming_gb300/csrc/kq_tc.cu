@@ -86,7 +86,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACols = kChunk / 2;
 constexpr uint32_t kTmemD = 2 * kACols;
 
-__host__ __device__ constexpr int code_chunk_bytes(int fmt) { return fmt == KQ_Q8_0 ? kRows * kChunk : kRows * kChunk / 4; }
+// code bytes of one 128-weight chunk of a row: 128 (Q8_0), 64 (SCALE4), 32 (PQ2_0)
+__host__ __device__ constexpr int chunk_row_bytes(int fmt) {
+  return fmt == KQ_Q8_0 ? kChunk : (fmt == KQ_SCALE4 ? kChunk / 2 : kChunk / 4);
+}
+__host__ __device__ constexpr int code_chunk_bytes(int fmt) { return kRows * chunk_row_bytes(fmt); }
 __host__ __device__ constexpr int b_box_bytes(int mp) { return 2 * mp * 128; }  // 64 fp16 x 2M' rows
 __host__ __device__ constexpr int stage_tx_bytes(int fmt, int mp) {
   return code_chunk_bytes(fmt) + kScaleBoxBytes + 2 * b_box_bytes(mp);
@@ -95,7 +99,7 @@ __host__ __device__ constexpr int stage_bytes(int fmt, int mp) { return (stage_t
 // Accumulator groups: a group holds `gb` consecutive blocks' accumulators
 // (2M' columns each) under one barrier pair, so the MMA thread waits and
 // commits once per group; groups rotate through d_groups() buffers.
-__host__ __device__ constexpr int blocks_per_chunk(int fmt) { return fmt == KQ_Q8_0 ? 4 : 1; }
+__host__ __device__ constexpr int blocks_per_chunk(int fmt) { return fmt == KQ_PQ2_0 ? 1 : 4; }
 __host__ __device__ constexpr int d_groups_for(int gb, int mp) {
   return (int)((kTmemCols - kTmemD) / (gb * 2 * mp)) < kMaxD ? (int)((kTmemCols - kTmemD) / (gb * 2 * mp)) : kMaxD;
 }
@@ -211,6 +215,12 @@ __host__ __device__ constexpr int pq2_0_shift(int e) { return e <= 4 ? 2 * e : 2
 // K position of weight j (within its 16-weight group) in a PQ2_0 B row: even
 // positions hold weights 0..7, odd positions weights 8..15.
 __device__ __forceinline__ int pq2_0_pos(int j) { return j < 8 ? 2 * j : 2 * (j - 8) + 1; }
+// SCALE4: a word's 4-bit codes unpack as the pairs (0,4), (1,5), (2,6),
+// (3,7) of its eight weights, codes 1, 3, 5, 7 at bit offset 4 inside their
+// fp16 half and codes 0, 2, 4, 6 at offset 0; weight j of an 8-group goes to
+// B position 2 (j % 4) + j / 4.
+__host__ __device__ constexpr int scale4_shift(int j) { return 4 * (j & 1); }
+__device__ __forceinline__ int scale4_pos(int j) { return 2 * (j & 3) + (j >> 2); }
 
 template <int FMT>
 __global__ void act_hilo_kernel(const float* __restrict__ X, int m, int mp, int64_t k, __half* __restrict__ B,
@@ -300,9 +310,9 @@ __global__ void act_hilo_kernel(const float* __restrict__ X, int m, int mp, int6
     for (int w = 0; w < nwarps; ++w) a = fmaxf(a, red[w]);
     // e = floor(log2 a) for normal a: x * 2^-e then lies in (-2, 2)
     int e = a > 0.f ? ((__float_as_int(a) >> 23) & 0xFF) - 127 : 0;
-    if (FMT == KQ_PQ2_0 && e > 116) tc_flag(KQ_ERR_RANGE);  // 2^(10+e) must stay a finite fp32
-    // PQ2_0 also scales by 2^(14-s-e) with s <= 8 and by 2^(10+e): e in [-113, 116]
-    red[0] = FMT == KQ_PQ2_0 ? (float)max(-113, min(116, e)) : (float)max(-126, min(126, e));
+    if (FMT != KQ_Q8_0 && e > 116) tc_flag(KQ_ERR_RANGE);  // 2^(10+e) must stay a finite fp32
+    // PQ2_0 and SCALE4 also scale by 2^(14-s-e) with s <= 8 and by 2^(10+e): e in [-113, 116]
+    red[0] = FMT != KQ_Q8_0 ? (float)max(-113, min(116, e)) : (float)max(-126, min(126, e));
   }
   __syncthreads();
   const int e = (int)red[0];
@@ -315,6 +325,17 @@ __global__ void act_hilo_kernel(const float* __restrict__ X, int m, int mp, int6
       lo[j] = __float2half_rn(v - __half2float(h));  // v - h is exact in fp32
     }
     if (threadIdx.x == 0) bscale[i] = __int_as_float((127 + e) << 23);  // 2^e
+  } else if (FMT == KQ_SCALE4) {
+    // B entry of weight j: x_j 2^(14 - s - e), s the bit offset of its code, at its unpack position
+    for (int64_t j = threadIdx.x; j < k; j += blockDim.x) {
+      const int jj = (int)(j & 7);
+      const float v = xs[j] * __int_as_float((127 + 14 - scale4_shift(jj) - e) << 23);
+      const __half h = __float2half_rn(v);
+      const int64_t pos = (j & ~(int64_t)7) + scale4_pos(jj);
+      hi[pos] = h;
+      lo[pos] = __float2half_rn(v - __half2float(h));
+    }
+    if (threadIdx.x == 0) bscale[i] = __int_as_float((127 + 10 + e) << 23);  // 2^(10+e)
   } else {
     // B entry of weight j: x'_j 2^(14 - s - e), s the bit offset of its code
     for (int64_t j = threadIdx.x; j < k; j += blockDim.x) {
@@ -418,6 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           const int32_t y0 = tile * kRows;
           if (FMT == KQ_Q8_0) {
             tma_load_2d(st, &p.map_codes, c * (kChunk / 4), y0, bar, policy);
+            tma_load_2d(st + off_scales, &p.map_scales, (4 * c) & ~7, y0, bar, policy);
+          } else if (FMT == KQ_SCALE4) {
+            tma_load_2d(st, &p.map_codes, c * (kChunk / 8), y0, bar, policy);
             tma_load_2d(st + off_scales, &p.map_scales, (4 * c) & ~7, y0, bar, policy);
           } else {
             tma_load_2d(st, &p.map_codes, c * (kChunk / 16), y0, bar, policy);
@@ -531,6 +555,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 }
                 tmem_st8(a_tmem + (uint32_t)(j * 8), o);
               }
+            } else if (FMT == KQ_SCALE4) {
+              // 64 codes of the row: 32 bytes (16-byte pieces 2 khalf, 2 khalf + 1)
+              // of the 64-byte row, 64-byte swizzle (piece c of row r at c ^ ((r / 2) % 4))
+#pragma unroll
+              for (int pc = 0; pc < 2; ++pc) {
+                const int piece = (2 * khalf + pc) ^ ((r >> 1) & 3);
+                const uint4 cw = *reinterpret_cast<const uint4*>(st + r * 64 + piece * 16);
+                const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+                for (int wh = 0; wh < 2; ++wh) {  // two words per 8 registers
+                  uint32_t o[8];
+#pragma unroll
+                  for (int q = 0; q < 8; ++q) {
+                    // pair (q % 4, q % 4 + 4) of word 2 wh + q / 4: masked in place it is
+                    // c * 2^(s-24); one fp16 subtraction of 8 * 2^(s-24) makes it (c - 8) * 2^(s-24), exact
+                    const uint32_t w = w4[2 * wh + (q >> 2)];
+                    const int pr = q & 3;
+                    const uint32_t src = pr < 2 ? w : w >> 8;
+                    const uint32_t cbits = src & (0x000F000Fu << scale4_shift(pr));
+                    o[q] = h2_bits(__hsub2(bits_h2(cbits), bits_h2(0x00080008u << scale4_shift(pr))));
+                  }
+                  tmem_st8(a_tmem + (uint32_t)(pc * 16 + wh * 8), o);
+                }
+              }
             } else {
               // 64 codes of the row: 16 bytes at column 16*khalf of the
               // 32-byte row, 32-byte swizzle (halves swapped on every other
@@ -590,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const uint8_t* st = stages + (size_t)ring.slot * sbytes;
             // this chunk's block scales of row r, from its 16-byte box
             const __half* srow = reinterpret_cast<const __half*>(st + off_scales + r * 16);
-            const int s0 = FMT == KQ_Q8_0 ? 4 * (c & 1) : (c & 7);
+            const int s0 = kBlocks == 4 ? 4 * (c & 1) : (c & 7);
             for (int b = 0; b < kBlocks; ++b) {
               const int bg = b % gb;
               if (bg == 0) {
@@ -688,7 +736,7 @@ TcGeometry tc_geometry(const kq_qmat* W, int64_t m, int sms, int requested) {
   TcGeometry g;
   g.mp = (m + 15) / 16 * 16;
   g.nb = 2 * g.mp;
-  const int fmt = W->fmt == KQ_Q8_0 ? KQ_Q8_0 : KQ_PQ2_0;
+  const int fmt = W->fmt;
   g.stages = (int)std::min<int64_t>(tc::kMaxStages, (int64_t)tc::kCarveBytes / tc::stage_bytes(fmt, (int)g.mp));
   g.tiles = (int)((W->n + tc::kRows - 1) / tc::kRows);
   g.chunks = (int)((W->k + tc::kChunk - 1) / tc::kChunk);
@@ -768,8 +816,8 @@ int encode(PFN_cuTensorMapEncodeTiled_v12000 fn, CUtensorMap* map, CUtensorMapDa
 }  // namespace
 
 int tc_check(const kq_qmat* W, int64_t m) {
-  if (W->fmt != KQ_Q8_0 && W->fmt != KQ_PQ2_0)
-    return fail(KQ_ERR_UNSUPPORTED, "format %d has no tensor-core path (the streaming kernel serves it)", W->fmt);
+  if (W->fmt != KQ_Q8_0 && W->fmt != KQ_PQ2_0 && W->fmt != KQ_SCALE4)
+    return fail(KQ_ERR_UNSUPPORTED, "format %d has no tensor-core path", W->fmt);
   if (m < 1 || m > kTcMaxM) return fail(KQ_ERR_SHAPE, "m = %lld outside [1, %d]", (long long)m, kTcMaxM);
   if (W->k > kTcMaxK)
     return fail(KQ_ERR_SHAPE, "k = %lld above the tensor-core path's %d", (long long)W->k, kTcMaxK);
@@ -807,12 +855,15 @@ int tc_gemm(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int split
   float* part = g.splits > 1 ? reinterpret_cast<float*>(ws + g.b_bytes + g.s_bytes) : nullptr;
 
   tc::TcParams p{};
-  const bool q8 = W->fmt == KQ_Q8_0;
   const int64_t rowbytes = code_row_bytes(W->fmt, W->k);
   const int64_t ss = scale_stride(W->fmt, W->k);
+  // one chunk of a row per box row: 128 bytes (Q8_0), 64 (SCALE4), 32 (PQ2_0), each with the matching swizzle
+  const uint32_t box_u32 = (uint32_t)tc::chunk_row_bytes(W->fmt) / 4;
+  const CUtensorMapSwizzle cswz = W->fmt == KQ_Q8_0    ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : W->fmt == KQ_SCALE4 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                        : CU_TENSOR_MAP_SWIZZLE_32B;
   if (int s = encode(fn, &p.map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, W->codes, rowbytes / 4, W->n, rowbytes,
-                     q8 ? 32u : 8u, tc::kRows, q8 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B,
-                     "the codes plane"))
+                     box_u32, tc::kRows, cswz, "the codes plane"))
     return s;
   if (int s = encode(fn, &p.map_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, W->scales, ss, W->n, ss * 2, 8u, tc::kRows,
                      CU_TENSOR_MAP_SWIZZLE_NONE, "the scales plane"))
@@ -831,13 +882,17 @@ int tc_gemm(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int split
   p.stages = g.stages;
 
   cudaStream_t st = (cudaStream_t)stream;
-  if (q8) {
+  const int grid = (int)std::min<int64_t>((int64_t)g.tiles * g.splits, sms);
+  if (W->fmt == KQ_Q8_0) {
     if (int s = launch_act<KQ_Q8_0>(W, d_X, (int)m, W->k, g.mp, B, bscale, st)) return s;
+    if (int s = launch_tc<KQ_Q8_0>(p, grid, st)) return s;
+  } else if (W->fmt == KQ_SCALE4) {
+    if (int s = launch_act<KQ_SCALE4>(W, d_X, (int)m, W->k, g.mp, B, bscale, st)) return s;
+    if (int s = launch_tc<KQ_SCALE4>(p, grid, st)) return s;
   } else {
     if (int s = launch_act<KQ_PQ2_0>(W, d_X, (int)m, W->k, g.mp, B, bscale, st)) return s;
+    if (int s = launch_tc<KQ_PQ2_0>(p, grid, st)) return s;
   }
-  const int grid = (int)std::min<int64_t>((int64_t)g.tiles * g.splits, sms);
-  if (int s = q8 ? launch_tc<KQ_Q8_0>(p, grid, st) : launch_tc<KQ_PQ2_0>(p, grid, st)) return s;
   if (g.splits > 1) {
     const int64_t total = m * W->n;
     const int rgrid = (int)std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8);

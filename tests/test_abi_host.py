@@ -212,7 +212,7 @@ def test_device_entry_points_validate_before_any_cuda_call(kq):
     assert lib.kq_rotate_blockwise(A, A, 1, 2048, 1024, A + 1, None) == kq.KQ_ERR_ALIGNMENT
     assert lib.kq_rotate_blockwise(A, A, 1, 1000, 1024, None, None) == kq.KQ_ERR_SHAPE
     s4 = kq.kq_qmat(kq.KQ_SCALE4, 0, 8, 2560, A, A)
-    assert lib.kq_gemm_tc(ctypes.byref(s4), A, 16, A, 0, None, 0, None) == kq.KQ_ERR_UNSUPPORTED
+    assert lib.kq_gemm_tc(ctypes.byref(s4), A, 65, A, 0, None, 0, None) == kq.KQ_ERR_SHAPE
     assert lib.kq_gemv_scale4(ctypes.byref(good), A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG  # a Q8_0 matrix
     s4_bad = kq.kq_qmat(kq.KQ_SCALE4, 0, 8, 48, A, A)
     assert lib.kq_gemv_scale4(ctypes.byref(s4_bad), A, A, None, 0, None) == kq.KQ_ERR_SHAPE

@@ -340,6 +340,9 @@ def _small_m_reference(fmt, n, k, m, seed, sw, sx, rows):
     if fmt == "pq2_0":
         deq = oracle.pq2_0_dequant(oracle.pq2_0_quantize(oracle.rotate_rows(w)[1]), rows.size, k)
         X64 = oracle.rotate_rows(Xh)[0]
+    elif fmt == "scale4":
+        deq = oracle.scale4_dequant(oracle.scale4_quantize(w), rows.size, k)
+        X64 = Xh.astype(np.float64)
     else:
         deq = oracle.q8_0_dequant(oracle.q8_0_quantize(w), rows.size, k)
         X64 = Xh.astype(np.float64)
@@ -357,7 +360,8 @@ def _run_tc(kq, W, X, m, splits):
 
 
 @pytest.mark.parametrize("fmt,n,k", [("q8_0", 300, 2080), ("pq2_0", 200, 1152), ("q8_0", 128, 128),
-                                     ("pq2_0", 1, 128), ("q8_0", 1000, 4096), ("pq2_0", 520, 5120)])
+                                     ("pq2_0", 1, 128), ("q8_0", 1000, 4096), ("pq2_0", 520, 5120),
+                                     ("scale4", 300, 2080), ("scale4", 1000, 4096), ("scale4", 1, 32)])
 @pytest.mark.parametrize("m", [1, 5, 16, 33, 64])
 @pytest.mark.parametrize("splits", [0, 3])
 def test_tc_gemm_matches_oracle(kq, wl, fmt, n, k, m, splits):
@@ -375,6 +379,25 @@ def test_tc_gemm_matches_oracle(kq, wl, fmt, n, k, m, splits):
         assert ok, (i, worst)
     # same plan, same bits
     assert np.array_equal(_run_tc(kq, W, X, m, splits), Y)
+
+
+def test_tc_scale4_exact_integer_case_tolerance_zero(kq):
+    """The tcgen05 path on scale4 codes with a 0 in every block (d = 2^-5)
+    and small integer activations: every product and sum is exact, so the
+    output equals the oracle's exactly (the codes enter the tensor core as the
+    exact (q - 8) * 2^(s - 24))."""
+    rng = np.random.default_rng(16)
+    n, k, m = 300, 2080, 16
+    q = rng.integers(0, 16, size=(n, k))
+    q[:, ::32] = 0
+    w = ((q - 8) * 2.0**-5).astype(np.float32)
+    X = rng.integers(-8, 9, size=(m, k)).astype(np.float32)
+    blocks = oracle.scale4_quantize(w)
+    W = kq.QMatrix("scale4", n, k)
+    kq.kq_prepare(W, torch.from_numpy(blocks.reshape(-1)).cuda())
+    Y = _run_tc(kq, W, torch.from_numpy(X.reshape(-1)).cuda(), m, 0)
+    want = ((q - 8) @ X.T.astype(np.int64)).T * 2.0**-5
+    assert np.array_equal(Y.astype(np.float64), want)
 
 
 def test_tc_q8_0_exact_integer_case_tolerance_zero(kq):
