@@ -622,8 +622,10 @@ __device__ __forceinline__ void scale4_tile(const uint8_t* st_codes, const uint1
   const int kh = kq >> 1;
   const uint8_t* base = st_codes + kh * (kRows * 128) + (rg * 64 + g) * 128 + 4 * t;
   const int g16 = g << 4;
-  const bool has_b = g < 2 * M;
-  const uint2* bthread = reinterpret_cast<const uint2*>(xbuf) + (has_b ? g : 0) * 4 + t;
+  // B column n comes from the lanes with g = n.  Lanes with g >= 2M load
+  // column 0 again: their products land only in output columns >= 2M, which
+  // nobody reads, so the load needs no predicate.
+  const uint2* bthread = reinterpret_cast<const uint2*>(xbuf) + (g < 2 * M ? g : 0) * 4 + t;
   const int bt0 = 4 * kq;       // first block of the quarter inside the tile row
   const int b0 = ci * 16 + bt0;  // first block inside the staged slice
   const int tm = t < M ? t : 0;
@@ -648,8 +650,7 @@ __device__ __forceinline__ void scale4_tile(const uint8_t* st_codes, const uint1
       for (int e = 0; e < 4; ++e) c[s4][e] = 0.f;
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      uint2 bf = make_uint2(0u, 0u);
-      if (has_b) bf = bb[j * (2 * M * 4)];
+      const uint2 bf = bb[j * (2 * M * 4)];
 #pragma unroll
       for (int s4 = 0; s4 < 4; ++s4) {
         const uint32_t xa = j ? w[s4][0] >> 8 : w[s4][0], xb = j ? w[s4][1] >> 8 : w[s4][1];
@@ -737,14 +738,17 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
   // t of chunk c is base + ((c ^ g) << 4) for all eight rows.
   const uint8_t* base = st_codes + kh * (kRows * 128) + (rg * 64 + g) * 128 + 4 * t;
   const int g16 = g << 4;
-  const bool has_b = g < 2 * M;
-  const uint2* bthread = reinterpret_cast<const uint2*>(xbuf) + (has_b ? g : 0) * 4 + t;
+  // B column n comes from the lanes with g = n.  Lanes with g >= 2M load
+  // column 0 again: their products land only in output columns >= 2M, which
+  // nobody reads, so the load needs no predicate.
+  const uint2* bthread = reinterpret_cast<const uint2*>(xbuf) + (g < 2 * M ? g : 0) * 4 + t;
   // the two blocks' activation factors and sums
   const int bt0 = 2 * kq;  // first block of the quarter inside the tile row
   const int b0 = ci * 8 + bt0;  // first block inside the staged slice
   const int tm = t < M ? t : 0;  // lanes t >= M hold no activation row
   const float2 F2 = *reinterpret_cast<const float2*>(fx + tm * (xlen_pad / 128) + b0);
   const float2 S2 = *reinterpret_cast<const float2*>(sx + tm * (xlen_pad / 128) + b0);
+  __half2 dpair[4][2];  // the scales of both blocks of rows g, g+8 of each slab, loaded once
 #pragma unroll
   for (int bl = 0; bl < 2; ++bl) {
     if (bt0 + bl >= nblk_valid) break;
@@ -766,8 +770,7 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        uint2 bf = make_uint2(0u, 0u);
-        if (has_b) bf = bb[(q * 4 + j) * (2 * M * 4)];
+        const uint2 bf = bb[(q * 4 + j) * (2 * M * 4)];
         const uint32_t m0 = 0x00030003u << pair_bit(j, 0), m1 = 0x00030003u << pair_bit(j, 1);
 #pragma unroll
         for (int s4 = 0; s4 < 4; ++s4) {
@@ -781,8 +784,12 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
 #pragma unroll
       for (int s4 = 0; s4 < 4; ++s4) {
         const int rA = rg * 64 + s4 * 16 + g;
-        const float dA = __half2float(__ushort_as_half(st_scales[rA * 8 + bt0 + bl]));
-        const float dB = __half2float(__ushort_as_half(st_scales[(rA + 8) * 8 + bt0 + bl]));
+        if (bl == 0) {
+          dpair[s4][0] = *reinterpret_cast<const __half2*>(st_scales + rA * 8 + bt0);
+          dpair[s4][1] = *reinterpret_cast<const __half2*>(st_scales + (rA + 8) * 8 + bt0);
+        }
+        const float dA = bl ? __high2float(dpair[s4][0]) : __low2float(dpair[s4][0]);
+        const float dB = bl ? __high2float(dpair[s4][1]) : __low2float(dpair[s4][1]);
         acc[s4][0] = fmaf(dA, fmaf(F, c[s4][0] + c[s4][1], -S), acc[s4][0]);
         acc[s4][1] = fmaf(dB, fmaf(F, c[s4][2] + c[s4][3], -S), acc[s4][1]);
       }
