@@ -353,23 +353,26 @@ typedef struct {
  *  - Every matrix writes its output to d_y_packed at offset sum_{j<i} n_j
  *    (all of them, also those read by later stages).  d_x_packed holds only
  *    the KQ_SRC_PACKED activations, in list order.
- *  - Stages with fewer 128-/256-row blocks than the GPU has SMs split K;
- *    the partial sums live in the step's workspace, and every reader (the
- *    dependent matrices' activation staging and the final write of y) adds
- *    them in split order, so results stay deterministic.
+ *  - Work is balanced per stage over all SMs: each CTA gets a contiguous
+ *    run of (row block, K chunk) pairs, so a row block may be cut between
+ *    CTAs (row blocks are kept whole where that balances as well).  A cut
+ *    row block's pieces write partial sums into the step's workspace;
+ *    every reader (the dependent matrices' activation staging, and the
+ *    write of y after the last stage) adds them in the same fixed order, so
+ *    results are deterministic and readers see exactly the final y.
  *  - Matrices that share one activation (KQ_SRC_INPUT_OF) share its
  *    staged, transformed copy inside each CTA (the transform memo): a CTA
- *    that goes on to an item of another matrix of the group with the same K
- *    range does not stage or transform the activation again.
+ *    stages the K range it needs from an activation once for all the
+ *    matrices of the group that it works on.
  *  - Errors: KQ_ERR_INVALID_ARG (NULL, unknown kind, `of` not earlier,
  *    non-finite alpha, reserved != 0), KQ_ERR_SHAPE (k mismatch of a link,
  *    decreasing stage, an output read in its own or a later stage),
  *    KQ_ERR_UNSUPPORTED (mixed formats, k above the staging limit), KQ_ERR_CUDA.
  * kq_decode_workspace_bytes gives the step's workspace (stage counters and
- * split partials); kq_decode_step runs it.  Steps of one plan that share a
+ * the partials of cut row blocks); kq_decode_step runs it.  Steps of one plan that share a
  * workspace must be ordered (one stream). */
 int kq_decode_plan_create_linked(const kq_qmat* mats, const kq_link* links, int64_t count, kq_plan** out);
-/* Number of stages of a plan and of matrices whose K is split. */
+/* Number of stages of a plan and of matrices with a row block cut between CTAs. */
 int kq_decode_plan_stages(const kq_plan* plan, int32_t* stages, int32_t* split_matrices);
 
 /* ---- read-only streaming control -------------------------------------------- */

@@ -124,6 +124,7 @@ struct Job {
   int32_t split_k;    // weights per split (multiple of the chunk)
   int32_t had_block;  // PQ2_0: Hadamard block of the rotation (128 or 1024)
   const int8_t* signs;  // PQ2_0: +-1 per position of K applied before the transform, or nullptr
+  int64_t tile_base;    // linked plan: index of the job's first row block in Params::tiles
 };
 
 // Where a decode-plan job's activation comes from (linked plans).
@@ -133,6 +134,43 @@ struct XLink {
   int32_t x_key;      // jobs with equal keys read the same activation (the transform memo)
   float alpha;        // the successor activation is alpha * output
 };
+
+// A linked plan's unit of work: chunks [c0, c1) of one row block of one job.
+// The plan gives every CTA of a stage an equal share of the stage's weight
+// bytes as a contiguous run of (row block, chunk) pairs, so a row block may be
+// cut between CTAs (stream-K).  A cut row block has nseg > 1 segments; each
+// writes its partial sums to slot `slot` of the block's partials.  Nobody
+// waits for them inside the stage: a reader of the block's output adds the
+// partials in slot order, and after the last stage the cut blocks' y is
+// written as the same sums, so readers and y agree bit for bit.
+struct Seg {
+  int32_t j;       // job
+  int32_t rb;      // row block
+  int32_t c0, c1;  // chunk range of the weights
+  int32_t u0, u1;  // chunks of the activation slice staged for it (one per CTA and activation)
+  int32_t nseg;    // segments of this row block (1: the segment writes y itself)
+  int32_t slot;    // this segment's place among them
+  int64_t part;    // floats from ws_base to the row block's partials, [nseg][tile rows] (nseg > 1)
+};
+
+// A row block of a linked plan's job as a reader finds it.
+struct TileOut {
+  int64_t part;  // floats from ws_base to its partials (nseg > 1)
+  int32_t nseg;  // 1: y holds the row block
+  int32_t pad;
+};
+
+// A cut row block: y[y .. y + rows) = its nseg partials added in slot order.
+struct CutOut {
+  int64_t part;
+  int64_t y;  // offset in the packed output
+  int32_t nseg;
+  int32_t rows;
+};
+
+struct Seg;
+struct TileOut;
+struct CutOut;
 
 struct Params {
   CUtensorMap map_codes0;  // single GEMV / GEMM: maps of the one matrix
@@ -145,11 +183,13 @@ struct Params {
   float* y_base;            // packed outputs (decode plan)
   float* ws_base;           // split partials (linked plan)
   int32_t* stage_done;      // linked plan: per stage, the CTAs that have finished it; or nullptr
-  const int32_t* split_jobs;  // linked plan: the jobs whose K is split (their y is written at the end)
-  const int64_t* bounds;    // item ranges of CTA c in stage s: [bounds[s (G+1) + c], bounds[s (G+1) + c + 1])
+  const Seg* segs;          // linked plan: the segments, stage-major, CTA-major
+  const TileOut* tiles;     // linked plan: every row block of every job, as its readers find it
+  const CutOut* cuts;       // linked plan: the cut row blocks, whose y is written after the last stage
+  const int64_t* bounds;    // item (segment) ranges of CTA c in stage s: [bounds[s (G+1) + c], bounds[s (G+1) + c + 1])
   int64_t total_items;
   int32_t nstages;          // stages of the plan (1 without links)
-  int32_t n_split_jobs;
+  int32_t n_cuts;
 };
 
 template <int FMT>
@@ -204,6 +244,17 @@ struct ItemCursor {
     }
     last = item;
   }
+  // Linked plans: makes job jj the current job.
+  __device__ void use(const Params& p, int32_t jj) {
+    if (jj == j) return;
+    j = jj;
+    job = p.jobs[j];
+    job.x = p.x_base + job.x_off;
+    job.y = p.y_base + job.y_off;
+    job.ws = p.ws_base + job.ws_off;
+    mc = p.maps + 2 * j;
+    ms = p.maps + 2 * j + 1;
+  }
   __device__ void seek(const Params& p, int64_t item) {
     if (p.jobs == nullptr) {
       if (j < 0) {
@@ -250,24 +301,58 @@ __device__ __forceinline__ void cta_range(const Params& p, int stage, int64_t& b
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((e + 127) << 23); }  // e in [-126, 127]
 
-// The activation a job reads: a plain vector, or alpha times the sum, in
-// split order, of an earlier job's split partials (a dependent chain).
+// The activation a job reads: a plain vector, or alpha times an earlier
+// job's output (a dependent chain).
 struct XSrc {
-  const float* base;   // the vector, or split 0 of the source's partials
-  int64_t stride;      // floats between consecutive partials
+  const float* base;   // the vector
   int64_t row_stride;  // floats between activation rows (m > 1)
-  int32_t nsum;        // partials added (1: a plain vector)
-  int32_t vec4;        // base and stride allow 16-byte loads
+  int32_t vec4;        // base allows 16-byte loads
   float alpha;
   int32_t had;          // PQ2_0 rotation block (128 or 1024)
   const int8_t* signs;  // PQ2_0 sign per position of K, or nullptr
+  const TileOut* tiles;  // linked source: its row blocks (a cut one is the sum of its partials), or nullptr
+  const float* parts;    // linked source: the partials' base
 };
 
 // x[i..i+3] of activation row m; loads bypass L1 (the source may have been
-// written by other CTAs of this launch).  The partials are added in split
-// order, exactly as the final write of the source's output adds them.
-template <bool IO16 = false>
+// written by other CTAs of this launch).  TR > 0: a linked plan's source
+// output in row blocks of TR rows, where a cut block is read as the sum of
+// its partials in slot order (i % 4 == 0, so the four share a block).
+template <bool IO16 = false, int TR = 0>
 __device__ __forceinline__ float4 load_x4(const XSrc& xs, int m, int64_t i) {
+  if constexpr (TR > 0) {
+    if (xs.tiles) {
+      const TileOut t = xs.tiles[i / TR];
+      if (t.nseg > 1) {
+        // up to eight partials loaded at once, then added in slot order
+        const float* b = xs.parts + t.part + i % TR;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q0 = 0; q0 < t.nseg; q0 += 8) {
+          float4 u[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q0 + q < t.nseg) u[q] = __ldcg(reinterpret_cast<const float4*>(b + (int64_t)(q0 + q) * TR));
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (q0 + q < t.nseg) {
+              if (q0 + q == 0) {
+                v = u[q];
+              } else {
+                v.x += u[q].x;
+                v.y += u[q].y;
+                v.z += u[q].z;
+                v.w += u[q].w;
+              }
+            }
+        }
+        v.x *= xs.alpha;
+        v.y *= xs.alpha;
+        v.z *= xs.alpha;
+        v.w *= xs.alpha;
+        return v;
+      }
+    }
+  }
   if constexpr (IO16) {  // fp16 activations (the fp16 chain): four halves, exact in fp32
     const __half* h = reinterpret_cast<const __half*>(xs.base) + (int64_t)m * xs.row_stride + i;
     const uint2 u = __ldcg(reinterpret_cast<const uint2*>(h));
@@ -277,30 +362,75 @@ __device__ __forceinline__ float4 load_x4(const XSrc& xs, int m, int64_t i) {
   }
   const float* b = xs.base + (int64_t)m * xs.row_stride + i;
   float4 v;
-  if (xs.vec4) {
+  if (xs.vec4)
     v = __ldcg(reinterpret_cast<const float4*>(b));
-    for (int s = 1; s < xs.nsum; ++s) {
-      const float4 u = __ldcg(reinterpret_cast<const float4*>(b + s * xs.stride));
-      v.x += u.x;
-      v.y += u.y;
-      v.z += u.z;
-      v.w += u.w;
-    }
-  } else {
+  else
     v = make_float4(__ldcg(b), __ldcg(b + 1), __ldcg(b + 2), __ldcg(b + 3));
-    for (int s = 1; s < xs.nsum; ++s) {
-      const float* u = b + s * xs.stride;
-      v.x += __ldcg(u);
-      v.y += __ldcg(u + 1);
-      v.z += __ldcg(u + 2);
-      v.w += __ldcg(u + 3);
-    }
-  }
   v.x *= xs.alpha;
   v.y *= xs.alpha;
   v.z *= xs.alpha;
   v.w *= xs.alpha;
   return v;
+}
+
+// A linked plan's activation slice x[kbeg, kbeg + len) (one row), alpha
+// applied, as plain fp32 into dst.  Each thread keeps four float4 fetches in
+// flight; a cut row block of the source is the sum of its partials in slot
+// order, one pass per slot, so the loads of a pass are independent.  The
+// arithmetic equals load_x4's: ((p0 + p1) + ...) * alpha.
+template <int TR>
+__device__ __forceinline__ void gather_slice(const XSrc& xs, int64_t kbeg, int len, float* dst, int tid) {
+  constexpr int kT = 32 * kConsumerWarps;
+  const int n4 = len / 4;
+  for (int i0 = tid; i0 < n4; i0 += 4 * kT) {
+    float4 r[4];
+    const float* pb[4];
+    int ns[4];
+    int nmax = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kT;
+      ns[u] = 0;
+      pb[u] = nullptr;
+      r[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < n4) {
+        const int64_t g = kbeg + 4 * (int64_t)i;
+        const TileOut t = xs.tiles ? xs.tiles[g / TR] : TileOut{0, 1, 0};
+        if (t.nseg > 1) {
+          ns[u] = t.nseg;
+          pb[u] = xs.parts + t.part + g % TR;
+          r[u] = __ldcg(reinterpret_cast<const float4*>(pb[u]));
+        } else {
+          ns[u] = 1;
+          const float* b = xs.base + g;
+          r[u] = xs.vec4 ? __ldcg(reinterpret_cast<const float4*>(b))
+                         : make_float4(__ldcg(b), __ldcg(b + 1), __ldcg(b + 2), __ldcg(b + 3));
+        }
+        nmax = max(nmax, ns[u]);
+      }
+    }
+    for (int q = 1; q < nmax; ++q) {
+      float4 t[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (q < ns[u]) t[u] = __ldcg(reinterpret_cast<const float4*>(pb[u] + (int64_t)q * TR));
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (q < ns[u]) {
+          r[u].x += t[u].x;
+          r[u].y += t[u].y;
+          r[u].z += t[u].z;
+          r[u].w += t[u].w;
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int i = i0 + u * kT;
+      if (i < n4)
+        *reinterpret_cast<float4*>(dst + 4 * i) =
+            make_float4(r[u].x * xs.alpha, r[u].y * xs.alpha, r[u].z * xs.alpha, r[u].w * xs.alpha);
+    }
+  }
 }
 
 // The rotation fields are read from the job table (or the single job), not
@@ -312,21 +442,16 @@ __device__ __forceinline__ XSrc make_xsrc(const Params& p, int32_t j, const Job&
   xs.signs = jm.signs;
   xs.row_stride = job.k;
   xs.alpha = 1.f;
-  xs.nsum = 1;
-  xs.stride = 0;
   xs.base = job.x;
-  if (lk.src_job >= 0) {
+  xs.tiles = nullptr;
+  xs.parts = p.ws_base;
+  if (lk.src_job >= 0) {  // a linked source: its output, cut row blocks as partials
     const Job& src = p.jobs[lk.src_job];
     xs.alpha = lk.alpha;
-    if (src.splits > 1) {
-      xs.base = p.ws_base + src.ws_off;
-      xs.nsum = src.splits;
-      xs.stride = src.n;
-    } else {
-      xs.base = p.y_base + src.y_off;
-    }
+    xs.base = p.y_base + src.y_off;
+    xs.tiles = p.tiles + src.tile_base;
   }
-  xs.vec4 = ((reinterpret_cast<uintptr_t>(xs.base) & 15u) == 0 && (xs.stride & 3) == 0) ? 1 : 0;
+  xs.vec4 = (reinterpret_cast<uintptr_t>(xs.base) & 15u) == 0 ? 1 : 0;
   return xs;
 }
 
@@ -438,16 +563,27 @@ __device__ __forceinline__ void fwht128_lane4(float (&v)[4], int lane) {
 // rounded to fp16 right after the transform (the fp16 chain).
 __device__ __forceinline__ float round_f16(float v) { return __half2float(__float2half_rn(v)); }
 
-template <int FMT, int M, bool IO16 = false>
+template <int FMT, int M, bool IO16 = false, bool LINKED = false>
 __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int xlen_pad, float* xbuf, float* fx,
                                  float* sx, float* scratch, int cw, int lane) {
+  constexpr int kTR = LINKED ? Geo<FMT>::kTileRows : 0;  // a linked source's row blocks
   const int len = (int)(kend - kbeg);
   constexpr int kT = 32 * kConsumerWarps;
+  // Linked PQ2_0 / SCALE4: the slice is first gathered as fp32 into the
+  // staging buffer; each warp below then reads its blocks from there and
+  // rewrites the same bytes with their table entries.
+  constexpr bool kGather = LINKED && FMT != KQ_Q8_0;
+  static_assert(!kGather || M == 1, "linked plans have one activation row");
+  if constexpr (kGather) {
+    gather_slice<Geo<FMT>::kTileRows>(xs, kbeg, len, xbuf, cw * 32 + lane);
+    named_barrier(1, kConsumerWarps * 32);
+  }
+
   if (FMT == KQ_Q8_0) {
     float4* xb4 = reinterpret_cast<float4*>(xbuf);
     for (int m = 0; m < M; ++m) {
       for (int i = cw * 32 + lane; i < len / 4; i += kT)
-        xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] = load_x4<IO16>(xs, m, kbeg + 4 * i);
+        xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] = load_x4<IO16, kTR>(xs, m, kbeg + 4 * i);
     }
   } else if (FMT == KQ_SCALE4) {
     // A warp takes 128 positions (four 32-blocks, eight lanes per block) at a
@@ -460,7 +596,12 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
       const int m = tt / ngrp, q = tt % ngrp;
       // len is a multiple of 32: a block's eight lanes are all inside or all past the slice
       const bool inside = q * 128 + 4 * lane < len;
-      const float4 f = inside ? load_x4<IO16>(xs, m, kbeg + q * 128 + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
+      if constexpr (kGather) {
+        if (inside) f = *reinterpret_cast<const float4*>(xbuf + q * 128 + 4 * lane);
+      } else {
+        if (inside) f = load_x4<IO16, kTR>(xs, m, kbeg + q * 128 + 4 * lane);
+      }
       float amax = fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)));
       float ssum = (f.x + f.y) + (f.z + f.w);
 #pragma unroll
@@ -508,7 +649,11 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
     if (h1024) {
       for (int tt = cw; tt < M * nblk; tt += kConsumerWarps) {
         const int m = tt / nblk, b = tt % nblk;
-        float4 f = load_x4<IO16>(xs, m, kbeg + b * 128 + 4 * lane);
+        float4 f;
+        if constexpr (kGather)
+          f = *reinterpret_cast<const float4*>(xbuf + b * 128 + 4 * lane);
+        else
+          f = load_x4<IO16, kTR>(xs, m, kbeg + b * 128 + 4 * lane);
         float v[4] = {f.x, f.y, f.z, f.w};
         if (xs.signs) {
           const char4 s4 = *reinterpret_cast<const char4*>(xs.signs + kbeg + b * 128 + 4 * lane);
@@ -554,7 +699,11 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
         v[2] = f.z;
         v[3] = f.w;
       } else {
-        const float4 f = load_x4<IO16>(xs, m, kbeg + b * 128 + 4 * lane);
+        float4 f;
+        if constexpr (kGather)
+          f = *reinterpret_cast<const float4*>(xbuf + b * 128 + 4 * lane);
+        else
+          f = load_x4<IO16, kTR>(xs, m, kbeg + b * 128 + 4 * lane);
         v[0] = f.x;
         v[1] = f.y;
         v[2] = f.z;
@@ -860,16 +1009,25 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       int64_t ib, ie;
       cta_range(p, st, ib, ie);
       for (int64_t item = ib; item < ie && ok; ++item) {
-        cur.next(p, item);
+        int rb;
+        int64_t kbeg, kend;
+        if constexpr (LINKED) {
+          const Seg& sg = p.segs[item];
+          cur.use(p, sg.j);
+          rb = sg.rb;
+          kbeg = (int64_t)sg.c0 * F::kChunk;
+          kend = min64(cur.job.k, (int64_t)sg.c1 * F::kChunk);
+        } else {
+          cur.next(p, item);
+          rb = cur.rb;
+          kbeg = (int64_t)cur.split * cur.job.split_k;
+          kend = min64(cur.job.k, kbeg + cur.job.split_k);
+        }
         if (cur.j != last_j) {
           prefetch_tmap(cur.mc);
           prefetch_tmap(cur.ms);
           last_j = cur.j;
         }
-        const Job& job = cur.job;
-        const int split = cur.split, rb = cur.rb;
-        const int64_t kbeg = (int64_t)split * job.split_k;
-        const int64_t kend = min64(job.k, kbeg + job.split_k);
         for (int64_t k0 = kbeg; k0 < kend; k0 += F::kChunk, ++tile) {
           const int s = (int)(tile % kStages);
           const uint32_t par = (uint32_t)((tile / kStages) & 1);
@@ -919,18 +1077,43 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   int64_t ib, ie;
   cta_range(p, st, ib, ie);
   for (int64_t item = ib; item < ie; ++item) {
-    cur.next(p, item);
+    // The unit of work: weights [kbeg, kend) of row block rb against the
+    // staged activation slice [sbeg, send) (an unlinked item stages exactly
+    // its own K range).
+    int rb;
+    int64_t kbeg, kend, sbeg, send;
+    uint32_t range;
+    int32_t nseg = 1, slot = 0;  // linked: the row block's segments (see Seg)
+    int64_t part = 0;
+    if constexpr (LINKED) {
+      const Seg sg = p.segs[item];
+      cur.use(p, sg.j);
+      rb = sg.rb;
+      kbeg = (int64_t)sg.c0 * F::kChunk;
+      kend = min64(cur.job.k, (int64_t)sg.c1 * F::kChunk);
+      sbeg = (int64_t)sg.u0 * F::kChunk;
+      send = min64(cur.job.k, (int64_t)sg.u1 * F::kChunk);
+      range = ((uint32_t)sg.u0 << 16) | (uint32_t)sg.u1;
+      nseg = sg.nseg;
+      slot = sg.slot;
+      part = sg.part;
+    } else {
+      cur.next(p, item);
+      rb = cur.rb;
+      kbeg = (int64_t)cur.split * cur.job.split_k;
+      kend = kbeg + min((int64_t)cur.job.split_k, cur.job.k - kbeg);
+      sbeg = kbeg;
+      send = kend;
+      range = (uint32_t)cur.split;
+    }
     const Job& job = cur.job;
-    const int split = cur.split, rb = cur.rb;
+    const int split = cur.split;
     const int64_t row0 = (int64_t)rb * kTileRows;
     const int rows = min(kTileRows, (int)(job.n - row0));
-    const int64_t kbeg = (int64_t)split * job.split_k;
-    const int64_t kend = kbeg + min((int64_t)job.split_k, job.k - kbeg);
     const int32_t key = LINKED ? p.links[cur.j].x_key : cur.j;
-    const uint32_t range = LINKED ? ((uint32_t)kbeg << 16) | (uint32_t)kend : (uint32_t)split;
     if (key != cached_key || range != cached_range) {
       const XLink lk = LINKED ? p.links[cur.j] : XLink{-1, -1, cur.j, 1.f};
-      xlen_pad = (int)(((kend - kbeg) + F::kChunk - 1) / F::kChunk * F::kChunk);
+      xlen_pad = (int)(((send - sbeg) + F::kChunk - 1) / F::kChunk * F::kChunk);
       if (LINKED && lk.dep_stage > ready) {  // the activation is an output of an earlier stage
         if (cw == 0 && lane == 0 && !*abort_flag && !wait_stage(p, lk.dep_stage)) {
           *abort_flag = 1;
@@ -939,8 +1122,8 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         ready = lk.dep_stage;
       }
       named_barrier(1, kConsumerWarps * 32);  // everyone is done with the previous slice
-      stage_activation<FMT, M, IO16>(make_xsrc(p, cur.j, job, lk), kbeg, kend, xlen_pad, xbuf, fx, sx, scratch, cw,
-                                     lane);
+      stage_activation<FMT, M, IO16, LINKED>(make_xsrc(p, cur.j, job, lk), sbeg, send, xlen_pad, xbuf, fx, sx,
+                                             scratch, cw, lane);
       named_barrier(1, kConsumerWarps * 32);
       cached_key = key;
       cached_range = range;
@@ -954,16 +1137,17 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 
     // After an abort every warp keeps walking the item list (so the named
     // barriers stay matched) but waits for and computes nothing.
-    const int klen = (int)(kend - kbeg);
-    const int nch = (klen + F::kChunk - 1) / F::kChunk;
-    for (int ci = 0; ci < nch; ++ci) {
+    const int klen = (int)(send - sbeg);  // chunk ci of the loop is chunk ci of the staged slice
+    const int ci0 = (int)((kbeg - sbeg) / F::kChunk);
+    const int nch = (int)((kend - sbeg + F::kChunk - 1) / F::kChunk);
+    for (int ci = ci0; ci < nch; ++ci) {
       const int s = ring;
       const uint32_t par = ring_par;
       if (++ring == kStages) {
         ring = 0;
         ring_par ^= 1u;
       }
-      const int64_t k0 = kbeg + (int64_t)ci * F::kChunk;
+      const int64_t k0 = sbeg + (int64_t)ci * F::kChunk;
       if (*abort_flag) continue;
       if (!mbar_wait_bounded(&full[s], par)) {
         *abort_flag = 1;
@@ -974,7 +1158,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       const uint16_t* st_scales = reinterpret_cast<const uint16_t*>(st + kTileCodeBytes);
       if constexpr (FMT == KQ_Q8_0) {
         // lanes whose granule lies past k have nothing to do in this chunk
-        if (k0 + (int64_t)(lane + 1) * F::kGran <= kend)
+        if (k0 + (int64_t)(lane + 1) * F::kGran <= send)
           q8_0_tile<M>(st, st_scales, rows, ci, xlen_pad, xbuf, cw, lane, acc8);
       } else if constexpr (FMT == KQ_SCALE4) {
         const int nblk_valid = min(16, (klen - ci * F::kChunk) / 32);
@@ -987,109 +1171,116 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
       if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    if constexpr (FMT == KQ_Q8_0) {
-      if (*abort_flag) continue;
-      // fixed-order lane reduction, then one write per (row, m)
+    do {  // the outputs (`break` skips them after an abort)
+      if constexpr (FMT == KQ_Q8_0) {
+        if (*abort_flag) break;
+        // fixed-order lane reduction, then one write per (row, m)
 #pragma unroll
-      for (int r = 0; r < kRowsPerWarp; ++r) {
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-          float v = acc8[r][m];
-#pragma unroll
-          for (int mk = 16; mk; mk >>= 1) v += __shfl_xor_sync(0xffffffffu, v, mk);
-          acc8[r][m] = v;
-        }
-      }
-      if (lane < kRowsPerWarp) {
-        const int row = cw * kRowsPerWarp + lane;
-        if (row < rows) {
-          float v[M];
+        for (int r = 0; r < kRowsPerWarp; ++r) {
 #pragma unroll
           for (int m = 0; m < M; ++m) {
-            v[m] = acc8[0][m];
+            float v = acc8[r][m];
 #pragma unroll
-            for (int r = 1; r < kRowsPerWarp; ++r)
-              if (lane == r) v[m] = acc8[r][m];
+            for (int mk = 16; mk; mk >>= 1) v += __shfl_xor_sync(0xffffffffu, v, mk);
+            acc8[r][m] = v;
           }
+        }
+        if (lane < kRowsPerWarp) {
+          const int row = cw * kRowsPerWarp + lane;
+          if (row < rows) {
+            float v[M];
 #pragma unroll
-          for (int m = 0; m < M; ++m) {
-            if (job.splits == 1) {
-              if constexpr (IO16)
-                reinterpret_cast<__half*>(job.y)[(int64_t)m * job.ldy + row0 + row] = __float2half_rn(v[m]);
-              else
-                job.y[(int64_t)m * job.ldy + row0 + row] = v[m];
-            } else {
-              job.ws[((int64_t)split * M + m) * job.n + row0 + row] = v[m];
+            for (int m = 0; m < M; ++m) {
+              v[m] = acc8[0][m];
+#pragma unroll
+              for (int r = 1; r < kRowsPerWarp; ++r)
+                if (lane == r) v[m] = acc8[r][m];
+            }
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+              if (LINKED && nseg > 1) {
+                p.ws_base[part + (int64_t)slot * kTileRows + row] = v[m];
+              } else if (job.splits == 1) {
+                if constexpr (IO16)
+                  reinterpret_cast<__half*>(job.y)[(int64_t)m * job.ldy + row0 + row] = __float2half_rn(v[m]);
+                else
+                  job.y[(int64_t)m * job.ldy + row0 + row] = v[m];
+              } else {
+                job.ws[((int64_t)split * M + m) * job.n + row0 + row] = v[m];
+              }
+            }
+          }
+        }
+      } else {
+        // warps cw, cw + 4, cw + 8, cw + 12 hold the four K quarters of the
+        // same 64 rows: the last three hand their partials over through the
+        // row group's buffer and go on (they only wait, before writing, until
+        // the previous handoff has been read); the first adds them in quarter
+        // order and writes the outputs
+        const int sp = cw & 3, kq = cw >> 2;
+        float* cb = combine + sp * (3 * 32 * 8);
+        const uint32_t cpar = combines & 1u;
+        ++combines;
+        if (*abort_flag) break;
+        if (kq > 0) {
+          if (!mbar_wait_bounded(&cfree[sp], cpar ^ 1u)) {
+            *abort_flag = 1;
+            stream_flag(KQ_ERR_TIMEOUT);
+            break;
+          }
+          float4* dst = reinterpret_cast<float4*>(cb + ((kq - 1) * 32 + lane) * 8);
+          dst[0] = make_float4(acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]);
+          dst[1] = make_float4(acc4[2][0], acc4[2][1], acc4[3][0], acc4[3][1]);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&cfull[sp]);
+        } else {
+          if (!mbar_wait_bounded(&cfull[sp], cpar)) {
+            *abort_flag = 1;
+            stream_flag(KQ_ERR_TIMEOUT);
+            break;
+          }
+          const int g = lane >> 2, t = lane & 3;
+          // this lane's output row of activation t (lanes t >= M write nothing)
+          float* yout = (LINKED && nseg > 1)
+                            ? p.ws_base + part + (int64_t)slot * kTileRows
+                            : (job.splits == 1 ? job.y + (int64_t)t * job.ldy : job.ws + ((int64_t)split * M + t) * job.n) +
+                                  row0;
+          const int rmax = t < M ? rows - (sp * 64 + g) : 0;  // rows of this lane's set that exist
+          float y8[8] = {acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1],
+                         acc4[2][0], acc4[2][1], acc4[3][0], acc4[3][1]};
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const float4* src = reinterpret_cast<const float4*>(cb + (q * 32 + lane) * 8);
+            const float4 v0 = src[0], v1 = src[1];
+            y8[0] += v0.x;
+            y8[1] += v0.y;
+            y8[2] += v0.z;
+            y8[3] += v0.w;
+            y8[4] += v1.x;
+            y8[5] += v1.y;
+            y8[6] += v1.z;
+            y8[7] += v1.w;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&cfree[sp]);
+          if (IO16 && job.splits == 1) {  // the final output, in fp16
+            __half* yh = reinterpret_cast<__half*>(job.y) + (int64_t)t * job.ldy + row0 + sp * 64 + g;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int dr = (e >> 1) * 16 + (e & 1) * 8;
+              if (dr < rmax) yh[dr] = __float2half_rn(y8[e]);
+            }
+          } else {
+            float* yl = yout + sp * 64 + g;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const int dr = (e >> 1) * 16 + (e & 1) * 8;  // slab e/2, row g or g+8
+              if (dr < rmax) yl[dr] = y8[e];
             }
           }
         }
       }
-    } else {
-      // warps cw, cw + 4, cw + 8, cw + 12 hold the four K quarters of the
-      // same 64 rows: the last three hand their partials over through the
-      // row group's buffer and go on (they only wait, before writing, until
-      // the previous handoff has been read); the first adds them in quarter
-      // order and writes the outputs
-      const int sp = cw & 3, kq = cw >> 2;
-      float* cb = combine + sp * (3 * 32 * 8);
-      const uint32_t cpar = combines & 1u;
-      ++combines;
-      if (*abort_flag) continue;
-      if (kq > 0) {
-        if (!mbar_wait_bounded(&cfree[sp], cpar ^ 1u)) {
-          *abort_flag = 1;
-          stream_flag(KQ_ERR_TIMEOUT);
-          continue;
-        }
-        float4* dst = reinterpret_cast<float4*>(cb + ((kq - 1) * 32 + lane) * 8);
-        dst[0] = make_float4(acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1]);
-        dst[1] = make_float4(acc4[2][0], acc4[2][1], acc4[3][0], acc4[3][1]);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&cfull[sp]);
-      } else {
-        if (!mbar_wait_bounded(&cfull[sp], cpar)) {
-          *abort_flag = 1;
-          stream_flag(KQ_ERR_TIMEOUT);
-          continue;
-        }
-        const int g = lane >> 2, t = lane & 3;
-        // this lane's output row of activation t (lanes t >= M write nothing)
-        float* yout = (job.splits == 1 ? job.y + (int64_t)t * job.ldy : job.ws + ((int64_t)split * M + t) * job.n) + row0;
-        const int rmax = t < M ? rows - (sp * 64 + g) : 0;  // rows of this lane's set that exist
-        float y8[8] = {acc4[0][0], acc4[0][1], acc4[1][0], acc4[1][1],
-                       acc4[2][0], acc4[2][1], acc4[3][0], acc4[3][1]};
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          const float4* src = reinterpret_cast<const float4*>(cb + (q * 32 + lane) * 8);
-          const float4 v0 = src[0], v1 = src[1];
-          y8[0] += v0.x;
-          y8[1] += v0.y;
-          y8[2] += v0.z;
-          y8[3] += v0.w;
-          y8[4] += v1.x;
-          y8[5] += v1.y;
-          y8[6] += v1.z;
-          y8[7] += v1.w;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&cfree[sp]);
-        if (IO16 && job.splits == 1) {  // the final output, in fp16
-          __half* yh = reinterpret_cast<__half*>(job.y) + (int64_t)t * job.ldy + row0 + sp * 64 + g;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int dr = (e >> 1) * 16 + (e & 1) * 8;
-            if (dr < rmax) yh[dr] = __float2half_rn(y8[e]);
-          }
-        } else {
-          float* yl = yout + sp * 64 + g;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int dr = (e >> 1) * 16 + (e & 1) * 8;  // slab e/2, row g or g+8
-            if (dr < rmax) yl[dr] = y8[e];
-          }
-        }
-      }
-    }
+    } while (0);
   }
   // linked plan: this CTA has written every output of its items of stage st
   if (LINKED) {
@@ -1101,25 +1292,55 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   }
   }
 
-  // Linked plan: once every stage has finished everywhere, the outputs of the
-  // split jobs are their partials added in split order (the order every
-  // dependent activation used), each CTA a slice of the rows of every job.
-  if (LINKED && p.n_split_jobs > 0) {
-    if (cw == 0 && lane == 0 && !*abort_flag && !wait_stage(p, nst - 1)) {
-      *abort_flag = 1;
-      stream_flag(KQ_ERR_TIMEOUT);
-    }
-    named_barrier(1, kConsumerWarps * 32);
-    if (*abort_flag) return;
-    for (int q = 0; q < p.n_split_jobs; ++q) {
-      const Job& J = p.jobs[p.split_jobs[q]];
-      const int64_t r0 = J.n * blockIdx.x / gridDim.x, r1 = J.n * (blockIdx.x + 1) / gridDim.x;
-      const float* w = p.ws_base + J.ws_off;
-      float* y = p.y_base + J.y_off;
-      for (int64_t r = r0 + cw * 32 + lane; r < r1; r += kConsumerWarps * 32) {
-        float v = __ldcg(w + r);
-        for (int sp = 1; sp < J.splits; ++sp) v += __ldcg(w + (int64_t)sp * J.n + r);
-        y[r] = v;
+  // Linked plan: once the last stage has finished everywhere, the cut row
+  // blocks' outputs are their partials added in slot order (the sums their
+  // readers used), each CTA every gridDim.x-th block.
+  if constexpr (LINKED) {
+    if (p.n_cuts > 0) {
+      if (cw == 0 && lane == 0 && !*abort_flag && !wait_stage(p, nst - 1)) {
+        *abort_flag = 1;
+        stream_flag(KQ_ERR_TIMEOUT);
+      }
+      named_barrier(1, kConsumerWarps * 32);
+      if (*abort_flag) return;
+      // one warp per cut block; a lane sums rows 4l .. 4l + 3 (and 4l + 128 ..)
+      for (int c = blockIdx.x + gridDim.x * cw; c < p.n_cuts; c += gridDim.x * kConsumerWarps) {
+        const CutOut cu = p.cuts[c];
+        const float* pb = p.ws_base + cu.part;
+        constexpr int kQ = kTileRows / 128;  // float4 per lane
+        float4 v[kQ];
+        for (int q0 = 0; q0 < cu.nseg; q0 += 4) {
+          float4 u[4][kQ];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int h = 0; h < kQ; ++h)
+              if (q0 + q < cu.nseg)
+                u[q][h] = __ldcg(reinterpret_cast<const float4*>(pb + (int64_t)(q0 + q) * kTileRows + 128 * h) + lane);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int h = 0; h < kQ; ++h)
+              if (q0 + q < cu.nseg) {
+                if (q0 + q == 0) {
+                  v[h] = u[q][h];
+                } else {
+                  v[h].x += u[q][h].x;
+                  v[h].y += u[q][h].y;
+                  v[h].z += u[q][h].z;
+                  v[h].w += u[q][h].w;
+                }
+              }
+        }
+        float* y = p.y_base + cu.y;
+#pragma unroll
+        for (int h = 0; h < kQ; ++h) {
+          const int r = 128 * h + 4 * lane;
+          const float e[4] = {v[h].x, v[h].y, v[h].z, v[h].w};
+#pragma unroll
+          for (int d = 0; d < 4; ++d)
+            if (r + d < cu.rows) y[r + d] = e[d];
+        }
       }
     }
   }
@@ -1419,13 +1640,16 @@ struct kq_plan {
   int32_t n_split = 0;
   bool linked = false;
   int64_t total_items = 0;
+  int32_t n_cuts = 0;        // linked plan: row blocks cut between CTAs
   size_t counter_bytes = 0;  // linked plan: stage counters at the start of the workspace ...
-  size_t ws_bytes = 0;       // ... then the split partials
+  size_t ws_bytes = 0;       // ... then the partials of the cut row blocks
   kq::Job* d_jobs = nullptr;
   CUtensorMap* d_maps = nullptr;
   int64_t* d_bounds = nullptr;
   kq::XLink* d_links = nullptr;
-  int32_t* d_split_jobs = nullptr;
+  kq::Seg* d_segs = nullptr;
+  kq::TileOut* d_tiles = nullptr;
+  kq::CutOut* d_cuts = nullptr;
 };
 
 using namespace kq;
@@ -1436,7 +1660,9 @@ static void destroy_plan(kq_plan* p) {
   cudaFree(p->d_maps);
   cudaFree(p->d_bounds);
   cudaFree(p->d_links);
-  cudaFree(p->d_split_jobs);
+  cudaFree(p->d_segs);
+  cudaFree(p->d_tiles);
+  cudaFree(p->d_cuts);
   delete p;
 }
 
@@ -1471,8 +1697,193 @@ static int check_links(const kq_qmat* mats, const kq_link* links, int64_t count)
   return KQ_OK;
 }
 
+// Linked plan: the segments of every stage (see Seg).  Each CTA gets a
+// contiguous run of (row block, chunk) pairs, in list order, in one of two
+// ways, whichever loads the busiest CTA less (the second on a tie within 2%):
+//  - equal shares of the stage's weight bytes: a chunk belongs to the CTA
+//    whose share holds the chunk's middle byte (stream-K);
+//  - a capacity L, as small as fits the grid: a row block that fits whole
+//    into the current CTA's rest goes there, one that fits a fresh CTA opens
+//    the next one, and only a row block larger than L is cut, filling each
+//    CTA to L.
+// The second cuts fewer row blocks (none when every CTA can take whole ones).
+// A CTA's run becomes segments, one per row block it touches; a row block cut
+// between CTAs gets partial slots in CTA order.
+// The chunk ranges a CTA needs from one activation are merged where they
+// overlap or touch, and each segment records the merged range that holds it,
+// which the CTA stages once (two pieces of different row blocks, say chunks
+// [14, 17) and [0, 2), stay two small slices rather than the whole K).  Fills
+// each job's row blocks (tiles, from jobs[j].tile_base) and the list of cut
+// row blocks.
+static void build_segments(std::vector<Job>& jobs, const std::vector<XLink>& xl, const kq_link* links,
+                           int64_t count, int fmt, int G, int32_t nstages, std::vector<Seg>& segs,
+                           std::vector<int64_t>& bounds, std::vector<TileOut>& tiles, std::vector<CutOut>& cuts,
+                           int64_t& part_floats, std::vector<char>& job_cut) {
+  const int64_t unit = chunk_of(fmt);
+  const int TR = tile_rows(fmt);
+  bounds.assign((size_t)nstages * (G + 1), 0);
+  part_floats = 0;
+  job_cut.assign((size_t)count, 0);
+  tiles.clear();
+  for (int64_t i = 0; i < count; ++i) {
+    jobs[(size_t)i].tile_base = (int64_t)tiles.size();
+    tiles.resize(tiles.size() + (size_t)jobs[(size_t)i].row_blocks, TileOut{0, 1, 0});
+  }
+  auto chunk_bytes = [&](const Job& J, int64_t rb, int64_t c) {
+    const int64_t rows = std::min<int64_t>(TR, J.n - rb * TR);
+    const int64_t kk = std::min<int64_t>(unit, J.k - c * unit);
+    return (double)rows * (double)(code_row_bytes(fmt, kk) + 2 * (kk / block_of(fmt)));
+  };
+  int64_t i0 = 0;
+  for (int32_t st = 0; st < nstages; ++st) {
+    int64_t i1 = i0;
+    while (i1 < count && links[i1].stage == st) ++i1;
+    double total = 0;
+    for (int64_t i = i0; i < i1; ++i) {
+      const Job& J = jobs[(size_t)i];
+      const int64_t nch = (J.k + unit - 1) / unit;
+      for (int64_t rb = 0; rb < J.row_blocks; ++rb)
+        for (int64_t c = 0; c < nch; ++c) total += chunk_bytes(J, rb, c);
+    }
+    // owners of the stage's chunks in (job, row block, chunk) order
+    std::vector<double> cb;     // chunk bytes
+    std::vector<size_t> tile0;  // first chunk of each row block, and the end
+    for (int64_t i = i0; i < i1; ++i) {
+      const Job& J = jobs[(size_t)i];
+      const int64_t nch = (J.k + unit - 1) / unit;
+      for (int64_t rb = 0; rb < J.row_blocks; ++rb) {
+        tile0.push_back(cb.size());
+        for (int64_t c = 0; c < nch; ++c) cb.push_back(chunk_bytes(J, rb, c));
+      }
+    }
+    tile0.push_back(cb.size());
+    std::vector<int> own_sk(cb.size()), own_pk(cb.size());
+    double cum = 0;
+    for (size_t g = 0; g < cb.size(); ++g) {
+      own_sk[g] = std::min(G - 1, (int)((cum + 0.5 * cb[g]) * G / total));
+      cum += cb[g];
+    }
+    // the packing with capacity L; returns the CTAs it needs
+    auto pack = [&](double L, std::vector<int>& own) {
+      int cta = 0;
+      double used = 0;
+      for (size_t t = 0; t + 1 < tile0.size(); ++t) {
+        double bt = 0;
+        for (size_t g = tile0[t]; g < tile0[t + 1]; ++g) bt += cb[g];
+        if (used + bt > L && bt <= L && used > 0) {  // starts a fresh CTA whole
+          ++cta;
+          used = 0;
+        }
+        for (size_t g = tile0[t]; g < tile0[t + 1]; ++g) {
+          if (used + cb[g] > L && used > 0) {
+            ++cta;
+            used = 0;
+          }
+          own[g] = cta;
+          used += cb[g];
+        }
+      }
+      return cb.empty() ? 0 : cta + 1;
+    };
+    auto busiest = [&](const std::vector<int>& own) {
+      std::vector<double> load((size_t)G, 0.0);
+      for (size_t g = 0; g < cb.size(); ++g) load[(size_t)std::min(own[g], G - 1)] += cb[g];
+      return cb.empty() ? 0.0 : *std::max_element(load.begin(), load.end());
+    };
+    double lo = total / G, hi = 0;
+    for (size_t g = 0; g < cb.size(); ++g) hi = std::max(hi, cb[g]);
+    hi = std::max(2.0 * lo, lo + 2 * hi);
+    if (!cb.empty() && pack(hi, own_pk) <= G) {
+      for (int it = 0; it < 50; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        if (pack(mid, own_pk) <= G) hi = mid; else lo = mid;
+      }
+    }
+    const bool packed = !cb.empty() && pack(hi, own_pk) <= G && busiest(own_pk) <= 1.02 * busiest(own_sk);
+    const std::vector<int>& own = packed ? own_pk : own_sk;
+    // the stage's (job, row block, chunk) runs per owning CTA
+    std::vector<Seg> raw;
+    std::vector<int> owner;
+    size_t gi = 0;
+    for (int64_t i = i0; i < i1; ++i) {
+      const Job& J = jobs[(size_t)i];
+      const int64_t nch = (J.k + unit - 1) / unit;
+      for (int64_t rb = 0; rb < J.row_blocks; ++rb)
+        for (int64_t c = 0; c < nch; ++c) {
+          const int cta = own[gi++];
+          if (!raw.empty() && owner.back() == cta && raw.back().j == (int32_t)i && raw.back().rb == (int32_t)rb) {
+            raw.back().c1 = (int32_t)c + 1;
+          } else {
+            Seg g{};
+            g.j = (int32_t)i;
+            g.rb = (int32_t)rb;
+            g.c0 = (int32_t)c;
+            g.c1 = (int32_t)c + 1;
+            raw.push_back(g);
+            owner.push_back(cta);
+          }
+        }
+    }
+    // cut row blocks (their pieces are adjacent in raw): slots and partials
+    for (size_t a = 0; a < raw.size();) {
+      size_t b = a + 1;
+      while (b < raw.size() && raw[b].j == raw[a].j && raw[b].rb == raw[a].rb) ++b;
+      const int32_t nseg = (int32_t)(b - a);
+      int64_t part = 0;
+      if (nseg > 1) {
+        const Job& J = jobs[(size_t)raw[a].j];
+        part = part_floats;
+        part_floats += (int64_t)nseg * TR;
+        job_cut[(size_t)raw[a].j] = 1;
+        tiles[(size_t)(J.tile_base + raw[a].rb)] = TileOut{part, nseg, 0};
+        cuts.push_back(CutOut{part, J.y_off + (int64_t)raw[a].rb * TR, nseg,
+                              (int32_t)std::min<int64_t>(TR, J.n - (int64_t)raw[a].rb * TR)});
+      }
+      for (size_t q = a; q < b; ++q) {
+        raw[q].nseg = nseg;
+        raw[q].slot = (int32_t)(q - a);
+        raw[q].part = part;
+      }
+      a = b;
+    }
+    // per CTA, in order: the staged union of each activation's chunk ranges
+    int64_t* bs = bounds.data() + (size_t)st * (G + 1);
+    size_t a = 0;
+    for (int c = 0; c < G; ++c) {
+      bs[c] = (int64_t)segs.size();
+      size_t b = a;
+      while (b < raw.size() && owner[b] == c) ++b;
+      for (size_t q = a; q < b; ++q) {
+        const int32_t key = xl[(size_t)raw[q].j].x_key;
+        std::vector<std::pair<int32_t, int32_t>> rs;
+        for (size_t r = a; r < b; ++r)
+          if (xl[(size_t)raw[r].j].x_key == key) rs.emplace_back(raw[r].c0, raw[r].c1);
+        std::sort(rs.begin(), rs.end());
+        int32_t u0 = 0, u1 = 0;
+        for (size_t r = 0; r < rs.size();) {  // the merged interval holding this segment
+          int32_t m0 = rs[r].first, m1 = rs[r].second;
+          size_t e = r + 1;
+          while (e < rs.size() && rs[e].first <= m1) m1 = std::max(m1, rs[e++].second);
+          if (raw[q].c0 >= m0 && raw[q].c1 <= m1) {
+            u0 = m0;
+            u1 = m1;
+          }
+          r = e;
+        }
+        Seg g = raw[q];
+        g.u0 = u0;
+        g.u1 = u1;
+        segs.push_back(g);
+      }
+      a = b;
+    }
+    bs[G] = (int64_t)segs.size();
+    i0 = i1;
+  }
+}
+
 // Builds a plan.  links == nullptr: every matrix reads its own packed input,
-// one stage, no splits (kq_decode_plan_create).
+// one stage, items of whole row blocks (kq_decode_plan_create).
 static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count, kq_plan** out) {
   if (!mats || !out) return fail(KQ_ERR_INVALID_ARG, "NULL pointer");
   if (count < 1) return fail(KQ_ERR_SHAPE, "count = %lld", (long long)count);
@@ -1491,30 +1902,15 @@ static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count,
   int sms = 0;
   if (int s = device_sms(&sms)) return s;
   const int32_t nstages = links ? links[count - 1].stage + 1 : 1;
-  // row blocks of every stage: a stage with fewer row blocks than SMs splits K
-  std::vector<int64_t> stage_rb((size_t)nstages, 0);
-  for (int64_t i = 0; i < count; ++i)
-    stage_rb[(size_t)(links ? links[i].stage : 0)] += (mats[i].n + tile_rows(fmt) - 1) / tile_rows(fmt);
   std::vector<Job> jobs((size_t)count);
   std::vector<CUtensorMap> maps((size_t)(2 * count));
   std::vector<XLink> xl((size_t)count);
-  std::vector<int32_t> split_jobs;
   std::vector<double> item_bytes;
-  std::vector<int64_t> stage_first((size_t)nstages + 1, 0);  // first item of each stage
-  int64_t items = 0, xf = 0, yf = 0, wb = 0, wsf = 0;
-  const int64_t unit = chunk_of(fmt);
+  int64_t items = 0, xf = 0, yf = 0, wb = 0;
   for (int64_t i = 0; i < count; ++i) {
     const kq_qmat& W = mats[i];
     if (int s = make_maps(&W, &maps[(size_t)(2 * i)], &maps[(size_t)(2 * i + 1)])) return s;
-    const int32_t stg = links ? links[i].stage : 0;
     const int64_t row_blocks = (W.n + tile_rows(fmt) - 1) / tile_rows(fmt);
-    int64_t splits = 1, split_k = W.k;
-    if (links && stage_rb[(size_t)stg] < sms) {
-      const int64_t chunks = (W.k + unit - 1) / unit;
-      const int64_t want = std::min<int64_t>(chunks, (sms + stage_rb[(size_t)stg] - 1) / stage_rb[(size_t)stg]);
-      split_k = round_up((W.k + want - 1) / want, unit);
-      splits = (W.k + split_k - 1) / split_k;
-    }
     Job& j = jobs[(size_t)i];
     j = Job{};
     j.y_off = yf;
@@ -1522,17 +1918,12 @@ static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count,
     j.k = W.k;
     j.ldy = W.n;
     j.item_begin = items;
-    j.items = row_blocks * splits;
+    j.items = row_blocks;
     j.row_blocks = (int32_t)row_blocks;
-    j.splits = (int32_t)splits;
-    j.split_k = (int32_t)split_k;
+    j.splits = 1;
+    j.split_k = (int32_t)W.k;
     j.had_block = W.had_block;
     j.signs = W.signs;
-    if (splits > 1) {
-      j.ws_off = wsf;
-      wsf += round_up(splits * W.n, 4);
-      split_jobs.push_back((int32_t)i);
-    }
     // activation source; INPUT_OF inherits its source's, so a group shares one key
     XLink& L = xl[(size_t)i];
     const int src = links ? links[i].src : KQ_SRC_PACKED;
@@ -1547,50 +1938,50 @@ static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count,
       j.x_off = 0;
       L = XLink{(int32_t)links[i].of, links[(size_t)links[i].of].stage, (int32_t)i, links[i].alpha};
     }
-    // items are split-major within a job (ItemCursor); bytes of each for the balance
-    const double rowbytes = (double)code_row_bytes(fmt, split_k) + 2.0 * (double)(split_k / block_of(fmt));
-    for (int64_t sp = 0; sp < splits; ++sp)
-      for (int64_t r = 0; r < row_blocks; ++r) {
-        const double kfrac = (double)std::min<int64_t>(split_k, W.k - sp * split_k) / (double)split_k;
-        item_bytes.push_back(rowbytes * kfrac *
-                             (double)std::min<int64_t>(tile_rows(fmt), W.n - r * tile_rows(fmt)));
-      }
-    items += j.items;
-    stage_first[(size_t)stg + 1] = items;
+    const double rowbytes = (double)code_row_bytes(fmt, W.k) + 2.0 * (double)(W.k / block_of(fmt));
+    for (int64_t r = 0; r < row_blocks; ++r)
+      item_bytes.push_back(rowbytes * (double)std::min<int64_t>(tile_rows(fmt), W.n - r * tile_rows(fmt)));
+    items += row_blocks;
     yf += W.n;
     wb += kq_codes_bytes(fmt, W.n, W.k) + W.n * (W.k / block_of(fmt)) * 2;
   }
-  for (int32_t s = 1; s <= nstages; ++s) stage_first[(size_t)s] = std::max(stage_first[(size_t)s], stage_first[(size_t)s - 1]);
   kq_plan* p = new kq_plan();
   p->fmt = fmt;
   p->count = count;
   p->x_floats = xf;
   p->y_floats = yf;
   p->weight_bytes = wb;
-  p->total_items = items;
   p->nstages = nstages;
   p->linked = links != nullptr;
-  p->n_split = (int32_t)split_jobs.size();
-  p->grid = (int)std::min<int64_t>(items, sms);
+  std::vector<int64_t> bounds;
+  std::vector<Seg> segs;
+  std::vector<TileOut> tiles;
+  std::vector<CutOut> cuts;
   if (p->linked) {
+    const int G = sms;
+    int64_t part_floats = 0;
+    std::vector<char> job_cut;
+    build_segments(jobs, xl, links, count, fmt, G, nstages, segs, bounds, tiles, cuts, part_floats, job_cut);
+    p->grid = G;
+    p->total_items = (int64_t)segs.size();
+    p->n_cuts = (int32_t)cuts.size();
+    p->n_split = (int32_t)std::count(job_cut.begin(), job_cut.end(), 1);
     p->counter_bytes = (size_t)round_up((int64_t)nstages * 4, 256);
-    p->ws_bytes = p->counter_bytes + (size_t)wsf * sizeof(float);
-  }
-  // byte-balanced contiguous item ranges, per stage and CTA
-  const int G = p->grid;
-  std::vector<int64_t> bounds((size_t)nstages * (G + 1));
-  for (int32_t s = 0; s < nstages; ++s) {
-    const int64_t b0 = stage_first[(size_t)s], b1 = stage_first[(size_t)s + 1];
-    int64_t* bs = bounds.data() + (size_t)s * (G + 1);
+    p->ws_bytes = p->counter_bytes + (size_t)part_floats * sizeof(float);
+  } else {
+    // byte-balanced contiguous item ranges, one per CTA
+    p->total_items = items;
+    p->grid = (int)std::min<int64_t>(items, sms);
+    const int G = p->grid;
+    bounds.assign((size_t)(G + 1), items);
+    bounds[0] = 0;
     double total = 0;
-    for (int64_t it = b0; it < b1; ++it) total += item_bytes[(size_t)it];
-    for (int c = 0; c <= G; ++c) bs[c] = b1;
-    bs[0] = b0;
+    for (double b : item_bytes) total += b;
     double accum = 0;
     int c = 1;
-    for (int64_t it = b0; it < b1 && c < G; ++it) {
+    for (int64_t it = 0; it < items && c < G; ++it) {
       accum += item_bytes[(size_t)it];
-      while (c < G && accum >= total * c / G) bs[c++] = it + 1;
+      while (c < G && accum >= total * c / G) bounds[(size_t)c++] = it + 1;
     }
   }
   cudaError_t e = cudaMalloc(&p->d_jobs, sizeof(Job) * (size_t)count);
@@ -1604,11 +1995,16 @@ static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count,
   if (p->linked) {
     if (e == cudaSuccess) e = cudaMalloc(&p->d_links, sizeof(XLink) * (size_t)count);
     if (e == cudaSuccess) e = cudaMemcpy(p->d_links, xl.data(), sizeof(XLink) * (size_t)count, cudaMemcpyHostToDevice);
-    if (e == cudaSuccess && !split_jobs.empty()) {
-      e = cudaMalloc(&p->d_split_jobs, sizeof(int32_t) * split_jobs.size());
-      if (e == cudaSuccess)
-        e = cudaMemcpy(p->d_split_jobs, split_jobs.data(), sizeof(int32_t) * split_jobs.size(),
-                       cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !segs.empty()) {
+      e = cudaMalloc(&p->d_segs, sizeof(Seg) * segs.size());
+      if (e == cudaSuccess) e = cudaMemcpy(p->d_segs, segs.data(), sizeof(Seg) * segs.size(), cudaMemcpyHostToDevice);
+    }
+    if (e == cudaSuccess) e = cudaMalloc(&p->d_tiles, sizeof(TileOut) * tiles.size());
+    if (e == cudaSuccess)
+      e = cudaMemcpy(p->d_tiles, tiles.data(), sizeof(TileOut) * tiles.size(), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess && !cuts.empty()) {
+      e = cudaMalloc(&p->d_cuts, sizeof(CutOut) * cuts.size());
+      if (e == cudaSuccess) e = cudaMemcpy(p->d_cuts, cuts.data(), sizeof(CutOut) * cuts.size(), cudaMemcpyHostToDevice);
     }
   }
   if (e != cudaSuccess) {
@@ -1764,8 +2160,10 @@ int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, vo
   if (plan->linked) {
     p.stage_done = static_cast<int32_t*>(d_ws);
     p.ws_base = reinterpret_cast<float*>(static_cast<uint8_t*>(d_ws) + plan->counter_bytes);
-    p.split_jobs = plan->d_split_jobs;
-    p.n_split_jobs = plan->n_split;
+    p.segs = plan->d_segs;
+    p.tiles = plan->d_tiles;
+    p.cuts = plan->d_cuts;
+    p.n_cuts = plan->n_cuts;
     KQ_CUDA_TRY(cudaMemsetAsync(d_ws, 0, (size_t)plan->nstages * sizeof(int32_t), st));
   }
   if (plan->fmt == KQ_Q8_0) return launch_plan<KQ_Q8_0>(p, plan->grid, plan->linked, st);
