@@ -596,12 +596,9 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
       const int m = tt / ngrp, q = tt % ngrp;
       // len is a multiple of 32: a block's eight lanes are all inside or all past the slice
       const bool inside = q * 128 + 4 * lane < len;
-      float4 f = make_float4(0.f, 0.f, 0.f, 0.f);
-      if constexpr (kGather) {
-        if (inside) f = *reinterpret_cast<const float4*>(xbuf + q * 128 + 4 * lane);
-      } else {
-        if (inside) f = load_x4<IO16, kTR>(xs, m, kbeg + q * 128 + 4 * lane);
-      }
+      const float4 f = !inside ? make_float4(0.f, 0.f, 0.f, 0.f)
+                       : kGather ? *reinterpret_cast<const float4*>(xbuf + q * 128 + 4 * lane)
+                                 : load_x4<IO16, kTR>(xs, m, kbeg + q * 128 + 4 * lane);
       float amax = fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w)));
       float ssum = (f.x + f.y) + (f.z + f.w);
 #pragma unroll
@@ -1285,10 +1282,10 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
   // linked plan: this CTA has written every output of its items of stage st
   if (LINKED) {
     named_barrier(1, kConsumerWarps * 32);
-    if (cw == 0 && lane == 0) {
-      __threadfence();
-      atomicAdd(p.stage_done + st, 1);
-    }
+    // a release add: the CTA's writes, ordered before it by the barrier,
+    // are visible to any thread that acquires the count
+    if (cw == 0 && lane == 0)
+      asm volatile("red.release.gpu.global.add.s32 [%0], 1;" ::"l"(p.stage_done + st) : "memory");
   }
   }
 
