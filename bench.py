@@ -155,6 +155,24 @@ def _time_steps(fn, steps, stream):
     return start.elapsed_time(end) / 1e3  # seconds
 
 
+def _step_stats(fn, n, stream):
+    """Per-step device times of n more steps, each between its own pair of
+    CUDA events on the stream: median, median absolute deviation, min, max (us)."""
+    import torch
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    t = np.array([a.elapsed_time(b) * 1e3 for a, b in ev])
+    med = float(np.median(t))
+    return {"n": n, "median_us": round(med, 2), "mad_us": round(float(np.median(np.abs(t - med))), 2),
+            "min_us": round(float(t.min()), 2), "max_us": round(float(t.max()), 2)}
+
+
 def max_over_ranks(value, device=None):
     """Largest `value` over all ranks of the default process group (the value
     itself without one).  Used for the timed seconds: the job is as slow as its
@@ -176,7 +194,7 @@ def aggregate_gbs(bytes_per_step, steps, seconds_max, world):
 
 
 def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None, world=1, limit=None, linked=False,
-                    e2e=True, rotation=None):
+                    e2e=True, rotation=None, stats=False):
     import torch
 
     W = wl_mod.DecodeWorkload(config, seed=0, limit=limit, linked=linked, rotation=rotation)
@@ -201,6 +219,7 @@ def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None,
         secs = max_over_ranks(secs, device="cuda")
     if kq.kq_device_status(True) != kq.KQ_OK:
         raise RuntimeError("device status not ok after the timed region")
+    step_stats = _step_stats(lambda: W.step(stream), min(steps, 50), stream) if stats else None
     per_step = secs / steps
     if not e2e:
         out = {"config": config, "matrices": len(W.mats_spec), "weight_bytes": W.weight_bytes,
@@ -239,6 +258,7 @@ def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None,
         "h2d_bytes": xh.numel() * 4,
         "d2h_bytes": yh.numel() * 4,
         "clocks": clocks,
+        "step_stats": step_stats,
     }
     W.close()
     del W
@@ -359,7 +379,7 @@ def run_kq(args):
     stream = torch.cuda.current_stream()
     gpu_index = torch.cuda.current_device()
     head = _decode_measure(kq, workloads, args.workload, args.steps, args.warmup, stream, sampler_gpu=gpu_index,
-                           world=world, limit=args.matrices)
+                           world=world, limit=args.matrices, stats=True)
     peak, peak_kind = _peaks()
     control = _control_measure(kq, head["bytes_per_step"], stream) if rank == 0 else None
     extras = {}
@@ -439,6 +459,7 @@ def run_kq(args):
                 "d2h_bytes_per_step": head["d2h_bytes"], "us_per_step": round(head["e2e_per_step_s"] * 1e6, 2)},
         "gpu_launches": args.steps,
         "clocks": head["clocks"],
+        "step_stats": head["step_stats"],
         "cpu_baseline": cpu,
     }
     if extras:
@@ -538,10 +559,29 @@ def cpu_baseline(config, budget_s=15.0):
         if el > budget_s / 2 or reps >= 50:
             break
     per = el / reps
-    return {"value": round(sample.bytes / per / 1e9, 5), "unit": "GB/s", "cores": oracle.max_threads(),
-            "kind": "oracle",
-            "sample": f"{sample.describe()}, {reps} timed passes of {per * 1e3:.1f} ms each "
-                      f"(FP64 dequantize + transform + GEMV)"}
+    out = {"value": round(sample.bytes / per / 1e9, 5), "unit": "GB/s", "cores": oracle.max_threads(),
+           "kind": "oracle",
+           "sample": f"{sample.describe()}, {reps} timed passes of {per * 1e3:.1f} ms each "
+                     f"(FP64 dequantize + transform + GEMV)"}
+    # the same code on one core, on a sample sized for it
+    cores = oracle.max_threads()
+    oracle.set_threads(1)
+    try:
+        one = _sized_sample(config, budget_s / 16)
+        one.step()
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            one.step()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el > budget_s / 4 or reps >= 20:
+                break
+    finally:
+        oracle.set_threads(cores)
+    per = el / reps
+    out["single_core"] = {"value": round(one.bytes / per / 1e9, 5), "unit": "GB/s", "cores": 1,
+                          "sample": f"{one.describe()}, {reps} timed passes of {per * 1e3:.1f} ms each"}
+    return out
 
 
 def run_reference(args):

@@ -74,6 +74,8 @@ def lib():
         L.orc_gemv_f64.argtypes = [P, I64, I64, P, P, I64, ctypes.c_int32, P, P]
         L.orc_gemv_f64.restype = ctypes.c_int
         L.orc_max_threads.restype = ctypes.c_int
+        L.orc_set_threads.argtypes = [ctypes.c_int]
+        L.orc_set_threads.restype = None
         _lib = L
     return _lib
 
@@ -89,6 +91,12 @@ def _f32(a):
 
 def max_threads():
     return lib().orc_max_threads()
+
+
+def set_threads(n):
+    """Threads of the row loops from now on (timing only; results do not
+    depend on it)."""
+    lib().orc_set_threads(int(n))
 
 
 # -- binary16 -----------------------------------------------------------------

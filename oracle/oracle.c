@@ -28,6 +28,16 @@ int orc_max_threads(void) {
 #endif
 }
 
+/* Threads for the row loops from now on (n >= 1); the timing harness uses it
+ * to time the same code on one core. */
+void orc_set_threads(int n) {
+#ifdef _OPENMP
+  if (n >= 1) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* binary16, from the IEEE 754 definition: 1 sign bit, 5 exponent bits (bias  */
 /* 15), 10 fraction bits; subnormals are f * 2^-24.                           */

@@ -119,6 +119,7 @@ int orc_gemv_f64(const float* w, int64_t n, int64_t k, const double* x, const in
 
 /* Threads the row loops may use (OpenMP), for reporting. */
 int orc_max_threads(void);
+void orc_set_threads(int n);
 
 #ifdef __cplusplus
 }
