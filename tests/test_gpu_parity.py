@@ -763,6 +763,59 @@ def test_linked_plan_chain(kq, wl, fmt):
     plan.close()
 
 
+def test_linked_plan_exact_integer_chain_tolerance_zero(kq):
+    """A Q8_0 chain whose every product and partial sum is exact in fp32
+    (power-of-two scales, small integer activations, |W| |x| below 2^24
+    units of the result's granularity): the device outputs, including row
+    blocks cut between CTAs and read back as sums of partials, must equal
+    the oracle's FP64 values exactly.  Every block's scale is pinned to 2^-5
+    by a code of 127 at its first position, where the activation is always
+    zero (packed inputs are zero there, and rows r % 32 == 0 are zero rows,
+    so every output read as a later activation is zero there too)."""
+    rng = np.random.default_rng(21)
+    # (n, k), (src, stage, of, alpha): a grouped stage of small matrices with
+    # long K (its row blocks are cut many ways), prefixes of outputs, a
+    # ragged K chunk (992) and scales alpha != 1
+    spec = [((512, 2048), (0, 0, 0, 1.0)), ((384, 2048), (1, 0, 0, 1.0)), ((2048, 512), (2, 1, 0, 1.0)),
+            ((1000, 2048), (2, 2, 2, 0.5)), ((256, 992), (2, 3, 3, 2.0))]
+    mats, deqs, links = [], [], []
+    for (n, k), lk in spec:
+        q = rng.choice([-1, 0, 0, 0, 1], size=(n, k))
+        q[:, ::32] = 127
+        q[::32, :] = 0
+        w = (q * 2.0**-5).astype(np.float32)
+        blocks = oracle.q8_0_quantize(w)
+        W = kq.QMatrix("q8_0", n, k)
+        kq.kq_prepare(W, torch.from_numpy(blocks.reshape(-1)).cuda())
+        mats.append(W)
+        deqs.append(oracle.q8_0_dequant(blocks, n, k))
+        links.append(lk)
+    plan = kq.DecodePlan(mats, links)
+    assert plan.split_matrices > 0
+    x0 = rng.integers(-4, 5, size=2048).astype(np.float32)
+    x0[::32] = 0.0
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    ws.view(torch.float32).fill_(float("nan"))
+    y = torch.full((plan.y_floats,), float("nan"), dtype=torch.float32, device="cuda")
+    plan.step(torch.from_numpy(x0).cuda(), y, ws)
+    _sync_ok(kq)
+    yh = y.cpu().numpy()
+    offs = np.cumsum([0] + [n for (n, _), _ in spec])
+    xin, gran = [x0.astype(np.float64)], [1.0]  # activation values and their granularity
+    for i, ((n, k), (src, _, of, alpha)) in enumerate(spec):
+        if i > 0:
+            if src == synth.SRC_INPUT_OF:
+                xin.append(xin[of])
+                gran.append(gran[of])
+            else:
+                xin.append(alpha * yh[offs[of]:offs[of] + k].astype(np.float64))
+                gran.append(alpha * 2.0**-5 * gran[of])
+        y_ref, absdot = oracle.gemv(deqs[i], xin[i])
+        assert (absdot / (2.0**-5 * gran[i])).max() < 2.0**24  # every partial sum is exact
+        assert np.array_equal(yh[offs[i]:offs[i + 1]].astype(np.float64), y_ref), i
+    plan.close()
+
+
 def test_linked_plan_rejects_bad_links(kq, wl):
     mats = [wl.build_matrix("q8_0", 256, 256, 1, synth.stream_id("test", 0, 380 + i)) for i in range(3)]
     bad = [
