@@ -75,7 +75,8 @@ constexpr int kMaxStages = 6;  // TMA ring depth limit
 constexpr int kMaxD = 4;       // accumulator buffers in tensor memory
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kDeqWarps + kEpiWarps);  // 576
+constexpr int kIssuer2Warp = 2 + kDeqWarps + kEpiWarps;  // the second MMA issuer
+constexpr int kThreads = 32 * (kIssuer2Warp + 1);           // 608
 constexpr int kScaleBoxBytes = kRows * 16;                   // 8 fp16 scales per row
 constexpr int kBarBytes = 256;
 constexpr size_t kSmemBytes = 232448;  // the per-CTA maximum; carved at run time
@@ -364,6 +365,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int nstages = p.stages;
   const int gb = group_blocks(FMT, MP);  // blocks per accumulator group
   const int nd = d_groups_for(gb, MP);   // accumulator groups in tensor memory
+  // PQ2_0 (one block, a few accumulator columns per chunk): two MMA issuers
+  // take alternate chunks (g = a chunk's place in this CTA's list); issuer
+  // g % 2 uses A buffer g % 2 and its own half of the accumulator buffers, so
+  // neither waits for the other.  Q8_0 and SCALE4 (four blocks per chunk)
+  // fill tensor memory with fewer chunks' accumulators and keep one issuer
+  // over all of them.
+  constexpr int NI = kBlocks == 1 ? 2 : 1;  // MMA issuers
+  const int ndi = nd / NI;                  // accumulator buffers per issuer
   const int sbytes = stage_bytes(FMT, MP);
   const int off_scales = kCodes, off_b = kCodes + kScaleBoxBytes;
   uint8_t* stages = smem;
@@ -374,8 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   uint64_t* a_empty = a_full + 2;               // [2] MMA commit -> unpack
   uint64_t* d_full = a_empty + 2;               // [kMaxD] MMA commit -> epilogue
   uint64_t* d_empty = d_full + kMaxD;           // [kMaxD] epilogue warps -> MMA
-  uint64_t* drain = d_empty + kMaxD;            // [1] final MMA commit
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* drain = d_empty + kMaxD;            // [2] final commit of each MMA issuer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -394,7 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(&d_full[b], 1);
       mbar_init(&d_empty[b], kEpiWarps);
     }
-    mbar_init(drain, 1);
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -466,56 +476,62 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         (void)mbar_wait_bounded(&tma_full[back.slot], back.phase);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------ MMA issuer --------------------------------
-    if (lane == 0) {
+  } else if (warp == 1 || warp == kIssuer2Warp) {
+    // ------------------------------ MMA issuers -------------------------------
+    const int me = warp == 1 ? 0 : 1;
+    if (lane == 0 && me < NI) {
       const uint32_t idesc = idesc_f16(kRows, 2 * MP);
-      Ring ring, dring;
-      int ab = 0;
-      uint32_t aph = 0;
+      Ring ring, dring;  // the stage of every chunk; this issuer's accumulator buffers
+      int g = 0;
       for (int item = ib; item < ie && !*abort_flag; ++item) {
         const int split = item / p.tiles;
         const int c0 = chunk_begin(split), c1 = chunk_begin(split + 1);
-        for (int c = c0; c < c1 && !*abort_flag; ++c) {
-          if (!mbar_wait_bounded(&tma_full[ring.slot], ring.phase) || !mbar_wait_bounded(&a_full[ab], aph)) {
+        for (int c = c0; c < c1 && !*abort_flag; ++c, ++g, ring.next(nstages)) {
+          if (g % NI != me) continue;
+          const int slot = ring.slot, ab = g & 1;  // A buffers alternate by chunk
+          if (!mbar_wait_bounded(&tma_full[slot], ring.phase) ||
+              !mbar_wait_bounded(&a_full[ab], (uint32_t)((g >> 1) & 1))) {
             fail_wait();
             break;
           }
           tc_fence_after();
           const uint32_t a_tmem = tmem_base + (uint32_t)ab * kACols;
-          const uint8_t* bt = stages + (size_t)ring.slot * sbytes + off_b;
+          const uint8_t* bt = stages + (size_t)slot * sbytes + off_b;
+          // descriptors of the two B boxes; a K step adds its 32-byte offset (>> 4) to the start field
+          const uint64_t bd0 = sw128_desc(bt), bd1 = sw128_desc(bt + b_box_bytes(MP));
+          bool ok = true;
           for (int b = 0; b < kBlocks; ++b) {
-            const int bg = b % gb;  // block within its accumulator group
+            const int bg = b % gb;
+            const int dslot = me * ndi + dring.slot;
             if (bg == 0) {
-              if (!mbar_wait_bounded(&d_empty[dring.slot], dring.phase ^ 1u)) {
+              if (!mbar_wait_bounded(&d_empty[dslot], dring.phase ^ 1u)) {
                 fail_wait();
+                ok = false;
                 break;
               }
               tc_fence_after();
             }
-            const uint32_t d_tmem = tmem_base + kTmemD + (uint32_t)((dring.slot * gb + bg) * 2 * MP);
+            const uint32_t d_tmem = tmem_base + kTmemD + (uint32_t)((dslot * gb + bg) * 2 * MP);
 #pragma unroll
             for (int t = 0; t < kSteps; ++t) {
               const int kk = b * kSteps + t;
               const int atom = kk >> 2, sub = (kk & 3) * 32;
-              tc_mma_ts(d_tmem, a_tmem + (uint32_t)(kk * 8), sw128_desc(bt + atom * b_box_bytes(MP) + sub), idesc,
+              tc_mma_ts(d_tmem, a_tmem + (uint32_t)(kk * 8), (atom ? bd1 : bd0) + (uint64_t)(sub >> 4), idesc,
                         t > 0 ? 1u : 0u);
             }
             if (bg == gb - 1) {
-              tc_commit(&d_full[dring.slot]);
-              dring.next(nd);
+              tc_commit(&d_full[dslot]);
+              dring.next(ndi);
             }
           }
+          if (!ok) break;
           tc_commit(&a_empty[ab]);
-          tc_commit(&tma_empty[ring.slot]);
-          ring.next(nstages);
-          ab ^= 1;
-          if (ab == 0) aph ^= 1u;
+          tc_commit(&tma_empty[slot]);
         }
       }
-      // wait until every MMA issued above has completed
-      tc_commit(drain);
-      (void)mbar_wait_bounded(drain, 0);
+      // wait until every MMA this thread issued has completed
+      tc_commit(&drain[me]);
+      (void)mbar_wait_bounded(&drain[me], 0);
     }
   } else if (warp < 2 + kDeqWarps) {
     // ------------------------------ unpack ----------------------------------
@@ -614,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         if (ab == 0) aph ^= 1u;
       }
     }
-  } else {
+  } else if (warp < kIssuer2Warp) {
     // ------------------------------ epilogue ------------------------------------
     const int quarter = warp & 3;                   // tensor-memory lane quarter
     const int ahalf = (warp - 2 - kDeqWarps) >> 2;  // half of the activation columns
@@ -622,7 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int half = MP / 2;  // 8 .. 32 activation columns per warp
     const int i0 = ahalf * half;
     const uint32_t d_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + kTmemD + (uint32_t)i0;
-    Ring ring, dring;
+    Ring ring, dr0, dr1;  // stages; each issuer's accumulator buffers
+    int g = 0;            // the chunk's place in this CTA's list (its issuer is g % NI)
     for (int item = ib; item < ie; ++item) {
       const int split = item / p.tiles, tile = item - split * p.tiles;
       const int c0 = chunk_begin(split), c1 = chunk_begin(split + 1);
@@ -630,26 +647,28 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       float acc[32];
 #pragma unroll
       for (int q = 0; q < 32; ++q) acc[q] = 0.f;
-      for (int c = c0; c < c1; ++c) {
+      for (int c = c0; c < c1; ++c, ++g) {
         if (!*abort_flag) {
           if (!mbar_wait_bounded(&tma_full[ring.slot], ring.phase)) {
             fail_wait();
           } else {
             const uint8_t* st = stages + (size_t)ring.slot * sbytes;
+            const int me = g % NI;
             // this chunk's block scales of row r, from its 16-byte box
             const __half* srow = reinterpret_cast<const __half*>(st + off_scales + r * 16);
             const int s0 = kBlocks == 4 ? 4 * (c & 1) : (c & 7);
             for (int b = 0; b < kBlocks; ++b) {
               const int bg = b % gb;
+              const int dslot = me ? ndi + dr1.slot : dr0.slot;
               if (bg == 0) {
-                if (!mbar_wait_bounded(&d_full[dring.slot], dring.phase)) {
+                if (!mbar_wait_bounded(&d_full[dslot], me ? dr1.phase : dr0.phase)) {
                   fail_wait();
                   break;
                 }
                 tc_fence_after();
               }
               const float d = __half2float(srow[s0 + b]);
-              const uint32_t t0 = d_lane + (uint32_t)((dring.slot * gb + bg) * 2 * MP);
+              const uint32_t t0 = d_lane + (uint32_t)((dslot * gb + bg) * 2 * MP);
 #pragma unroll
               for (int g = 0; g < 32; g += 8) {
                 if (g < half) {
@@ -664,8 +683,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               if (bg == gb - 1) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&d_empty[dring.slot]);
-                dring.next(nd);
+                if (lane == 0) mbar_arrive(&d_empty[dslot]);
+                if (me)
+                  dr1.next(ndi);
+                else
+                  dr0.next(ndi);
               }
             }
             __syncwarp();
