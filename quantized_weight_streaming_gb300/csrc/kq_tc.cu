@@ -75,8 +75,9 @@ constexpr int kMaxStages = 6;  // TMA ring depth limit
 constexpr int kMaxD = 4;       // accumulator buffers in tensor memory
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 8;
-constexpr int kIssuer2Warp = 2 + kDeqWarps + kEpiWarps;  // the second MMA issuer
-constexpr int kThreads = 32 * (kIssuer2Warp + 1);           // 608
+constexpr int kIssuer2Warp = 2 + kDeqWarps + kEpiWarps;  // the second and third MMA issuers
+constexpr int kMaxIssuers = 3;
+constexpr int kThreads = 32 * (kIssuer2Warp + kMaxIssuers - 1);  // 640
 constexpr int kScaleBoxBytes = kRows * 16;                   // 8 fp16 scales per row
 constexpr int kBarBytes = 256;
 constexpr size_t kSmemBytes = 232448;  // the per-CTA maximum; carved at run time
@@ -365,26 +366,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int nstages = p.stages;
   const int gb = group_blocks(FMT, MP);  // blocks per accumulator group
   const int nd = d_groups_for(gb, MP);   // accumulator groups in tensor memory
-  // PQ2_0 (one block, a few accumulator columns per chunk): two MMA issuers
-  // take alternate chunks (g = a chunk's place in this CTA's list); issuer
-  // g % 2 uses A buffer g % 2 and its own half of the accumulator buffers, so
-  // neither waits for the other.  Q8_0 and SCALE4 (four blocks per chunk)
-  // fill tensor memory with fewer chunks' accumulators and keep one issuer
-  // over all of them.
-  constexpr int NI = kBlocks == 1 ? 2 : 1;  // MMA issuers
-  const int ndi = nd / NI;                  // accumulator buffers per issuer
+  // PQ2_0 (one block, a few accumulator columns per chunk): three MMA issuers
+  // take turns by chunk (g = a chunk's place in this CTA's list); issuer
+  // g % 3 owns accumulator buffer g % 3 (nd >= 3), the A buffers alternate
+  // by chunk, and no issuer waits for another.  Q8_0 and SCALE4 (four blocks
+  // per chunk) fill tensor memory with fewer chunks' accumulators and keep
+  // one issuer over all of them.
+  constexpr int NI = kBlocks == 1 ? kMaxIssuers : 1;  // MMA issuers
+  const int ndi = nd / NI;                            // accumulator buffers per issuer (1 when NI > 1)
   const int sbytes = stage_bytes(FMT, MP);
   const int off_scales = kCodes, off_b = kCodes + kScaleBoxBytes;
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCarveBytes);
   uint64_t* tma_full = bars;                    // [kMaxStages] producer -> unpack, MMA, epilogue
   uint64_t* tma_empty = tma_full + kMaxStages;  // [kMaxStages] unpack, MMA commit, epilogue -> producer
-  uint64_t* a_full = tma_empty + kMaxStages;    // [2] unpack warps -> MMA
-  uint64_t* a_empty = a_full + 2;               // [2] MMA commit -> unpack
+  uint64_t* a_full = tma_empty + kMaxStages;    // [kMaxStages] unpack warps -> the chunk's issuer, per stage
+  uint64_t* a_empty = a_full + kMaxStages;      // [2] MMA commit -> unpack (per A buffer)
   uint64_t* d_full = a_empty + 2;               // [kMaxD] MMA commit -> epilogue
   uint64_t* d_empty = d_full + kMaxD;           // [kMaxD] epilogue warps -> MMA
-  uint64_t* drain = d_empty + kMaxD;            // [2] final commit of each MMA issuer
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 2);
+  uint64_t* drain = d_empty + kMaxD;            // [kMaxIssuers] final commit of each MMA issuer
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -395,16 +396,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       mbar_init(&tma_full[s], 1);
       mbar_init(&tma_empty[s], kDeqWarps + 1 + kEpiWarps);  // codes, B (MMA commit), scales
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&a_full[b], kDeqWarps);
-      mbar_init(&a_empty[b], 1);
-    }
+    // a_full per stage, with the stage's phase: an issuer waits on it only
+    // after tma_full of the same stage and phase, which already implies that
+    // the stage's previous chunk was unpacked, and the stage's next chunk
+    // cannot be unpacked before this one's MMAs were issued; so no issuer,
+    // however many there are, sees a phase early or late
+    for (int s2 = 0; s2 < nstages; ++s2) mbar_init(&a_full[s2], kDeqWarps);
+    for (int b = 0; b < 2; ++b) mbar_init(&a_empty[b], 1);
     for (int b = 0; b < nd; ++b) {
       mbar_init(&d_full[b], 1);
       mbar_init(&d_empty[b], kEpiWarps);
     }
-    mbar_init(&drain[0], 1);
-    mbar_init(&drain[1], 1);
+    for (int i = 0; i < kMaxIssuers; ++i) mbar_init(&drain[i], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -476,9 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         (void)mbar_wait_bounded(&tma_full[back.slot], back.phase);
       }
     }
-  } else if (warp == 1 || warp == kIssuer2Warp) {
+  } else if (warp == 1 || warp >= kIssuer2Warp) {
     // ------------------------------ MMA issuers -------------------------------
-    const int me = warp == 1 ? 0 : 1;
+    const int me = warp == 1 ? 0 : warp - kIssuer2Warp + 1;
     if (lane == 0 && me < NI) {
       const uint32_t idesc = idesc_f16(kRows, 2 * MP);
       Ring ring, dring;  // the stage of every chunk; this issuer's accumulator buffers
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           if (g % NI != me) continue;
           const int slot = ring.slot, ab = g & 1;  // A buffers alternate by chunk
           if (!mbar_wait_bounded(&tma_full[slot], ring.phase) ||
-              !mbar_wait_bounded(&a_full[ab], (uint32_t)((g >> 1) & 1))) {
+              !mbar_wait_bounded(&a_full[slot], ring.phase)) {
             fail_wait();
             break;
           }
@@ -620,7 +623,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-              mbar_arrive(&a_full[ab]);
+              mbar_arrive(&a_full[ring.slot]);
               mbar_arrive(&tma_empty[ring.slot]);
             }
           }
@@ -638,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int half = MP / 2;  // 8 .. 32 activation columns per warp
     const int i0 = ahalf * half;
     const uint32_t d_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + kTmemD + (uint32_t)i0;
-    Ring ring, dr0, dr1;  // stages; each issuer's accumulator buffers
+    Ring ring, dr0;  // stages; the accumulator buffers (one issuer)
     int g = 0;            // the chunk's place in this CTA's list (its issuer is g % NI)
     for (int item = ib; item < ie; ++item) {
       const int split = item / p.tiles, tile = item - split * p.tiles;
@@ -659,9 +662,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             const int s0 = kBlocks == 4 ? 4 * (c & 1) : (c & 7);
             for (int b = 0; b < kBlocks; ++b) {
               const int bg = b % gb;
-              const int dslot = me ? ndi + dr1.slot : dr0.slot;
+              // one issuer: a ring over the buffers; several: buffer `me`, its (g / NI)-th use
+              const int dslot = NI == 1 ? dr0.slot : me;
+              const uint32_t dphase = NI == 1 ? dr0.phase : (uint32_t)((g / NI) & 1);
               if (bg == 0) {
-                if (!mbar_wait_bounded(&d_full[dslot], me ? dr1.phase : dr0.phase)) {
+                if (!mbar_wait_bounded(&d_full[dslot], dphase)) {
                   fail_wait();
                   break;
                 }
@@ -684,10 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&d_empty[dslot]);
-                if (me)
-                  dr1.next(ndi);
-                else
-                  dr0.next(ndi);
+                if (NI == 1) dr0.next(nd);
               }
             }
             __syncwarp();
