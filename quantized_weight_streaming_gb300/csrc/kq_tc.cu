@@ -79,14 +79,14 @@ constexpr int kIssuer2Warp = 2 + kDeqWarps + kEpiWarps;  // the second and third
 constexpr int kMaxIssuers = 3;
 constexpr int kThreads = 32 * (kIssuer2Warp + kMaxIssuers - 1);  // 640
 constexpr int kScaleBoxBytes = kRows * 16;                   // 8 fp16 scales per row
-constexpr int kBarBytes = 256;
+constexpr int kBarBytes = 512;
 constexpr size_t kSmemBytes = 232448;  // the per-CTA maximum; carved at run time
 constexpr size_t kCarveBytes = kSmemBytes - 1024 /* alignment slack */ - kBarBytes;
 // tensor memory: two A buffers of 64 columns (128 fp16 per row) at [0, 128),
 // then the accumulators, 2M' columns each
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kACols = kChunk / 2;
-constexpr uint32_t kTmemD = 2 * kACols;
+constexpr uint32_t kACols = kChunk / 2;  // tensor-memory columns of one A buffer
+constexpr int kMaxA = 4;                 // A buffers
 
 // code bytes of one 128-weight chunk of a row: 128 (Q8_0), 64 (SCALE4), 32 (PQ2_0)
 __host__ __device__ constexpr int chunk_row_bytes(int fmt) {
@@ -102,8 +102,18 @@ __host__ __device__ constexpr int stage_bytes(int fmt, int mp) { return (stage_t
 // (2M' columns each) under one barrier pair, so the MMA thread waits and
 // commits once per group; groups rotate through d_groups() buffers.
 __host__ __device__ constexpr int blocks_per_chunk(int fmt) { return fmt == KQ_PQ2_0 ? 1 : 4; }
-__host__ __device__ constexpr int d_groups_for(int gb, int mp) {
-  return (int)((kTmemCols - kTmemD) / (gb * 2 * mp)) < kMaxD ? (int)((kTmemCols - kTmemD) / (gb * 2 * mp)) : kMaxD;
+__host__ __device__ constexpr int d_groups_for(int gb, int mp, int na = 2) {
+  return (int)((kTmemCols - na * kACols) / (gb * 2 * mp)) < kMaxD ? (int)((kTmemCols - na * kACols) / (gb * 2 * mp))
+                                                                  : kMaxD;
+}
+// A buffers (the unpack runs that many chunks ahead of the MMAs): PQ2_0 takes
+// four, or three, while tensor memory still holds an accumulator buffer for
+// each of its three issuers; Q8_0 and SCALE4 keep two.
+__host__ __device__ constexpr int a_buffers(int fmt, int mp) {
+  return blocks_per_chunk(fmt) != 1          ? 2
+         : d_groups_for(1, mp, 4) >= 3       ? 4
+         : d_groups_for(1, mp, 3) >= 3       ? 3
+                                             : 2;
 }
 // largest group (4, 2 or 1 blocks, dividing the chunk's blocks) that still leaves three buffers
 __host__ __device__ constexpr int group_blocks(int fmt, int mp) {
@@ -365,7 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const int MP = p.mp;
   const int nstages = p.stages;
   const int gb = group_blocks(FMT, MP);  // blocks per accumulator group
-  const int nd = d_groups_for(gb, MP);   // accumulator groups in tensor memory
+  const int na = a_buffers(FMT, MP);      // A buffers
+  const uint32_t tmem_d = (uint32_t)na * kACols;  // first accumulator column
+  const int nd = d_groups_for(gb, MP, na);  // accumulator groups in tensor memory
   // PQ2_0 (one block, a few accumulator columns per chunk): three MMA issuers
   // take turns by chunk (g = a chunk's place in this CTA's list); issuer
   // g % 3 owns accumulator buffer g % 3 (nd >= 3), the A buffers alternate
@@ -381,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   uint64_t* tma_full = bars;                    // [kMaxStages] producer -> unpack, MMA, epilogue
   uint64_t* tma_empty = tma_full + kMaxStages;  // [kMaxStages] unpack, MMA commit, epilogue -> producer
   uint64_t* a_full = tma_empty + kMaxStages;    // [kMaxStages] unpack warps -> the chunk's issuer, per stage
-  uint64_t* a_empty = a_full + kMaxStages;      // [2] MMA commit -> unpack (per A buffer)
-  uint64_t* d_full = a_empty + 2;               // [kMaxD] MMA commit -> epilogue
+  uint64_t* a_empty = a_full + kMaxStages;      // [kMaxA] MMA commit -> unpack (per A buffer)
+  uint64_t* d_full = a_empty + kMaxA;               // [kMaxD] MMA commit -> epilogue
   uint64_t* d_empty = d_full + kMaxD;           // [kMaxD] epilogue warps -> MMA
   uint64_t* drain = d_empty + kMaxD;            // [kMaxIssuers] final commit of each MMA issuer
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + kMaxIssuers);
@@ -402,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // cannot be unpacked before this one's MMAs were issued; so no issuer,
     // however many there are, sees a phase early or late
     for (int s2 = 0; s2 < nstages; ++s2) mbar_init(&a_full[s2], kDeqWarps);
-    for (int b = 0; b < 2; ++b) mbar_init(&a_empty[b], 1);
+    for (int b = 0; b < na; ++b) mbar_init(&a_empty[b], 1);
     for (int b = 0; b < nd; ++b) {
       mbar_init(&d_full[b], 1);
       mbar_init(&d_empty[b], kEpiWarps);
@@ -484,14 +496,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int me = warp == 1 ? 0 : warp - kIssuer2Warp + 1;
     if (lane == 0 && me < NI) {
       const uint32_t idesc = idesc_f16(kRows, 2 * MP);
-      Ring ring, dring;  // the stage of every chunk; this issuer's accumulator buffers
+      Ring ring, dring, ar;  // the stage and A buffer of every chunk; this issuer's accumulator buffers
       int g = 0;
       for (int item = ib; item < ie && !*abort_flag; ++item) {
         const int split = item / p.tiles;
         const int c0 = chunk_begin(split), c1 = chunk_begin(split + 1);
-        for (int c = c0; c < c1 && !*abort_flag; ++c, ++g, ring.next(nstages)) {
+        for (int c = c0; c < c1 && !*abort_flag; ++c, ++g, ring.next(nstages), ar.next(na)) {
           if (g % NI != me) continue;
-          const int slot = ring.slot, ab = g & 1;  // A buffers alternate by chunk
+          const int slot = ring.slot, ab = ar.slot;
           if (!mbar_wait_bounded(&tma_full[slot], ring.phase) ||
               !mbar_wait_bounded(&a_full[slot], ring.phase)) {
             fail_wait();
@@ -514,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               }
               tc_fence_after();
             }
-            const uint32_t d_tmem = tmem_base + kTmemD + (uint32_t)((dslot * gb + bg) * 2 * MP);
+            const uint32_t d_tmem = tmem_base + tmem_d + (uint32_t)((dslot * gb + bg) * 2 * MP);
 #pragma unroll
             for (int t = 0; t < kSteps; ++t) {
               const int kk = b * kSteps + t;
@@ -542,20 +554,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int khalf = (warp - 2) >> 2;  // half of the chunk's K
     const int r = quarter * 32 + lane;  // weight row in the tile
     const uint32_t a_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(khalf * 32);
-    Ring ring;
-    int ab = 0;
-    uint32_t aph = 0;
+    Ring ring, ar;  // stages; A buffers
     for (int item = ib; item < ie; ++item) {
       const int split = item / p.tiles;
       const int c0 = chunk_begin(split), c1 = chunk_begin(split + 1);
       for (int c = c0; c < c1; ++c) {
         if (!*abort_flag) {
-          if (!mbar_wait_bounded(&tma_full[ring.slot], ring.phase) || !mbar_wait_bounded(&a_empty[ab], aph ^ 1u)) {
+          if (!mbar_wait_bounded(&tma_full[ring.slot], ring.phase) ||
+              !mbar_wait_bounded(&a_empty[ar.slot], ar.phase ^ 1u)) {
             fail_wait();
           } else {
             tc_fence_after();
             const uint8_t* st = stages + (size_t)ring.slot * sbytes;
-            const uint32_t a_tmem = a_lane + (uint32_t)ab * kACols;
+            const uint32_t a_tmem = a_lane + (uint32_t)ar.slot * kACols;
             if (FMT == KQ_Q8_0) {
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
@@ -629,8 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
         }
         ring.next(nstages);
-        ab ^= 1;
-        if (ab == 0) aph ^= 1u;
+        ar.next(na);
       }
     }
   } else if (warp < kIssuer2Warp) {
@@ -640,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int r = quarter * 32 + lane;
     const int half = MP / 2;  // 8 .. 32 activation columns per warp
     const int i0 = ahalf * half;
-    const uint32_t d_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + kTmemD + (uint32_t)i0;
+    const uint32_t d_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + tmem_d + (uint32_t)i0;
     Ring ring, dr0;  // stages; the accumulator buffers (one issuer)
     int g = 0;            // the chunk's place in this CTA's list (its issuer is g % NI)
     for (int item = ib; item < ie; ++item) {
