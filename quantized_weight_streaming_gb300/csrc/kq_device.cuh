@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 namespace kq {
 
 // Cycles a bounded wait spins before it gives up (about 1 s at 2 GHz).
@@ -56,6 +58,32 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (clock64() - start > kWaitLimitCycles) return false;
   }
   return true;
+}
+
+// Programmatic dependent launch: waits until the grid launched before this
+// one on the stream has completed and its writes are visible.  A kernel
+// launched with the programmatic-serialization attribute may start (and run
+// its prologue) while that grid is still running; launched without it, this
+// returns at once.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches kernel k as a programmatic dependent of the stream's previous
+// kernel (the kernel must call grid_dependency_wait before reading that
+// kernel's outputs).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*k)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, std::forward<Args>(args)...);
 }
 
 // L2 policy for data read exactly once (the weight stream): evict first.

@@ -1348,6 +1348,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
 template <bool OUT16 = false>
 __global__ void reduce_splits_kernel(const float* __restrict__ ws, float* __restrict__ y, int64_t n, int64_t ldy,
                                      int m, int splits) {
+  grid_dependency_wait();  // the partials of the kernel before (a programmatic dependent launch)
   const int64_t total = (int64_t)m * n;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t mm = i / n, row = i % n;
@@ -1599,11 +1600,13 @@ static int gemm_impl(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, 
     if (g.splits > 1) {
       const int64_t tot = (int64_t)mm * W->n;
       const int rgrid = (int)std::min<int64_t>((tot + 255) / 256, (int64_t)sms * 8);
+      // launched as a programmatic dependent: its launch overlaps the GEMV's tail
       if (io16)
-        reduce_splits_kernel<true><<<rgrid, 256, 0, st>>>((const float*)d_ws, d_Y, W->n, W->n, mm, g.splits);
+        KQ_CUDA_TRY(launch_dependent(reduce_splits_kernel<true>, dim3(rgrid), dim3(256), 0, st, (const float*)d_ws,
+                                     d_Y, W->n, W->n, mm, g.splits));
       else
-        reduce_splits_kernel<<<rgrid, 256, 0, st>>>((const float*)d_ws, d_Y + m0 * W->n, W->n, W->n, mm, g.splits);
-      KQ_CUDA_TRY(cudaGetLastError());
+        KQ_CUDA_TRY(launch_dependent(reduce_splits_kernel<false>, dim3(rgrid), dim3(256), 0, st, (const float*)d_ws,
+                                     d_Y + m0 * W->n, W->n, W->n, mm, g.splits));
     }
   }
   return KQ_OK;

@@ -429,6 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (warp == 1) tmem_relinquish();
+  // everything above overlaps the activation prologue; its B matrix and
+  // scales are read below
+  grid_dependency_wait();
 
   const int items = p.tiles * p.splits;
   const int ib = (int)((int64_t)items * blockIdx.x / gridDim.x);
@@ -728,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
 // Y[i][row] = sum over splits, in split order, of the partials
 __global__ void tc_reduce_kernel(const float* __restrict__ part, float* __restrict__ y, int64_t total, int splits) {
+  grid_dependency_wait();  // the GEMM's partials (a programmatic dependent launch)
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total; t += (int64_t)gridDim.x * blockDim.x) {
     float acc = part[t];
     for (int s = 1; s < splits; ++s) acc += part[(int64_t)s * total + t];
@@ -813,8 +817,9 @@ int launch_tc(const tc::TcParams& p, int grid, cudaStream_t st) {
                                 (int)tc::kSmemBytes);
   });
   KQ_CUDA_TRY(attr);
-  tc::tc_gemm_kernel<FMT><<<grid, tc::kThreads, tc::kSmemBytes, st>>>(p);
-  KQ_CUDA_TRY(cudaGetLastError());
+  // a programmatic dependent of the activation prologue: barrier set-up and
+  // tensor-memory allocation overlap its tail
+  KQ_CUDA_TRY(launch_dependent(tc::tc_gemm_kernel<FMT>, dim3(grid), dim3(tc::kThreads), tc::kSmemBytes, st, p));
   return KQ_OK;
 }
 
@@ -930,8 +935,8 @@ int tc_gemm(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int split
   if (g.splits > 1) {
     const int64_t total = m * W->n;
     const int rgrid = (int)std::min<int64_t>((total + 255) / 256, (int64_t)sms * 8);
-    tc::tc_reduce_kernel<<<rgrid, 256, 0, st>>>(part, d_Y, total, g.splits);
-    KQ_CUDA_TRY(cudaGetLastError());
+    KQ_CUDA_TRY(launch_dependent(tc::tc_reduce_kernel, dim3(rgrid), dim3(256), 0, st, (const float*)part, d_Y,
+                                 total, g.splits));
   }
   return KQ_OK;
 }
