@@ -816,6 +816,41 @@ def test_linked_plan_exact_integer_chain_tolerance_zero(kq):
     plan.close()
 
 
+def test_linked_plan_cuts_row_blocks_only_where_it_pays(kq, wl):
+    """The plan deals each stage to the SMs either in equal byte shares
+    (cutting row blocks) or whole row blocks, whichever loads the busiest SM
+    less.  Two 17408 x 5120 PQ2_0 matrices (136 row blocks of 5 chunks) go
+    whole onto one SM each when there are at least 136 SMs; a 5120 x 6144
+    stage (120 chunks) is cut when there are more SMs than chunks.  Sampled
+    rows of each output match the oracle on the activation read."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    spec = [((17408, 5120), (0, 0, 0, 1.0)), ((17408, 5120), (1, 0, 0, 1.0)), ((5120, 6144), (2, 1, 0, 0.5))]
+    seed = 7
+    streams = [synth.stream_id("test", 0, 390 + i) for i in range(len(spec))]
+    mats = [wl.build_matrix("pq2_0", n, k, seed, sw) for ((n, k), _), sw in zip(spec, streams)]
+    plan = kq.DecodePlan(mats, [lk for _, lk in spec])
+    if sms >= 136 and sms > 120:
+        assert plan.split_matrices == 1  # only the 120-chunk stage is cut
+    x0 = synth.fill_host("x", 5120, seed, synth.stream_id("test", 1, 390))
+    ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    ws.view(torch.float32).fill_(float("nan"))
+    y = torch.full((plan.y_floats,), float("nan"), dtype=torch.float32, device="cuda")
+    plan.step(torch.from_numpy(x0).cuda(), y, ws)
+    _sync_ok(kq)
+    yh = y.cpu().numpy()
+    offs = np.cumsum([0] + [n for (n, _), _ in spec])
+    xin = [x0, x0, (np.float32(0.5) * yh[: 6144]).astype(np.float32)]
+    rng = np.random.default_rng(3)
+    for i, ((n, k), _) in enumerate(spec):
+        rows = np.unique(np.r_[0, n - 1, rng.integers(0, n, size=8)])
+        w = synth.matrix_rows_host(n, k, rows, seed, streams[i])
+        deq = oracle.pq2_0_dequant(oracle.pq2_0_quantize(oracle.rotate_rows(w)[1]), rows.size, k)
+        y_ref, absdot = oracle.gemv(deq, oracle.rotate_rows(xin[i])[0])
+        ok, worst = oracle.within_bound(yh[offs[i] + rows], y_ref, absdot, TOL)
+        assert ok, (i, worst)
+    plan.close()
+
+
 def test_linked_plan_rejects_bad_links(kq, wl):
     mats = [wl.build_matrix("q8_0", 256, 256, 1, synth.stream_id("test", 0, 380 + i)) for i in range(3)]
     bad = [
