@@ -22,6 +22,8 @@
 //      warp 1       allocates tensor memory; one thread issues tcgen05.mma
 //                   (kind::f16, M = 128, N = 2M', K = 16, A from tensor
 //                   memory, B from shared memory) and commits;
+//      warps 18-19  for PQ2_0, two more issuing threads: issuer g % 3 takes
+//                   the CTA's chunk g and owns accumulator buffer g % 3;
 //      warps 2-9    unpack the chunk into the A operand in tensor memory
 //                   (tcgen05.st): lane i of a warp owns weight row i of its
 //                   quarter, each warp half of the chunk's K;
@@ -42,13 +44,17 @@
 //    (c - 1) * 2^(s-24).  The prologue scales the matching B entries by
 //    2^(24-s) and permutes B's K order to the pairing, so A x B sums
 //    (c - 1) x' 2^-(10+e) for every position.
-//  * The single MMA thread issues one instruction per 16-weight K step
-//    (8 per chunk).  Measured on GB300: a thread issuing tcgen05.mma back to
-//    back spends ~55-110 cycles per instruction whatever N is up to 128, so
-//    at small N this thread, not the tensor pipe, sets the pace (about one
-//    chunk per ~1400 cycles).  Several issuing warps reach the tensor pipe's
-//    peak in isolation, but in this pipeline their extra barrier waits and
-//    commits cost more than they saved.
+//  * An issuing thread issues one instruction per 16-weight K step (8 per
+//    chunk).  Measured on GB300: a thread issuing tcgen05.mma back to back
+//    spends ~55-110 cycles per instruction whatever N is up to 128, so at
+//    small N one thread, not the tensor pipe, would set the pace.  PQ2_0 has
+//    three issuers that take whole chunks in turn and never wait for one
+//    another; Q8_0 and SCALE4 keep one, as their four accumulator blocks per
+//    chunk leave tensor memory for only three chunks' accumulators.
+//  * The unpack -> issuer barrier is per stage slot and waited on with the
+//    stage's phase right after that slot's tma_full, so an issuer that skips
+//    the other issuers' chunks can never take another chunk's phase for its
+//    own.
 // Every wait is bounded; a timeout sets KQ_ERR_TIMEOUT in the status word,
 // every role stops waiting, the producer waits (bounded) for its copies in
 // flight, the MMA thread drains its work, and the tensor memory is freed
