@@ -509,8 +509,9 @@ class OracleSample:
             self.bytes += rows.size * (k // (4 if fmt == "pq2_0" else 1) + 2 * k // bs) + 4 * (k + rows.size)
 
     def describe(self):
+        which = "every projection" if self.stride == 1 else f"one projection in {self.stride}"
         return (f"{self.rows} rows of {len(self.items)} of the {len(self.spec)} projections of {self.config} "
-                f"(every {self.stride}th; {self.bytes / 1e6:.2f} MB of the step's bytes)")
+                f"({which}; {self.bytes / 1e6:.2f} MB of the step's bytes)")
 
     def step(self):
         o = self.oracle
@@ -524,25 +525,25 @@ class OracleSample:
             o.gemv(deq, x64)
 
 
-def _sized_sample(config, step_budget_s):
-    """OracleSample whose step takes about step_budget_s on this host."""
-    probe = OracleSample(config, 1, 1)
-    probe.step()
-    t0 = time.perf_counter()
-    probe.step()
-    t1 = time.perf_counter() - t0
+def _sized_sample(config, step_budget_s, max_rows=64):
+    """OracleSample whose step takes about step_budget_s on this host.  The
+    per-row cost comes from two small probes (1 and 4 rows of every
+    projection), so only one more sample is built; rows are capped, since
+    building a sample (generate, rotate, quantize in FP64) costs more than
+    stepping it."""
+    def timed(sample):
+        sample.step()
+        t0 = time.perf_counter()
+        sample.step()
+        return time.perf_counter() - t0
+
+    t1 = timed(OracleSample(config, 1, 1))
     if t1 > step_budget_s:
         return OracleSample(config, 1, int(np.ceil(t1 / step_budget_s)))
-    # per extra row the step grows by roughly the GEMV share; grow rows geometrically
-    rows = 1
-    while rows < 512:
-        trial = OracleSample(config, rows * 4, 1)
-        t0 = time.perf_counter()
-        trial.step()
-        if time.perf_counter() - t0 > step_budget_s:
-            break
-        rows *= 4
-    return OracleSample(config, rows, 1)
+    t4 = timed(OracleSample(config, 4, 1))
+    per_row = max((t4 - t1) / 3.0, 1e-6)
+    rows = int((step_budget_s - (t1 - per_row)) / per_row)
+    return OracleSample(config, max(1, min(max_rows, rows)), 1)
 
 
 def cpu_baseline(config, budget_s=15.0):
