@@ -550,7 +550,7 @@ def cpu_baseline(config, budget_s=15.0):
     """The oracle as it stands, timed on the host cores on a bounded sample."""
     import oracle
 
-    sample = _sized_sample(config, budget_s / 8)
+    sample = _sized_sample(config, budget_s / 8, max_rows=128)
     sample.step()
     reps, t0 = 0, time.perf_counter()
     while True:
