@@ -234,6 +234,37 @@ def test_device_entry_points_validate_before_any_cuda_call(kq):
     assert lib.kq_stream_read(A + 8, 1024, 4096, 4, A, None) == kq.KQ_ERR_ALIGNMENT
 
 
+def test_linked_plan_links_validated_before_any_cuda_call(kq):
+    """kq_decode_plan_create_linked checks every link on the host first:
+    its kind, that the source is an earlier matrix, the stage order, that an
+    output is read only by a later stage, k against the source's n (or its
+    k for a grouped matvec), a finite alpha and the reserved field."""
+    lib = kq.lib()
+    A = 1 << 20
+    m = lambda n, k: kq.kq_qmat(kq.KQ_Q8_0, 0, n, k, A, A)  # noqa: E731
+    h = ctypes.c_void_p()
+
+    def create(mats, links):
+        arr = (kq.kq_qmat * len(mats))(*mats)
+        la = (kq.kq_link * len(links))(*[kq.kq_link(*lk) for lk in links])
+        return lib.kq_decode_plan_create_linked(arr, la, len(mats), ctypes.byref(h))
+
+    P, I, O = 0, 1, 2
+    three = [m(256, 256), m(256, 256), m(256, 256)]
+    assert create(three, [(P, 0, 0, 1.0, 0), (I, 0, 0, 1.0, 0), (O, 0, 1, 1.0, 0)]) == kq.KQ_ERR_SHAPE  # own stage
+    assert create(three, [(P, 1, 0, 1.0, 0), (P, 0, 0, 1.0, 0), (P, 2, 0, 1.0, 0)]) == kq.KQ_ERR_SHAPE  # decreasing
+    assert create(three, [(P, 0, 0, 1.0, 0), (O, 1, 2, 1.0, 0), (P, 2, 0, 1.0, 0)]) == kq.KQ_ERR_INVALID_ARG  # later
+    assert create(three, [(P, 0, 0, 1.0, 0), (3, 1, 0, 1.0, 0), (P, 2, 0, 1.0, 0)]) == kq.KQ_ERR_INVALID_ARG  # kind
+    assert create(three, [(P, 0, 0, 1.0, 0), (O, 1, 0, float("nan"), 0), (P, 2, 0, 1.0, 0)]) == kq.KQ_ERR_INVALID_ARG
+    assert create(three, [(P, 0, 0, 1.0, 7), (P, 1, 0, 1.0, 0), (P, 2, 0, 1.0, 0)]) == kq.KQ_ERR_INVALID_ARG  # reserved
+    assert create(three, [(P, -1, 0, 1.0, 0), (P, 0, 0, 1.0, 0), (P, 1, 0, 1.0, 0)]) == kq.KQ_ERR_SHAPE  # stage < 0
+    wide = [m(256, 256), m(8, 512)]
+    assert create(wide, [(P, 0, 0, 1.0, 0), (O, 1, 0, 1.0, 0)]) == kq.KQ_ERR_SHAPE  # k above the source's n
+    assert create(wide, [(P, 0, 0, 1.0, 0), (I, 0, 0, 1.0, 0)]) == kq.KQ_ERR_SHAPE  # grouped k differs
+    arr = (kq.kq_qmat * 1)(m(256, 256))
+    assert lib.kq_decode_plan_create_linked(arr, None, 1, ctypes.byref(h)) == kq.KQ_ERR_INVALID_ARG
+
+
 def test_status_strings(kq):
     lib = kq.lib()
     for s in range(10):
