@@ -315,6 +315,18 @@ int kq_decode_plan_sizes(const kq_plan* plan, int64_t* x_floats, int64_t* y_floa
 size_t kq_decode_workspace_bytes(const kq_plan* plan);
 int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, void* d_ws, size_t ws_bytes,
                    void* stream);
+/* One step with the activations and outputs in host memory: enqueues on
+ * `stream` the copy of the plan's x_floats packed activations from
+ * h_x_packed to the device buffer d_x_packed, the step, and the copy of the
+ * y_floats outputs from d_y_packed back to h_y_packed (plain asynchronous
+ * copies: pinned host buffers overlap nothing but need no staging; the
+ * caller synchronises the stream before reading h_y_packed).
+ *  - d_x_packed, d_y_packed: device buffers of the plan's sizes, 16-byte
+ *    aligned, owned by the caller; h_x_packed may be NULL when x_floats is 0.
+ *  - Errors: those of kq_decode_step, checked before any copy; KQ_ERR_INVALID_ARG
+ *    for a NULL host buffer; KQ_ERR_CUDA if a copy cannot be enqueued. */
+int kq_decode_step_host(kq_plan* plan, const float* h_x_packed, float* h_y_packed, float* d_x_packed,
+                        float* d_y_packed, void* d_ws, size_t ws_bytes, void* stream);
 void kq_decode_plan_destroy(kq_plan* plan);
 
 /* Decode plans with the dependencies of a real decode step.  In a model's

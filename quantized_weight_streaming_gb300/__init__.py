@@ -114,6 +114,7 @@ SIGNATURES = {
     "kq_decode_plan_sizes": (ctypes.c_int, [_P, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
     "kq_decode_workspace_bytes": (_SZ, [_P]),
     "kq_decode_step": (ctypes.c_int, [_P, _P, _P, _P, _SZ, _P]),
+    "kq_decode_step_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _SZ, _P]),
     "kq_decode_plan_destroy": (None, [_P]),
     "kq_stream_read": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P]),
     "kq_device_status": (ctypes.c_int, [ctypes.c_int]),
@@ -430,6 +431,13 @@ class DecodePlan:
         p, nb = _ws(ws)
         _check(_lib.kq_decode_step(self.handle, _ptr(d_x_packed), _ptr(d_y_packed), p, nb, _stream(stream)),
                "kq_decode_step")
+
+    def step_host(self, h_x_packed, h_y_packed, d_x_packed, d_y_packed, ws=None, stream=None):
+        """kq_decode_step_host: host (ideally pinned) CPU tensors in and out,
+        through the given device buffers; asynchronous on `stream`."""
+        p, nb = _ws(ws)
+        _check(_lib.kq_decode_step_host(self.handle, _ptr(h_x_packed), _ptr(h_y_packed), _ptr(d_x_packed),
+                                        _ptr(d_y_packed), p, nb, _stream(stream)), "kq_decode_step_host")
 
     def close(self):
         if self.handle:

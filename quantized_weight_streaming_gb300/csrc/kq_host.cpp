@@ -8,6 +8,7 @@
 // (q-1)*d, d = max|w|, q = round(w/d)+1).  Rounding of w/d is half away from
 // zero, decided on the FP64 quotient of the two floats.
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstring>
@@ -338,6 +339,29 @@ int kq_rotate_blockwise_host(const float* in, float* out, int64_t rows, int64_t 
       for (int32_t i = 0; i < block; ++i) dst[i] = static_cast<float>(scale * v[i]);
     }
   }
+  return KQ_OK;
+}
+
+// One decode step with host buffers: the copies around kq_decode_step, on
+// the caller's stream (plain cudaMemcpyAsync; pinned buffers make them
+// asynchronous).  Uses the plan only through its public queries.
+int kq_decode_step_host(kq_plan* plan, const float* h_x_packed, float* h_y_packed, float* d_x_packed,
+                        float* d_y_packed, void* d_ws, size_t ws_bytes, void* stream) {
+  clear_error();
+  if (!plan) return fail(KQ_ERR_INVALID_ARG, "NULL plan");
+  int64_t xf = 0, yf = 0;
+  if (int s = kq_decode_plan_sizes(plan, &xf, &yf, nullptr)) return s;
+  if ((!h_x_packed && xf > 0) || !h_y_packed) return fail(KQ_ERR_INVALID_ARG, "NULL host buffer");
+  if ((!d_x_packed && xf > 0) || !d_y_packed) return fail(KQ_ERR_INVALID_ARG, "NULL device buffer");
+  if (!aligned16(d_x_packed) || !aligned16(d_y_packed)) return fail(KQ_ERR_ALIGNMENT, "x or y not 16-byte aligned");
+  const size_t need = kq_decode_workspace_bytes(plan);
+  if (need > 0 && (!d_ws || ws_bytes < need))
+    return fail(KQ_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, d_ws ? ws_bytes : (size_t)0);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (xf > 0)
+    KQ_CUDA_TRY(cudaMemcpyAsync(d_x_packed, h_x_packed, (size_t)xf * sizeof(float), cudaMemcpyHostToDevice, st));
+  if (int s = kq_decode_step(plan, d_x_packed, d_y_packed, d_ws, ws_bytes, stream)) return s;
+  KQ_CUDA_TRY(cudaMemcpyAsync(h_y_packed, d_y_packed, (size_t)yf * sizeof(float), cudaMemcpyDeviceToHost, st));
   return KQ_OK;
 }
 
