@@ -195,6 +195,42 @@ def test_gemv_matches_oracle(kq, wl, fmt, n, k):
     assert np.array_equal(_run_gemv(kq, W, x), y)
 
 
+@pytest.mark.parametrize("fmt", ["q8_0", "pq2_0", "scale4"])
+def test_gemv_at_k_32768(kq, wl, fmt):
+    """The largest K the tests use for a single GEMV (above a plan's staging
+    limit, so it is split): every row against the oracle."""
+    n, k = 40, 32768
+    sw, sx = synth.stream_id("test", 0, 311), synth.stream_id("test", 1, 311)
+    W = wl.build_matrix(fmt, n, k, 0, sw)
+    y = _run_gemv(kq, W, wl.build_activation(k, 0, sx))
+    _, _, y_ref, absdot = oracle.reference(fmt, synth.fill_host("w", n * k, 0, sw).reshape(n, k),
+                                           synth.fill_host("x", k, 0, sx))
+    ok, worst = oracle.within_bound(y, y_ref, absdot, TOL)
+    assert ok, worst
+
+
+@pytest.mark.parametrize("fmt,limit,block", [("q8_0", 18432, 32), ("pq2_0", 18432, 128), ("scale4", 16384, 32)])
+def test_decode_plan_at_its_staging_limit(kq, wl, fmt, limit, block):
+    """A plan accepts a matrix whose K is exactly the staging limit (every
+    row checked) and refuses one block more with KQ_ERR_UNSUPPORTED."""
+    n = 70
+    sw, sx = synth.stream_id("test", 0, 312), synth.stream_id("test", 1, 312)
+    W = wl.build_matrix(fmt, n, limit, 2, sw)
+    plan = kq.DecodePlan([W])
+    x = synth.fill_host("x", limit, 2, sx)
+    y = torch.empty(plan.y_floats, dtype=torch.float32, device="cuda")
+    plan.step(torch.from_numpy(x).cuda(), y)
+    _sync_ok(kq)
+    _, _, y_ref, absdot = oracle.reference(fmt, synth.fill_host("w", n * limit, 2, sw).reshape(n, limit), x)
+    ok, worst = oracle.within_bound(y.cpu().numpy(), y_ref, absdot, TOL)
+    assert ok, worst
+    plan.close()
+    big = wl.build_matrix(fmt, 8, limit + block, 2, sw)
+    with pytest.raises(kq.KQError) as e:
+        kq.DecodePlan([big])
+    assert e.value.status == kq.KQ_ERR_UNSUPPORTED
+
+
 def test_q8_0_exact_integer_case_tolerance_zero(kq):
     # integer codes, power-of-two scales, small integer activations: every
     # partial sum is an exact fp32 value, so the result must match exactly
