@@ -67,6 +67,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 // returns at once.
 __device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Lets the grid launched after this one on the stream as a programmatic
+// dependent begin: its CTAs take SMs as this grid's CTAs exit and run their
+// prologue, then wait in grid_dependency_wait until this grid has completed.
+// Every kernel of the library waits before its first global access, so the
+// trigger can come as early as right after that wait.
+__device__ __forceinline__ void allow_dependent_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Launches kernel k as a programmatic dependent of the stream's previous
 // kernel (the kernel must call grid_dependency_wait before reading that
 // kernel's outputs).

@@ -983,6 +983,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     fence_barrier_init();
   }
   __syncthreads();
+  // Launched as a programmatic dependent, the CTA got here while the kernel
+  // before it may still run: the weights, the activations and the outputs
+  // are touched only after it has completed.
+  grid_dependency_wait();
+  allow_dependent_launch();
 
   const int nst = LINKED ? p.nstages : 1;
 
@@ -1349,6 +1354,7 @@ template <bool OUT16 = false>
 __global__ void reduce_splits_kernel(const float* __restrict__ ws, float* __restrict__ y, int64_t n, int64_t ldy,
                                      int m, int splits) {
   grid_dependency_wait();  // the partials of the kernel before (a programmatic dependent launch)
+  allow_dependent_launch();
   const int64_t total = (int64_t)m * n;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t mm = i / n, row = i % n;
@@ -1497,8 +1503,10 @@ static int launch_stream(const Params& p, int grid, cudaStream_t st) {
   static char msg[160];
   if (int s = prepare_kernel_once(stream_kernel<FMT, M, false, IO16>, Geo<FMT>::kSmemBytes, once, status, msg))
     return s;
-  stream_kernel<FMT, M, false, IO16><<<grid, kThreads, Geo<FMT>::kSmemBytes, st>>>(p);
-  KQ_CUDA_TRY(cudaGetLastError());
+  // a programmatic dependent of the stream's previous kernel: its CTAs set up
+  // while that kernel's last CTAs finish
+  KQ_CUDA_TRY(launch_dependent(stream_kernel<FMT, M, false, IO16>, dim3(grid), dim3(kThreads),
+                               Geo<FMT>::kSmemBytes, st, p));
   return KQ_OK;
 }
 
