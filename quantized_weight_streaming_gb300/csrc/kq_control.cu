@@ -7,7 +7,7 @@
 // (cp.async.bulk, L2 evict-first) into a ring of shared-memory stages, and
 // sixteen consumer warps that read every 16-byte word of each stage back from
 // shared memory, fold it into an XOR and free the stage.  The achieved rate is
-// the in-harness ceiling that the GEMV kernels' bandwidth is judged against
+// the in-harness ceiling that the GEMV kernels' bandwidth is measured against
 // (the weight-bandwidth argument of "Kipp Benchmarks", "Decode is
 // weight-bandwidth-bound"; the Bonsai page's measured practical ceiling of a
 // read-only streaming kernel, section 8).
