@@ -321,6 +321,10 @@ int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, vo
  * y_floats outputs from d_y_packed back to h_y_packed (plain asynchronous
  * copies: pinned host buffers overlap nothing but need no staging; the
  * caller synchronises the stream before reading h_y_packed).
+ *  - A plan of one stage never reads its own outputs: when h_y_packed is
+ *    page-locked host memory (cudaHostAlloc / cudaHostRegister) whose device
+ *    mapping is 16-byte aligned, the step writes the outputs there directly
+ *    and d_y_packed is left unwritten (no copy back).
  *  - d_x_packed, d_y_packed: device buffers of the plan's sizes, 16-byte
  *    aligned, owned by the caller; h_x_packed may be NULL when x_floats is 0.
  *  - Errors: those of kq_decode_step, checked before any copy; KQ_ERR_INVALID_ARG

@@ -345,6 +345,11 @@ int kq_rotate_blockwise_host(const float* in, float* out, int64_t rows, int64_t 
 // One decode step with host buffers: the copies around kq_decode_step, on
 // the caller's stream (plain cudaMemcpyAsync; pinned buffers make them
 // asynchronous).  Uses the plan only through its public queries.
+//
+// A plan of one stage only writes its outputs (no matrix reads an earlier
+// one's), so when h_y is page-locked host memory the step stores them through
+// h_y's device mapping as each row block finishes, and the copy back after the
+// step disappears from the step's critical path.
 int kq_decode_step_host(kq_plan* plan, const float* h_x_packed, float* h_y_packed, float* d_x_packed,
                         float* d_y_packed, void* d_ws, size_t ws_bytes, void* stream) {
   clear_error();
@@ -357,9 +362,20 @@ int kq_decode_step_host(kq_plan* plan, const float* h_x_packed, float* h_y_packe
   const size_t need = kq_decode_workspace_bytes(plan);
   if (need > 0 && (!d_ws || ws_bytes < need))
     return fail(KQ_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, d_ws ? ws_bytes : (size_t)0);
+  int32_t stages = 0;
+  if (int s = kq_decode_plan_stages(plan, &stages, nullptr)) return s;
+  float* y_direct = nullptr;
+  if (stages == 1) {
+    cudaPointerAttributes pa{};
+    if (cudaPointerGetAttributes(&pa, h_y_packed) != cudaSuccess)
+      (void)cudaGetLastError();  // not a pointer the runtime knows: the copy back serves it
+    else if (pa.type == cudaMemoryTypeHost && pa.devicePointer && aligned16(pa.devicePointer))
+      y_direct = static_cast<float*>(pa.devicePointer);
+  }
   cudaStream_t st = (cudaStream_t)stream;
   if (xf > 0)
     KQ_CUDA_TRY(cudaMemcpyAsync(d_x_packed, h_x_packed, (size_t)xf * sizeof(float), cudaMemcpyHostToDevice, st));
+  if (y_direct) return kq_decode_step(plan, d_x_packed, y_direct, d_ws, ws_bytes, stream);
   if (int s = kq_decode_step(plan, d_x_packed, d_y_packed, d_ws, ws_bytes, stream)) return s;
   KQ_CUDA_TRY(cudaMemcpyAsync(h_y_packed, d_y_packed, (size_t)yf * sizeof(float), cudaMemcpyDeviceToHost, st));
   return KQ_OK;
