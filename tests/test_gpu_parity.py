@@ -887,15 +887,20 @@ def test_linked_plan_cuts_row_blocks_only_where_it_pays(kq, wl):
     plan.close()
 
 
-@pytest.mark.parametrize("linked", [False, True])
-def test_decode_step_host_matches_device_step(kq, wl, linked):
-    """kq_decode_step_host (host buffers in and out, copies on the stream)
-    gives bitwise the outputs of kq_decode_step on the same inputs."""
+@pytest.mark.parametrize("linked,pinned", [(False, True), (True, True), (False, False)])
+def test_decode_step_host_matches_device_step(kq, wl, linked, pinned):
+    """kq_decode_step_host (host buffers in and out) gives bitwise the outputs
+    of kq_decode_step on the same inputs: the one-stage plan with a pinned
+    output buffer (written by the kernel through its device mapping), the
+    plan with stages (copied back), and a pageable output buffer (copied
+    back)."""
     spec = [((300, 512), (0, 0, 0, 1.0)), ((200, 512), (1, 0, 0, 1.0)), ((64, 256), (2, 1, 0, 0.5))]
     mats = [wl.build_matrix("q8_0", n, k, 9, synth.stream_id("test", 0, 395 + i)) for i, ((n, k), _) in enumerate(spec)]
     plan = kq.DecodePlan(mats, [lk for _, lk in spec] if linked else None)
     xh = torch.from_numpy(synth.fill_host("x", plan.x_floats, 9, synth.stream_id("test", 1, 395))).pin_memory()
-    yh = torch.full((plan.y_floats,), float("nan"), dtype=torch.float32).pin_memory()
+    yh = torch.full((plan.y_floats,), float("nan"), dtype=torch.float32)
+    if pinned:
+        yh = yh.pin_memory()
     nb = plan.workspace_bytes
     ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
     dx = torch.empty(plan.x_floats, dtype=torch.float32, device="cuda")
