@@ -235,7 +235,10 @@ def _decode_measure(kq, wl_mod, config, steps, warmup, stream, sampler_gpu=None,
     xh.copy_(W.x.cpu())
     yh = torch.empty(W.y.numel(), dtype=torch.float32, pin_memory=True)
 
-    def e2e_step():  # the public host-buffer call: copy in, step, copy out, on one stream
+    # the public host-buffer call on one stream: the activations copied in, then the step,
+    # whose outputs reach the pinned yh (stored there by the kernel for a one-stage plan,
+    # copied back otherwise)
+    def e2e_step():
         W.plan.step_host(xh, yh, W.x, W.y, W.ws, stream=stream)
 
     for _ in range(3):
