@@ -414,6 +414,17 @@ def run_kq(args):
                          "frac_of_measured_hbm": round(r["gbs"] / peak, 4),
                          "frac_of_control": round(r["gbs"] / control["gbs"], 4), "weight_bytes": r["weight_bytes"],
                          "matrices": r["matrices"]}
+        # the same Bonsai step with the opt-in tcgen05 consumer of PQ2_0 at one row
+        kq.kq_set_pq2_0_consumer(kq.KQ_PQ2_0_TCGEN05)
+        try:
+            r = _decode_measure(kq, workloads, HEADLINE, max(3, args.steps // 4), args.warmup, stream, e2e=False)
+        finally:
+            kq.kq_set_pq2_0_consumer(kq.KQ_PQ2_0_MMA_SYNC)
+        more["bonsai_27b_pq2_0_step_tcgen05_consumer"] = {
+            "gbs": round(r["gbs"], 1), "us_per_step": round(r["per_step_s"] * 1e6, 2),
+            "frac_of_measured_hbm": round(r["gbs"] / peak, 4), "frac_of_control": round(r["gbs"] / control["gbs"], 4),
+            "kernel": "kq::tcs::tcs_kernel (tcgen05.mma kind::f8f6f4)", "weight_bytes": r["weight_bytes"],
+            "matrices": r["matrices"]}
         extras["decode_steps"].update(more)
         gemv = []
         for fmt, n, k, m in (("q8_0", 1024, 2560, 1), ("pq2_0", 10240, 5120, 1), ("q8_0", 9728, 2560, 1),

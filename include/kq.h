@@ -414,6 +414,28 @@ int kq_decode_plan_stages(const kq_plan* plan, int32_t* stages, int32_t* split_m
 int kq_stream_read(const void* d_src, int64_t bytes, int32_t stage_bytes, int32_t stages, uint32_t* d_sink,
                    void* stream);
 
+/* ---- PQ2_0 consumer at one activation row ------------------------------------ */
+
+/* Two consumers compute PQ2_0 products at one activation row (kq_gemv_pq2_0,
+ * kq_gemm_splitk and kq_gemm_splitk_noalloc with m = 1, and kq_decode_step of
+ * PQ2_0 plans without links); both give results within the same bound (the
+ * weights are never rounded) and are deterministic.
+ *  - KQ_PQ2_0_MMA_SYNC (the default): the streaming kernel's warp-level
+ *    tensor-core consumer (mma.sync, fp16 code values in registers, the
+ *    transformed activation as an fp16 high/low pair).
+ *  - KQ_PQ2_0_TCGEN05: a 5th-generation tensor-core consumer (tcgen05.mma
+ *    kind::f8f6f4): the codes masked into e4m3 values in tensor memory, the
+ *    transformed activation as four e4m3 planes (relative error 2^-16), one
+ *    MMA per 128 rows x 32 weights into per-block accumulators.  It needs
+ *    fewer integer operations per code but, measured on GB300, streams the
+ *    Bonsai-27B-shaped step slower than the default (its per-slot handoffs
+ *    between warps dominate), so it is opt-in.
+ * The setting is process-wide and applies to calls made after it returns.
+ * Errors: KQ_ERR_INVALID_ARG for an unknown value. */
+typedef enum { KQ_PQ2_0_MMA_SYNC = 0, KQ_PQ2_0_TCGEN05 = 1 } kq_pq2_0_consumer;
+int kq_set_pq2_0_consumer(int consumer);
+int kq_get_pq2_0_consumer(void);
+
 /* ---- device status --------------------------------------------------------- */
 
 /* binaryVersion (major*10 + minor) of the streaming kernel as loaded on the

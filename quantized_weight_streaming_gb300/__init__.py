@@ -118,6 +118,8 @@ SIGNATURES = {
     "kq_decode_plan_destroy": (None, [_P]),
     "kq_stream_read": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P]),
     "kq_device_status": (ctypes.c_int, [ctypes.c_int]),
+    "kq_set_pq2_0_consumer": (ctypes.c_int, [ctypes.c_int]),
+    "kq_get_pq2_0_consumer": (ctypes.c_int, []),
     "kq_kernel_binary_version": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int)]),
 }
 
@@ -398,6 +400,20 @@ def kq_stream_read(d_src, nbytes, d_sink, stage_bytes=34816, stages=4, stream=No
 
 def kq_device_status(clear=True):
     return _lib.kq_device_status(1 if clear else 0)
+
+
+KQ_PQ2_0_MMA_SYNC = 0
+KQ_PQ2_0_TCGEN05 = 1
+
+
+def kq_set_pq2_0_consumer(consumer):
+    """Selects the consumer of PQ2_0 products at one activation row
+    (KQ_PQ2_0_MMA_SYNC, the default, or KQ_PQ2_0_TCGEN05); process-wide."""
+    _check(_lib.kq_set_pq2_0_consumer(int(consumer)), "kq_set_pq2_0_consumer")
+
+
+def kq_get_pq2_0_consumer():
+    return _lib.kq_get_pq2_0_consumer()
 
 
 class DecodePlan:

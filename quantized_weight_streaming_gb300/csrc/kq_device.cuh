@@ -50,6 +50,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return done != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// suspended (for at most kSuspendNs, woken when the phase completes) instead of
+// returning at once, so waiting warps do not take issue slots from working ones.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return done != 0;
+}
+
+// Waits (suspended between checks) for the phase with the given parity to
+// complete; false after about one second.
+__device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait_suspend(bar, parity)) return true;
+  long long start = clock64();
+  while (!mbar_try_wait_suspend(bar, parity)) {
+    if (clock64() - start > kWaitLimitCycles) return false;
+  }
+  return true;
+}
+
 // Waits for the phase with the given parity to complete; false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -39,6 +39,21 @@ def wl(kq):
     return workloads
 
 
+@pytest.fixture(params=["mma_sync", "tcgen05"])
+def consumer(request, kq):
+    """Runs a PQ2_0 one-row test under each consumer (kq_set_pq2_0_consumer);
+    cases the setting does not touch (other formats, tcgen05 GEMM paths,
+    linked plans) run once, under the default."""
+    params = request.node.callspec.params
+    untouched = (params.get("fmt", "pq2_0") != "pq2_0" or params.get("config", "bonsai_27b_pq2_0_step").startswith("qwen")
+                 or params.get("path", "gemv") != "gemv" or params.get("linked", False))
+    if request.param == "tcgen05" and untouched:
+        pytest.skip("the consumer setting does not apply to this case")
+    kq.kq_set_pq2_0_consumer(kq.KQ_PQ2_0_TCGEN05 if request.param == "tcgen05" else kq.KQ_PQ2_0_MMA_SYNC)
+    yield request.param
+    kq.kq_set_pq2_0_consumer(kq.KQ_PQ2_0_MMA_SYNC)
+
+
 def _sync_ok(kq):
     torch.cuda.synchronize()
     assert kq.kq_device_status(True) == kq.KQ_OK
@@ -181,7 +196,7 @@ SHAPES = [
 
 
 @pytest.mark.parametrize("fmt,n,k", SHAPES)
-def test_gemv_matches_oracle(kq, wl, fmt, n, k):
+def test_gemv_matches_oracle(kq, consumer, wl, fmt, n, k):
     sw, sx = synth.stream_id("test", 0, 310), synth.stream_id("test", 1, 310)
     W = wl.build_matrix(fmt, n, k, 0, sw)
     x = wl.build_activation(k, 0, sx)
@@ -196,7 +211,7 @@ def test_gemv_matches_oracle(kq, wl, fmt, n, k):
 
 
 @pytest.mark.parametrize("fmt", ["q8_0", "pq2_0", "scale4"])
-def test_gemv_at_k_32768(kq, wl, fmt):
+def test_gemv_at_k_32768(kq, consumer, wl, fmt):
     """The largest K the tests use for a single GEMV (above a plan's staging
     limit, so it is split): every row against the oracle."""
     n, k = 40, 32768
@@ -210,7 +225,7 @@ def test_gemv_at_k_32768(kq, wl, fmt):
 
 
 @pytest.mark.parametrize("fmt,limit,block", [("q8_0", 18432, 32), ("pq2_0", 18432, 128), ("scale4", 16384, 32)])
-def test_decode_plan_at_its_staging_limit(kq, wl, fmt, limit, block):
+def test_decode_plan_at_its_staging_limit(kq, consumer, wl, fmt, limit, block):
     """A plan accepts a matrix whose K is exactly the staging limit (every
     row checked) and refuses one block more with KQ_ERR_UNSUPPORTED."""
     n = 70
@@ -268,7 +283,7 @@ def test_scale4_exact_integer_case_tolerance_zero(kq):
     assert np.array_equal(y3.astype(np.float64), y_ref)
 
 
-def test_pq2_0_nonzero_mean_activation(kq, wl):
+def test_pq2_0_nonzero_mean_activation(kq, consumer, wl):
     n, k = 96, 5120
     sw = synth.stream_id("test", 0, 311)
     W = wl.build_matrix("pq2_0", n, k, 0, sw)
@@ -280,7 +295,7 @@ def test_pq2_0_nonzero_mean_activation(kq, wl):
     assert ok, worst
 
 
-def test_pq2_0_activation_scale_extremes(kq, wl):
+def test_pq2_0_activation_scale_extremes(kq, consumer, wl):
     # per-block exponent normalisation: tiny and huge activations keep precision
     n, k = 32, 1024
     sw = synth.stream_id("test", 0, 312)
@@ -297,7 +312,7 @@ def test_pq2_0_activation_scale_extremes(kq, wl):
 
 
 @pytest.mark.parametrize("fmt,n,k", [("q8_0", 200, 9728), ("pq2_0", 120, 20480), ("pq2_0", 64, 5120)])
-def test_split_k(kq, wl, fmt, n, k):
+def test_split_k(kq, consumer, wl, fmt, n, k):
     sw, sx = synth.stream_id("test", 0, 320), synth.stream_id("test", 1, 320)
     W = wl.build_matrix(fmt, n, k, 1, sw)
     x = wl.build_activation(k, 1, sx)
@@ -475,7 +490,7 @@ def _single_weight_pq2_0(kq, n, k, d=2.0**-3):
 
 
 @pytest.mark.parametrize("path", ["gemv", "tc"])
-def test_pq2_0_single_weight_rows(kq, path):
+def test_pq2_0_single_weight_rows(kq, consumer, path):
     # row r holds one nonzero ternary weight: y[r] = +-d x'[col r], so the
     # bound 1e-4 * sum |w x'| is 1e-4 * d |x'[col r]|.  This pins the code
     # pairing and B permutation, and fails a kernel that forms sum c x' and
@@ -530,7 +545,7 @@ def test_stream_read_control_xor(kq, nbytes, stage_bytes, stages):
     assert not sink[1:].any()
 
 
-def test_decode_plan_small_mixed_shapes(kq, wl):
+def test_decode_plan_small_mixed_shapes(kq, consumer, wl):
     spec = [(16, 256), (33, 1024), (1, 5120), (300, 2048), (17, 17408), (64, 128)]
     for fmt in ("q8_0", "pq2_0", "scale4"):
         mats, xs, host = [], [], []
@@ -665,7 +680,7 @@ def test_device_signed_rotation_bit_identical_to_host(kq, wl):
 
 @pytest.mark.parametrize("n,k", [(300, 5120), (64, 17408), (1000, 1024), (40, 6144)])
 @pytest.mark.parametrize("with_signs", [True, False])
-def test_pq2_0_page_rotation_matches_oracle(kq, wl, n, k, with_signs):
+def test_pq2_0_page_rotation_matches_oracle(kq, consumer, wl, n, k, with_signs):
     """PQ2_0 with the page's n = 1024 rotation: device planes equal the
     oracle's bytes; the GEMV, the split GEMV, the streaming small-M path (the
     transform passes in the upper half of the staging buffer) and the
@@ -694,7 +709,7 @@ def test_pq2_0_page_rotation_matches_oracle(kq, wl, n, k, with_signs):
         assert ok, (m, worst)
 
 
-def test_decode_plans_with_page_rotation(kq, wl):
+def test_decode_plans_with_page_rotation(kq, consumer, wl):
     """Unlinked and linked plans over matrices of three K widths sharing one
     sign vector per width, as on the page."""
     widths = (5120, 6144, 17408)
@@ -888,7 +903,7 @@ def test_linked_plan_cuts_row_blocks_only_where_it_pays(kq, wl):
 
 
 @pytest.mark.parametrize("linked,pinned", [(False, True), (True, True), (False, False)])
-def test_decode_step_host_matches_device_step(kq, wl, linked, pinned):
+def test_decode_step_host_matches_device_step(kq, consumer, wl, linked, pinned):
     """kq_decode_step_host (host buffers in and out) gives bitwise the outputs
     of kq_decode_step on the same inputs: the one-stage plan with a pinned
     output buffer (written by the kernel through its device mapping), the
@@ -983,7 +998,7 @@ def test_linked_decode_step_full_size_sampled_rows(kq, wl, config):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("config", ["qwen3_4b_q8_0_step", "bonsai_27b_pq2_0_step"])
-def test_decode_step_full_size_sampled_rows(kq, wl, config):
+def test_decode_step_full_size_sampled_rows(kq, consumer, wl, config):
     W = wl.DecodeWorkload(config, seed=0)
     W.step()
     _sync_ok(kq)
