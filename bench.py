@@ -537,12 +537,17 @@ class OracleSample:
             o.gemv(deq, x64)
 
 
-def _sized_sample(config, step_budget_s, max_rows=64):
+# One sizing rule for every timing of the oracle (the reference arm and the
+# cpu_baseline leg): rows of every projection, as many as the step budget
+# allows, at most this many (building a sample costs more than stepping it).
+ORACLE_MAX_ROWS = 128
+
+
+def _sized_sample(config, step_budget_s, max_rows=ORACLE_MAX_ROWS):
     """OracleSample whose step takes about step_budget_s on this host.  The
     per-row cost comes from two small probes (1 and 4 rows of every
-    projection), so only one more sample is built; rows are capped, since
-    building a sample (generate, rotate, quantize in FP64) costs more than
-    stepping it."""
+    projection), so only one more sample is built; rows are capped at
+    max_rows."""
     def timed(sample):
         sample.step()
         t0 = time.perf_counter()
@@ -562,7 +567,7 @@ def cpu_baseline(config, budget_s=15.0):
     """The oracle as it stands, timed on the host cores on a bounded sample."""
     import oracle
 
-    sample = _sized_sample(config, budget_s / 8, max_rows=128)
+    sample = _sized_sample(config, budget_s / 8)
     sample.step()
     reps, t0 = 0, time.perf_counter()
     while True:

@@ -122,14 +122,18 @@ int64_t kq_scales_bytes(int fmt, int64_t n, int64_t k);
 
 /* ---- host quantizers (offline weight preparation, deterministic) ----------- */
 
-/* Q8_0 per row and 32-block: d = fp16(amax/127) (fp32 quotient, then round to
+/* Q8_0 ("Kipp Architecture", "Weight quantization": 32-weight blocks, an fp16
+ * scale against which the codes are quantized, value d*q).
+ * Per row and 32-block: d = fp16(amax/127) (fp32 quotient, then round to
  * nearest even), q = round-half-away-from-zero(w / float(d)) clamped to
  * [-127, 127]; a block whose fp16 scale is zero gets q = 0.  Output: n*k/32
  * blocks of 34 bytes (d little endian, then 32 int8), row-major.
  * Errors: KQ_ERR_SHAPE (k % 32), KQ_ERR_NONFINITE, KQ_ERR_RANGE. */
 int kq_quantize_q8_0(const float* w, int64_t n, int64_t k, void* blocks);
 
-/* PQ2_0 per row and 128-block of the ROTATED weights: d = fp16(max|w|), code =
+/* PQ2_0 ("Bonsai 2 27B", section 3.1 for the block, section 4.1 for the
+ * weights being rotated before they are quantized).
+ * Per row and 128-block of the ROTATED weights: d = fp16(max|w|), code =
  * round-half-away-from-zero(w / float(d)) clamped to [-1, 1], plus 1; a block
  * whose fp16 scale is zero gets code 1.  Output: n*k/128 blocks of 34 bytes.
  * Errors: KQ_ERR_SHAPE (k % 128), KQ_ERR_NONFINITE, KQ_ERR_RANGE. */
@@ -154,7 +158,9 @@ int kq_quantize_scale4(const float* w, int64_t n, int64_t k, void* blocks);
  * Errors: KQ_ERR_SHAPE (k % 128), KQ_ERR_NONFINITE, KQ_ERR_RANGE. */
 int kq_quantize_ptq1_0(const float* w_rot, int64_t n, int64_t k, void* blocks);
 
-/* Blockwise normalised Walsh-Hadamard transform of each row, on the host:
+/* Blockwise normalised Walsh-Hadamard transform of each row, on the host
+ * (R = H_n / sqrt(n), Sylvester natural order, block-diagonal along K:
+ * "Bonsai 2 27B", sections 4.1-4.2):
  * out[b*block + i] = (1/sqrt(block)) * sum_c H[i][c] in[b*block + c], with the
  * sum taken in FP64, one FP64 multiply, one rounding to fp32.  block is a
  * power of two dividing k.  in == out is allowed. */
@@ -162,7 +168,10 @@ int kq_hadamard_blockwise_host(const float* in, float* out, int64_t rows, int64_
 
 /* ---- device weight preparation ------------------------------------------- */
 
-/* Repack n*k/block AoS blocks (device memory, as produced by the host
+/* The device planes of a matrix ("Bonsai 2 27B", section 3.1: a block's qs
+ * bytes read as little-endian words are its code words; "Kipp
+ * Architecture": the 34-byte Q8_0 block).  Repack n*k/block AoS blocks
+ * (device memory, as produced by the host
  * quantizers) into the codes and scales planes.  fmt = KQ_PTQ1_0 reads
  * 28-byte PTQ1_0 blocks and writes the PQ2_0 planes of the same trits and
  * scales (a lossless transcode; the matrix is then a PQ2_0 matrix). */
@@ -216,14 +225,18 @@ int kq_rotate_blockwise(const float* d_in, float* d_out, int64_t rows, int64_t k
  * (split-K partials; 0 when the call needs none). */
 size_t kq_gemv_workspace_bytes(const kq_qmat* W, int64_t m);
 
-/* y[n] = W x for a Q8_0 matrix: d_x fp32 [k], d_y fp32 [n]. */
+/* y[n] = W x for a Q8_0 matrix: d_x fp32 [k], d_y fp32 [n].  The batch-1
+ * product that bounds decode, every weight streamed once ("Kipp Benchmarks",
+ * "Decode is weight-bandwidth-bound"). */
 int kq_gemv_q8_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
 
 /* y[n] = W x for a SCALE4 matrix: d_x fp32 [k], d_y fp32 [n]. */
 int kq_gemv_scale4(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
 
 /* y[n] = W' (R x) for a PQ2_0 matrix: d_x is the UNROTATED fp32 activation
- * [k]; the blockwise transform runs in the kernel's activation prologue. */
+ * [k]; the blockwise transform runs in the kernel's activation prologue (the
+ * activation side of every folded matmul: "Bonsai 2 27B", section 4.2; the
+ * ternary matvec of section 8.5). */
 int kq_gemv_pq2_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
 
 /* The fp16 chain of the Bonsai page, section 4.4 (its token-identity
@@ -235,7 +248,9 @@ int kq_gemv_pq2_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, si
  * aligned. */
 int kq_gemv_f16(const kq_qmat* W, const void* d_x, void* d_y, void* d_ws, size_t ws_bytes, void* stream);
 
-/* Y[m][n] = X[m][k] W^T (rotated per row for PQ2_0), X and Y row-major fp32,
+/* Batched decode / speculation: several activation rows against one weight
+ * stream ("Kipp Benchmarks", tensor matmul section).
+ * Y[m][n] = X[m][k] W^T (rotated per row for PQ2_0), X and Y row-major fp32,
  * 1 <= m <= 64.  From m = 16 on (and k <= 32768) this is kq_gemm_tc with an
  * automatic split; below, the streaming kernel applies each weight tile to
  * up to 4 activation rows per pass.  kq_gemv_workspace_bytes(W, m) sizes the
@@ -270,9 +285,10 @@ int kq_gemm_tc(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int32_
 size_t kq_gemm_tc_workspace_bytes(const kq_qmat* W, int64_t m, int32_t splits);
 
 /* GEMV/GEMM with an explicit split-K factor (1 = no split; 0 = automatic).
- * Splits are whole multiples of 1024 weights along K; the partial sums of
- * each split are added in split order by a second pass, so a given split
- * factor always gives bitwise the same result. */
+ * Splits are whole multiples of the format's tile chunk along K: 256
+ * weights (Q8_0), 512 (SCALE4), 1024 (PQ2_0); the partial sums of each split
+ * are added in split order by a second pass, so a given split factor always
+ * gives bitwise the same result. */
 int kq_gemm_splitk(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int32_t splits, void* d_ws,
                    size_t ws_bytes, void* stream);
 size_t kq_gemm_splitk_workspace_bytes(const kq_qmat* W, int64_t m, int32_t splits);
@@ -290,8 +306,10 @@ size_t kq_gemm_splitk_workspace_bytes(const kq_qmat* W, int64_t m, int32_t split
  *  - A split plan whose partials need more than the scratch is rejected with
  *    KQ_ERR_WORKSPACE before anything is enqueued.
  *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current; make that first call
- *    before any stream capture on the device.
+ *    (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ *    first call before any stream capture on the device.  The kept address
+ *    does not survive a device reset (cudaDeviceReset): do not call this
+ *    entry point again in a process after resetting a device it was used on.
  *  - Every call on a device shares the one array and leaves its partials in
  *    it; nothing in it has to start at zero (each call writes every partial
  *    it reads).  Calls that overlap on the GPU (different streams without
@@ -301,7 +319,10 @@ size_t kq_gemm_splitk_noalloc_max_bytes(void);
 
 /* ---- decode-step driver ---------------------------------------------------- */
 
-/* A plan for streaming a whole model's projection list once per step: count
+/* The decode step: a whole model's projection list streamed once per token
+ * ("Bonsai 2 27B", sections 8.5-8.7: the per-token matvec stream and the
+ * cost of dispatching it one kernel at a time).
+ * A plan for streaming a whole model's projection list once per step: count
  * matrices of one format.  Creating it copies the descriptors and a
  * per-SM schedule to device memory (the only allocation the plan makes);
  * kq_decode_step then runs the whole list in one persistent kernel.
@@ -313,6 +334,13 @@ int kq_decode_plan_create(const kq_qmat* mats, int64_t count, kq_plan** out);
 int kq_decode_plan_sizes(const kq_plan* plan, int64_t* x_floats, int64_t* y_floats, int64_t* weight_bytes);
 /* Workspace bytes of kq_decode_step (0 for a plan made by kq_decode_plan_create). */
 size_t kq_decode_workspace_bytes(const kq_plan* plan);
+/* One decode step: every matrix of the plan applied to its activation in one
+ * launch (the page's token of matvecs, "Bonsai 2 27B", section 8.5, without
+ * its per-matvec dispatches, sections 8.6-8.7).  d_x_packed / d_y_packed:
+ * 16-byte-aligned device buffers of the plan's sizes; d_ws: the plan's
+ * workspace (kq_decode_workspace_bytes; NULL when 0).  Asynchronous on
+ * `stream`.  Errors: KQ_ERR_INVALID_ARG (NULL plan or buffers),
+ * KQ_ERR_ALIGNMENT, KQ_ERR_WORKSPACE, KQ_ERR_CUDA. */
 int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, void* d_ws, size_t ws_bytes,
                    void* stream);
 /* One step with the activations and outputs in host memory: enqueues on
@@ -327,8 +355,10 @@ int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, vo
  *    and d_y_packed is left unwritten (no copy back).
  *  - d_x_packed, d_y_packed: device buffers of the plan's sizes, 16-byte
  *    aligned, owned by the caller; h_x_packed may be NULL when x_floats is 0.
- *  - Errors: those of kq_decode_step, checked before any copy; KQ_ERR_INVALID_ARG
- *    for a NULL host buffer; KQ_ERR_CUDA if a copy cannot be enqueued. */
+ *  - Errors: every argument check of kq_decode_step (and KQ_ERR_INVALID_ARG
+ *    for a NULL host buffer) runs before anything is enqueued.  KQ_ERR_CUDA
+ *    reports a copy or the step's launch that could not be enqueued; when
+ *    the launch fails, the activation copy may already be enqueued. */
 int kq_decode_step_host(kq_plan* plan, const float* h_x_packed, float* h_y_packed, float* d_x_packed,
                         float* d_y_packed, void* d_ws, size_t ws_bytes, void* stream);
 void kq_decode_plan_destroy(kq_plan* plan);

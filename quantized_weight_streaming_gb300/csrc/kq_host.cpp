@@ -362,6 +362,7 @@ int kq_decode_step_host(kq_plan* plan, const float* h_x_packed, float* h_y_packe
   const size_t need = kq_decode_workspace_bytes(plan);
   if (need > 0 && (!d_ws || ws_bytes < need))
     return fail(KQ_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, d_ws ? ws_bytes : (size_t)0);
+  if (need > 0 && !aligned16(d_ws)) return fail(KQ_ERR_ALIGNMENT, "workspace not 16-byte aligned");
   int32_t stages = 0;
   if (int s = kq_decode_plan_stages(plan, &stages, nullptr)) return s;
   float* y_direct = nullptr;

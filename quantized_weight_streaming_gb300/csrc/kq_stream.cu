@@ -1849,8 +1849,12 @@ static constexpr size_t kNoAllocScratchBytes = 2u << 20;  // 2 MiB per device
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
 
 static std::mutex g_noalloc_mutex;
-static std::vector<void*> g_noalloc_ptr;  // device address of the array, per device (host stand-in resolved once)
+static std::vector<void*> g_noalloc_ptr;  // device address of the array, per device
 
+// The array's device address on the current device.  In host code the
+// array's name is only a host-side stand-in, so its address is looked up
+// once per device (cudaGetSymbolAddress, with that device current; it
+// allocates nothing) and kept.  A device reset invalidates the kept address.
 static int noalloc_scratch(void** out) {
   int dev = 0;
   KQ_CUDA_TRY(cudaGetDevice(&dev));

@@ -77,6 +77,28 @@ def test_noalloc_matches_regular_entry_point_twice(kq, fmt, n, k, m, splits):
             assert ok, (call, i, worst)
 
 
+def test_noalloc_call_allocates_no_device_memory(kq):
+    """After a first call (which may load the library's device code on this
+    device), a call leaves the device's free memory (cudaMemGetInfo)
+    unchanged: nothing is allocated, by the library or by anything it calls."""
+    import workloads
+
+    n, k, m, splits = 640, 5120, 1, 4
+    W = workloads.build_matrix("pq2_0", n, k, 6, synth.stream_id("test", 0, 502))
+    X = workloads.build_activation(k, 6, synth.stream_id("test", 1, 502))
+    Y = torch.empty(m * n, dtype=torch.float32, device="cuda")
+    lib = kq.lib()
+    args = (ctypes.byref(W.desc), X.data_ptr(), m, Y.data_ptr(), splits, torch.cuda.current_stream().cuda_stream)
+    assert lib.kq_gemm_splitk_noalloc(*args) == kq.KQ_OK
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        assert lib.kq_gemm_splitk_noalloc(*args) == kq.KQ_OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert kq.kq_device_status(True) == kq.KQ_OK
+
+
 def test_noalloc_rejects_plans_beyond_its_scratch(kq):
     import workloads
 
