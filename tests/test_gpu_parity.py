@@ -410,6 +410,34 @@ def _run_tc(kq, W, X, m, splits):
     return Y.cpu().numpy().reshape(m, W.n)
 
 
+@pytest.mark.parametrize("fmt,n,k", [("q8_0", 300, 2080), ("scale4", 300, 2080), ("pq2_0", 200, 1152)])
+@pytest.mark.parametrize("m", [1, 3, 16, 33])
+def test_full_mantissa_activations(kq, wl, consumer, fmt, n, k, m):
+    """Activations with full 24-bit mantissas (not the generator's 2^-16
+    grid), each 32-block scaled by its own power of two in 2^-12 .. 2^12:
+    the fp16 high/low split of the tensor-core paths (m = 16, 33), the
+    per-block normalisation of the streaming consumers (m = 1, 3) and the
+    transform's rounding all see values they do not hold exactly."""
+    if m != 1 and consumer == "tcgen05":
+        pytest.skip("the consumer setting applies to one activation row")
+    sw = synth.stream_id("test", 0, 340)
+    W = wl.build_matrix(fmt, n, k, 3, sw)
+    w = synth.fill_host("w", n * k, 3, sw).reshape(n, k)
+    rng = np.random.default_rng(340 + m)
+    X = rng.standard_normal((m, k)).astype(np.float32)
+    X *= np.exp2(rng.integers(-12, 13, size=(m, k // 32))).repeat(32, axis=1).astype(np.float32)
+    assert np.count_nonzero(np.modf(X * np.float32(2.0 ** 16))[0]) > 0.9 * X.size  # off the 2^-16 grid
+    Xd = torch.from_numpy(X.reshape(-1)).cuda()
+    if m >= 16:
+        Y = _run_tc(kq, W, Xd, m, 0)
+    else:
+        Y = _run_gemv(kq, W, Xd, splits=0 if m == 1 else 2, m=m).reshape(m, n)
+    for i in range(m):
+        _, _, y_ref, absdot = oracle.reference(fmt, w, X[i])
+        ok, worst = oracle.within_bound(Y[i], y_ref, absdot, TOL)
+        assert ok, (i, worst)
+
+
 @pytest.mark.parametrize("fmt,n,k", [("q8_0", 300, 2080), ("pq2_0", 200, 1152), ("q8_0", 128, 128),
                                      ("pq2_0", 1, 128), ("q8_0", 1000, 4096), ("pq2_0", 520, 5120),
                                      ("scale4", 300, 2080), ("scale4", 1000, 4096), ("scale4", 1, 32)])

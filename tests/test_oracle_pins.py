@@ -534,6 +534,63 @@ def test_f16_chain_exact_integer_case():
     assert not slack.any()
 
 
+def _midpoint_case(x2):
+    """The page's n = 1024 rotation (no signs) divides by 32 exactly, so
+    R x is rational and can be placed on an fp16 rounding midpoint by hand.
+    x = (1024, 1/2, x2, 0, ...) in fp16: R x_j = (1024 + s1 / 2 + s2 x2) / 32
+    with s1 = (-1)^bit0(j), s2 = (-1)^bit1(j).  For even j that is
+    32 + 2^-6 +- x2 / 32: within x2 / 32 of the midpoint 32 + 2^-6 between the
+    fp16 values 32 and 32 + 2^-5 (fp16 step 2^-5 at 32, 2^-6 below it); for
+    odd j it is 32 - 2^-6 +- x2 / 32, next to the fp16 value 32 - 2^-6 and
+    half a step from any midpoint.  The weights are W = T R with T ternary
+    (+-1/8, 0): R R = I with exact FP64 arithmetic on these values, so the
+    rotated weights are T exactly and so is the dequantized matrix."""
+    n, k = 6, 1024
+    rng = np.random.default_rng(21)
+    t = rng.integers(-1, 2, size=(n, k)) * 0.125
+    t[:, ::128] = 0.125  # every 128-block has a nonzero weight: its scale is 1/8
+    w = (t @ scipy.linalg.hadamard(k) / 32.0).astype(np.float32)
+    assert np.array_equal(w.astype(np.float64), t @ scipy.linalg.hadamard(k) / 32.0)  # exact in fp32
+    x16 = np.zeros(k, dtype=np.float16)
+    x16[:3] = [1024.0, 0.5, x2]
+    assert float(x16[2]) == x2
+    y, absdot, slack, xp16 = oracle.f16_chain_reference("pq2_0", w, x16, had=1024)
+    return t, x16, y, absdot, slack, xp16
+
+
+@pytest.mark.parametrize("x2", [2.0 ** -14, 2.0 ** -11])
+def test_f16_chain_slack_at_an_fp16_midpoint(x2):
+    """R x lies x2 / 32 (2^-19 or 2^-16) from an fp16 midpoint at every even
+    j; the fp32 transform's error bound there is (log2 1024 + 3) 2^-24
+    sum|x| / 32 = 13 * 2^-24 * (1024.5 + x2) / 32, about 2.48e-5, so both
+    cases count as near.  Worked by hand: x'16_j is the exact value rounded
+    once (32 + 2^-5 when bit1(j) = 0, above the midpoint; 32 when bit1 = 1,
+    below it; 32 - 2^-6 for odd j); the fp16 step at a near position is
+    max(c - lo, hi - c) = 2^-5 (c = 32: neighbours 32 - 2^-6 and 32 + 2^-5;
+    c = 32 + 2^-5: 32 and 32 + 2^-4); so slack_i = 2^-5 sum_{j even} |T_ij|."""
+    t, x16, y, absdot, slack, xp16 = _midpoint_case(x2)
+    j = np.arange(1024)
+    b0, b1 = j & 1, (j >> 1) & 1
+    want16 = np.where(b0 == 0, np.where(b1 == 0, 32.0 + 2.0 ** -5, 32.0), 32.0 - 2.0 ** -6)
+    assert np.array_equal(xp16.astype(np.float64), want16)
+    want_slack = 2.0 ** -5 * np.abs(t[:, b0 == 0]).sum(axis=1)
+    assert np.array_equal(slack, want_slack)
+    assert np.array_equal(y, t @ want16)  # every term is a multiple of 2^-9: exact
+    assert np.array_equal(absdot, np.abs(t) @ want16)
+
+
+def test_f16_chain_no_slack_just_outside_the_bound():
+    """x2 = 2^-10: R x is 2^-15 = 3.05e-5 from the midpoint, just above the
+    error bound 13 * 2^-24 * (1024.5 + 2^-10) / 32 = 2.48e-5, so no position
+    counts as near and the slack is zero; x'16 is the same correctly rounded
+    transform."""
+    _, _, _, _, slack, xp16 = _midpoint_case(2.0 ** -10)
+    assert not slack.any()
+    j = np.arange(1024)
+    want16 = np.where(j & 1 == 0, np.where((j >> 1) & 1 == 0, 32.0 + 2.0 ** -5, 32.0), 32.0 - 2.0 ** -6)
+    assert np.array_equal(xp16.astype(np.float64), want16)
+
+
 def test_gemv_brute_force_4x128_pq2_0():
     w = synth.fill_host("w", 4 * 128, 9, synth.stream_id("test", 0, 9)).reshape(4, 128)
     x = synth.fill_host("x", 128, 9, synth.stream_id("test", 1, 9))
