@@ -361,6 +361,14 @@ def _control_measure(kq, nbytes, stream, reps=10):
             "bytes": nbytes, "by_ring": by_ring}
 
 
+def _head_kernel(args):
+    if args.workload == SECONDARY:
+        return "kq::stream_kernel<Q8_0,1> (one launch per step)"
+    if args.pq2_0_consumer == "tcgen05":
+        return "kq::tcs::tcs_kernel (tcgen05.mma kind::f8f6f4; one launch per step)"
+    return "kq::stream_kernel<PQ2_0,1> (one launch per step)"
+
+
 def run_kq(args):
     import torch
 
@@ -377,6 +385,8 @@ def run_kq(args):
     if ver != 103:
         raise SystemExit(f"refusing to measure: kernels loaded as sm_{ver}, not sm_103a")
     kq.kq_device_status(True)
+    if args.pq2_0_consumer == "tcgen05":  # the headline line under the opt-in consumer (profiling cases)
+        kq.kq_set_pq2_0_consumer(kq.KQ_PQ2_0_TCGEN05)
     stream = torch.cuda.current_stream()
     gpu_index = torch.cuda.current_device()
     head = _decode_measure(kq, workloads, args.workload, args.steps, args.warmup, stream, sampler_gpu=gpu_index,
@@ -458,15 +468,16 @@ def run_kq(args):
                    "matrices": head["matrices"], "weight_bytes": head["weight_bytes"],
                    "activation_bytes": head["activation_bytes"], "bytes_per_step": head["bytes_per_step"],
                    "l2": "inputs larger than L2 (weights streamed once per step, 50x the L2)",
-                   "parallelism": f"replicas x{world}", "seed": 0},
+                   "parallelism": f"replicas x{world}", "seed": 0, "pq2_0_consumer": args.pq2_0_consumer},
         "frac_of_measured_hbm": round(per_gpu_gbs / peak, 4),
         "frac_of_nominal_8tbs": round(per_gpu_gbs / 8000.0, 4),
         "frac_of_control": round(per_gpu_gbs / control["gbs"], 4) if control else None,
         "control": control,
         "roofline": {"bound": "hbm", "achieved": round(per_gpu_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(per_gpu_gbs / peak, 4),
-                     "traffic": args.traffic if args.traffic is not None else _traffic(args.workload),
-                     "peak_kind": peak_kind, "kernel": "kq::stream_kernel<PQ2_0,1> (one launch per step)"},
+                     "traffic": args.traffic if args.traffic is not None else (
+                         _traffic(args.workload) if "stream_kernel" in _head_kernel(args) else None),
+                     "peak_kind": peak_kind, "kernel": _head_kernel(args)},
         "e2e": {"value": round(head["e2e_gbs"] * world, 2), "unit": "GB/s", "h2d_bytes_per_step": head["h2d_bytes"],
                 "d2h_bytes_per_step": head["d2h_bytes"], "us_per_step": round(head["e2e_per_step_s"] * 1e6, 2)},
         "gpu_launches": args.steps,
@@ -679,6 +690,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--matrices", type=int, default=None,
                     help="only the first N projections of the workload (small profiling cases)")
+    ap.add_argument("--pq2-0-consumer", choices=("mma_sync", "tcgen05"), default="mma_sync",
+                    help="consumer of PQ2_0 products at one activation row for the headline line")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per launch of the stream kernel from an ncu capture (reported as is)")
     ap.add_argument("--profile-gemm", default=None, metavar="FMT,N,K,M",

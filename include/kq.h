@@ -347,11 +347,15 @@ int kq_decode_step(kq_plan* plan, const float* d_x_packed, float* d_y_packed, vo
  * `stream` the copy of the plan's x_floats packed activations from
  * h_x_packed to the device buffer d_x_packed, the step, and the copy of the
  * y_floats outputs from d_y_packed back to h_y_packed (plain asynchronous
- * copies: pinned host buffers overlap nothing but need no staging; the
- * caller synchronises the stream before reading h_y_packed).
+ * copies; the caller synchronises the stream before reading h_y_packed and
+ * leaves h_x_packed unchanged until then).
+ *  - When h_x_packed is page-locked host memory (cudaHostAlloc /
+ *    cudaHostRegister) whose device mapping is 16-byte aligned, the kernel
+ *    reads the activations through that mapping as it stages them, spread
+ *    over the step instead of a copy before it; d_x_packed is then left
+ *    unwritten.
  *  - A plan of one stage never reads its own outputs: when h_y_packed is
- *    page-locked host memory (cudaHostAlloc / cudaHostRegister) whose device
- *    mapping is 16-byte aligned, the step writes the outputs there directly
+ *    such page-locked memory, the step writes the outputs there directly
  *    and d_y_packed is left unwritten (no copy back).
  *  - d_x_packed, d_y_packed: device buffers of the plan's sizes, 16-byte
  *    aligned, owned by the caller; h_x_packed may be NULL when x_floats is 0.

@@ -350,6 +350,20 @@ int kq_rotate_blockwise_host(const float* in, float* out, int64_t rows, int64_t 
 // one's), so when h_y is page-locked host memory the step stores them through
 // h_y's device mapping as each row block finishes, and the copy back after the
 // step disappears from the step's critical path.
+// The device mapping of a page-locked host buffer (cudaHostAlloc or
+// cudaHostRegister) if it is 16-byte aligned, else nullptr (pageable memory:
+// the caller's copies serve it).
+static float* mapped_device_pointer(const float* h) {
+  cudaPointerAttributes pa{};
+  if (cudaPointerGetAttributes(&pa, h) != cudaSuccess) {
+    (void)cudaGetLastError();  // not a pointer the runtime knows
+    return nullptr;
+  }
+  if (pa.type == cudaMemoryTypeHost && pa.devicePointer && aligned16(pa.devicePointer))
+    return static_cast<float*>(pa.devicePointer);
+  return nullptr;
+}
+
 int kq_decode_step_host(kq_plan* plan, const float* h_x_packed, float* h_y_packed, float* d_x_packed,
                         float* d_y_packed, void* d_ws, size_t ws_bytes, void* stream) {
   clear_error();
@@ -365,19 +379,17 @@ int kq_decode_step_host(kq_plan* plan, const float* h_x_packed, float* h_y_packe
   if (need > 0 && !aligned16(d_ws)) return fail(KQ_ERR_ALIGNMENT, "workspace not 16-byte aligned");
   int32_t stages = 0;
   if (int s = kq_decode_plan_stages(plan, &stages, nullptr)) return s;
-  float* y_direct = nullptr;
-  if (stages == 1) {
-    cudaPointerAttributes pa{};
-    if (cudaPointerGetAttributes(&pa, h_y_packed) != cudaSuccess)
-      (void)cudaGetLastError();  // not a pointer the runtime knows: the copy back serves it
-    else if (pa.type == cudaMemoryTypeHost && pa.devicePointer && aligned16(pa.devicePointer))
-      y_direct = static_cast<float*>(pa.devicePointer);
-  }
+  // Page-locked host buffers with a 16-byte-aligned device mapping are read
+  // (x) or written (y, one-stage plans only: no stage reads them back) by the
+  // kernel itself, so no copy runs before or after it.
+  float* y_direct = stages == 1 ? mapped_device_pointer(h_y_packed) : nullptr;
+  const float* x_direct = xf > 0 ? mapped_device_pointer(h_x_packed) : nullptr;
   cudaStream_t st = (cudaStream_t)stream;
-  if (xf > 0)
+  if (xf > 0 && !x_direct)
     KQ_CUDA_TRY(cudaMemcpyAsync(d_x_packed, h_x_packed, (size_t)xf * sizeof(float), cudaMemcpyHostToDevice, st));
-  if (y_direct) return kq_decode_step(plan, d_x_packed, y_direct, d_ws, ws_bytes, stream);
-  if (int s = kq_decode_step(plan, d_x_packed, d_y_packed, d_ws, ws_bytes, stream)) return s;
+  const float* x_in = x_direct ? x_direct : d_x_packed;
+  if (y_direct) return kq_decode_step(plan, x_in, y_direct, d_ws, ws_bytes, stream);
+  if (int s = kq_decode_step(plan, x_in, d_y_packed, d_ws, ws_bytes, stream)) return s;
   KQ_CUDA_TRY(cudaMemcpyAsync(h_y_packed, d_y_packed, (size_t)yf * sizeof(float), cudaMemcpyDeviceToHost, st));
   return KQ_OK;
 }

@@ -589,6 +589,19 @@ __device__ __forceinline__ void pq2_0_tile(const uint8_t* st_codes, const uint16
   }
 }
 
+// Waits for the stage phase with the given parity: 0 once it completed, 1 if
+// another warp has aborted the kernel meanwhile, 2 after about one second.
+// The abort flag is read only while waiting, not once per tile.
+__device__ __forceinline__ int stage_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return 0;
+  const long long start = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (*abort_flag) return 1;
+    if (clock64() - start > kWaitLimitCycles) return 2;
+  }
+  return 0;
+}
+
 // ---------------------------------------------------------------------------
 // The persistent streaming kernel.
 // ---------------------------------------------------------------------------
@@ -796,10 +809,12 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         ring_par ^= 1u;
       }
       const int64_t k0 = sbeg + (int64_t)ci * F::kChunk;
-      if (*abort_flag) continue;
-      if (!mbar_wait_bounded(&full[s], par)) {
-        *abort_flag = 1;
-        stream_flag(KQ_ERR_TIMEOUT);
+      const int wr = stage_wait(&full[s], par, abort_flag);
+      if (wr != 0) {  // another warp aborted (1), or this wait ran out (2)
+        if (wr == 2) {
+          *abort_flag = 1;
+          stream_flag(KQ_ERR_TIMEOUT);
+        }
         continue;
       }
       const uint8_t* st = stages + (size_t)s * kStageBytes;

@@ -930,27 +930,31 @@ def test_linked_plan_cuts_row_blocks_only_where_it_pays(kq, wl):
     plan.close()
 
 
-@pytest.mark.parametrize("linked,pinned", [(False, True), (True, True), (False, False)])
-def test_decode_step_host_matches_device_step(kq, consumer, wl, linked, pinned):
+@pytest.mark.parametrize("fmt", ["q8_0", "pq2_0"])
+@pytest.mark.parametrize("linked,pinned", [(False, True), (True, True), (False, False), (True, False)])
+def test_decode_step_host_matches_device_step(kq, consumer, wl, fmt, linked, pinned):
     """kq_decode_step_host (host buffers in and out) gives bitwise the outputs
-    of kq_decode_step on the same inputs: the one-stage plan with a pinned
-    output buffer (written by the kernel through its device mapping), the
-    plan with stages (copied back), and a pageable output buffer (copied
-    back)."""
-    spec = [((300, 512), (0, 0, 0, 1.0)), ((200, 512), (1, 0, 0, 1.0)), ((64, 256), (2, 1, 0, 0.5))]
-    mats = [wl.build_matrix("q8_0", n, k, 9, synth.stream_id("test", 0, 395 + i)) for i, ((n, k), _) in enumerate(spec)]
+    of kq_decode_step on the same inputs.  Pinned buffers: the kernel reads
+    the activations through their device mapping (the device buffer d_x is
+    left untouched) and a one-stage plan writes its outputs there; a plan
+    with stages copies its outputs back.  Pageable buffers: both copies."""
+    spec = [((300, 1024), (0, 0, 0, 1.0)), ((200, 1024), (1, 0, 0, 1.0)), ((64, 256), (2, 1, 0, 0.5))]
+    if fmt == "pq2_0":
+        spec[2] = ((64, 128), (2, 1, 0, 0.5))
+    mats = [wl.build_matrix(fmt, n, k, 9, synth.stream_id("test", 0, 395 + i)) for i, ((n, k), _) in enumerate(spec)]
     plan = kq.DecodePlan(mats, [lk for _, lk in spec] if linked else None)
-    xh = torch.from_numpy(synth.fill_host("x", plan.x_floats, 9, synth.stream_id("test", 1, 395))).pin_memory()
+    xh = torch.from_numpy(synth.fill_host("x", plan.x_floats, 9, synth.stream_id("test", 1, 395)))
     yh = torch.full((plan.y_floats,), float("nan"), dtype=torch.float32)
     if pinned:
-        yh = yh.pin_memory()
+        xh, yh = xh.pin_memory(), yh.pin_memory()
     nb = plan.workspace_bytes
     ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda") if nb else None
-    dx = torch.empty(plan.x_floats, dtype=torch.float32, device="cuda")
+    dx = torch.full((plan.x_floats,), float("nan"), dtype=torch.float32, device="cuda")
     dy = torch.empty(plan.y_floats, dtype=torch.float32, device="cuda")
     plan.step_host(xh, yh, dx, dy, ws)
     torch.cuda.synchronize()
     _sync_ok(kq)
+    assert torch.isnan(dx).all() == pinned  # read in place when pinned, copied in otherwise
     y2 = torch.empty(plan.y_floats, dtype=torch.float32, device="cuda")
     plan.step(xh.cuda(), y2, ws)
     _sync_ok(kq)
