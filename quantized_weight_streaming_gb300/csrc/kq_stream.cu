@@ -61,62 +61,50 @@ __device__ unsigned int g_stream_status = 0;
 __device__ __forceinline__ void stream_flag(int status) { atomicOr(&g_stream_status, 1u << status); }
 
 // A linked plan's activation slice x[kbeg, kbeg + len) (one row), alpha
-// applied, as plain fp32 into dst.  Each thread keeps four float4 fetches in
-// flight; a cut row block of the source is the sum of its partials in slot
-// order, one pass per slot, so the loads of a pass are independent.  The
-// arithmetic equals load_x4's: ((p0 + p1) + ...) * alpha.
+// applied, as plain fp32 into dst.  A thread takes one float4 of the slice
+// per pass; a cut row block of the source is the sum of its partials in slot
+// order, with up to 4 of them loaded at once, so a block cut n ways costs
+// ceil(n / 4) round trips rather than n.  The arithmetic equals load_x4's:
+// ((p0 + p1) + ...) * alpha.
+// t_first: the source row block of the thread's first float4, read by the
+// caller ahead of time (see first_tile).
 template <int TR>
-__device__ __forceinline__ void gather_slice(const XSrc& xs, int64_t kbeg, int len, float* dst, int tid) {
+__device__ __forceinline__ void gather_slice(const XSrc& xs, int64_t kbeg, int len, float* dst, int tid,
+                                             TileOut t_first) {
   constexpr int kT = 32 * kConsumerWarps;
+  constexpr int kS = 4;  // partial loads in flight
   const int n4 = len / 4;
-  for (int i0 = tid; i0 < n4; i0 += 4 * kT) {
-    float4 r[4];
-    const float* pb[4];
-    int ns[4];
-    int nmax = 0;
+  for (int i = tid; i < n4; i += kT) {
+    const int64_t g = kbeg + 4 * (int64_t)i;
+    const TileOut t = i == tid ? t_first : (xs.tiles ? xs.tiles[g / TR] : TileOut{0, 1, 0});
+    float4 r;
+    if (t.nseg > 1) {
+      const float* pb = xs.parts + t.part + g % TR;
+      r = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int q0 = 0; q0 < t.nseg; q0 += kS) {
+        float4 u[kS];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * kT;
-      ns[u] = 0;
-      pb[u] = nullptr;
-      r[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < n4) {
-        const int64_t g = kbeg + 4 * (int64_t)i;
-        const TileOut t = xs.tiles ? xs.tiles[g / TR] : TileOut{0, 1, 0};
-        if (t.nseg > 1) {
-          ns[u] = t.nseg;
-          pb[u] = xs.parts + t.part + g % TR;
-          r[u] = __ldcg(reinterpret_cast<const float4*>(pb[u]));
-        } else {
-          ns[u] = 1;
-          const float* b = xs.base + g;
-          r[u] = xs.vec4 ? __ldcg(reinterpret_cast<const float4*>(b))
-                         : make_float4(__ldcg(b), __ldcg(b + 1), __ldcg(b + 2), __ldcg(b + 3));
-        }
-        nmax = max(nmax, ns[u]);
+        for (int q = 0; q < kS; ++q)
+          if (q0 + q < t.nseg) u[q] = __ldcg(reinterpret_cast<const float4*>(pb + (int64_t)(q0 + q) * TR));
+#pragma unroll
+        for (int q = 0; q < kS; ++q)
+          if (q0 + q < t.nseg) {
+            if (q0 + q == 0) {
+              r = u[q];
+            } else {
+              r.x += u[q].x;
+              r.y += u[q].y;
+              r.z += u[q].z;
+              r.w += u[q].w;
+            }
+          }
       }
+    } else {
+      const float* b = xs.base + g;
+      r = xs.vec4 ? __ldcg(reinterpret_cast<const float4*>(b))
+                  : make_float4(__ldcg(b), __ldcg(b + 1), __ldcg(b + 2), __ldcg(b + 3));
     }
-    for (int q = 1; q < nmax; ++q) {
-      float4 t[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (q < ns[u]) t[u] = __ldcg(reinterpret_cast<const float4*>(pb[u] + (int64_t)q * TR));
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (q < ns[u]) {
-          r[u].x += t[u].x;
-          r[u].y += t[u].y;
-          r[u].z += t[u].z;
-          r[u].w += t[u].w;
-        }
-    }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int i = i0 + u * kT;
-      if (i < n4)
-        *reinterpret_cast<float4*>(dst + 4 * i) =
-            make_float4(r[u].x * xs.alpha, r[u].y * xs.alpha, r[u].z * xs.alpha, r[u].w * xs.alpha);
-    }
+    *reinterpret_cast<float4*>(dst + 4 * i) = make_float4(r.x * xs.alpha, r.y * xs.alpha, r.z * xs.alpha, r.w * xs.alpha);
   }
 }
 
@@ -209,9 +197,17 @@ __device__ __forceinline__ int btab4_index(int b, int j, int n, int t) {
 // rounded to fp16 right after the transform (the fp16 chain).
 __device__ __forceinline__ float round_f16(float v) { return __half2float(__float2half_rn(v)); }
 
+// The source row block that holds float4 `tid` of a linked gather from kbeg
+// (the plan's tables only: it can be read before the source stage is done).
+template <int TR>
+__device__ __forceinline__ TileOut first_tile(const XSrc& xs, int64_t kbeg, int64_t kend, int tid) {
+  const int64_t g = kbeg + 4 * (int64_t)tid;
+  return xs.tiles && g < kend ? xs.tiles[g / TR] : TileOut{0, 1, 0};
+}
+
 template <int FMT, int M, bool IO16 = false, bool LINKED = false>
 __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int xlen_pad, float* xbuf, float* fx,
-                                 float* sx, float* scratch, int cw, int lane) {
+                                 float* sx, float* scratch, int cw, int lane, TileOut t_first = TileOut{0, 1, 0}) {
   constexpr int kTR = LINKED ? Geo<FMT>::kTileRows : 0;  // a linked source's row blocks
   const int len = (int)(kend - kbeg);
   constexpr int kT = 32 * kConsumerWarps;
@@ -221,7 +217,7 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
   constexpr bool kGather = LINKED && FMT != KQ_Q8_0;
   static_assert(!kGather || M == 1, "linked plans have one activation row");
   if constexpr (kGather) {
-    gather_slice<Geo<FMT>::kTileRows>(xs, kbeg, len, xbuf, cw * 32 + lane);
+    gather_slice<Geo<FMT>::kTileRows>(xs, kbeg, len, xbuf, cw * 32 + lane, t_first);
     named_barrier(1, kConsumerWarps * 32);
   }
 
@@ -229,7 +225,8 @@ __device__ void stage_activation(const XSrc& xs, int64_t kbeg, int64_t kend, int
     float4* xb4 = reinterpret_cast<float4*>(xbuf);
     for (int m = 0; m < M; ++m) {
       for (int i = cw * 32 + lane; i < len / 4; i += kT)
-        xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] = load_x4<IO16, kTR>(xs, m, kbeg + 4 * i);
+        xb4[m * (xlen_pad / 4) + q8_swz4(4 * i)] =
+            load_x4<IO16, kTR>(xs, m, kbeg + 4 * i, LINKED && i == cw * 32 + lane ? &t_first : nullptr);
     }
   } else if (FMT == KQ_SCALE4) {
     // A warp takes 128 positions (four 32-blocks, eight lanes per block) at a
@@ -774,6 +771,11 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
     const int32_t key = LINKED ? p.links[cur.j].x_key : cur.j;
     if (key != cached_key || range != cached_range) {
       const XLink lk = LINKED ? p.links[cur.j] : XLink{-1, -1, cur.j, 1.f};
+      // where the activation comes from and, for a linked source, the row
+      // block of this thread's first float4: plan tables only, read here so
+      // that their loads overlap the wait for the source stage
+      const XSrc xs = make_xsrc(p, cur.j, job, lk);
+      const TileOut t_first = LINKED ? first_tile<kTileRows>(xs, sbeg, send, cw * 32 + lane) : TileOut{0, 1, 0};
       xlen_pad = (int)(((send - sbeg) + F::kChunk - 1) / F::kChunk * F::kChunk);
       if (LINKED && lk.dep_stage > ready) {  // the activation is an output of an earlier stage
         if (cw == 0 && lane == 0 && !*abort_flag && !wait_stage(p, lk.dep_stage)) {
@@ -783,8 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) stream_kernel(const __grid_consta
         ready = lk.dep_stage;
       }
       named_barrier(1, kConsumerWarps * 32);  // everyone is done with the previous slice
-      stage_activation<FMT, M, IO16, LINKED>(make_xsrc(p, cur.j, job, lk), sbeg, send, xlen_pad, xbuf, fx, sx,
-                                             scratch, cw, lane);
+      stage_activation<FMT, M, IO16, LINKED>(xs, sbeg, send, xlen_pad, xbuf, fx, sx, scratch, cw, lane, t_first);
       named_barrier(1, kConsumerWarps * 32);
       cached_key = key;
       cached_range = range;

@@ -276,12 +276,13 @@ struct XSrc {
 // x[i..i+3] of activation row m; loads bypass L1 (the source may have been
 // written by other CTAs of this launch).  TR > 0: a linked plan's source
 // output in row blocks of TR rows, where a cut block is read as the sum of
-// its partials in slot order (i % 4 == 0, so the four share a block).
+// its partials in slot order (i % 4 == 0, so the four share a block);
+// `known`, when given, is that block's entry, already read.
 template <bool IO16 = false, int TR = 0>
-__device__ __forceinline__ float4 load_x4(const XSrc& xs, int m, int64_t i) {
+__device__ __forceinline__ float4 load_x4(const XSrc& xs, int m, int64_t i, const TileOut* known = nullptr) {
   if constexpr (TR > 0) {
     if (xs.tiles) {
-      const TileOut t = xs.tiles[i / TR];
+      const TileOut t = known ? *known : xs.tiles[i / TR];
       if (t.nseg > 1) {
         // up to eight partials loaded at once, then added in slot order
         const float* b = xs.parts + t.part + i % TR;
