@@ -450,9 +450,10 @@ class DecodePlan:
 
     def step_host(self, h_x_packed, h_y_packed, d_x_packed, d_y_packed, ws=None, stream=None):
         """kq_decode_step_host: host (ideally pinned) CPU tensors in and out,
-        through the given device buffers; asynchronous on `stream`.  A
-        one-stage plan writes a pinned h_y_packed directly (d_y_packed is then
-        left unwritten)."""
+        through the given device buffers; asynchronous on `stream`.  A pinned
+        h_x_packed is read by the kernel in place (d_x_packed is then left
+        unwritten), and a one-stage plan writes a pinned h_y_packed directly
+        (d_y_packed is then left unwritten)."""
         p, nb = _ws(ws)
         _check(_lib.kq_decode_step_host(self.handle, _ptr(h_x_packed), _ptr(h_y_packed), _ptr(d_x_packed),
                                         _ptr(d_y_packed), p, nb, _stream(stream)), "kq_decode_step_host")

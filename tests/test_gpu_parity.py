@@ -962,6 +962,30 @@ def test_decode_step_host_matches_device_step(kq, consumer, wl, fmt, linked, pin
     plan.close()
 
 
+def test_decode_step_host_misaligned_pinned_buffers_are_copied(kq, wl):
+    """Page-locked host buffers whose device mapping is not 16-byte aligned
+    are served by copies (the kernel's in-place path needs 16-byte rows):
+    d_x is written, and the outputs still equal kq_decode_step's bit for bit."""
+    mats = [wl.build_matrix("pq2_0", n, k, 9, synth.stream_id("test", 0, 398 + i))
+            for i, (n, k) in enumerate([(300, 1024), (96, 512)])]
+    plan = kq.DecodePlan(mats)
+    xbig = torch.empty(plan.x_floats + 1, dtype=torch.float32).pin_memory()
+    ybig = torch.full((plan.y_floats + 1,), float("nan"), dtype=torch.float32).pin_memory()
+    xh, yh = xbig[1:], ybig[1:]  # 4 bytes past a 16-byte boundary
+    xh.copy_(torch.from_numpy(synth.fill_host("x", plan.x_floats, 9, synth.stream_id("test", 1, 398))))
+    dx = torch.full((plan.x_floats,), float("nan"), dtype=torch.float32, device="cuda")
+    dy = torch.empty(plan.y_floats, dtype=torch.float32, device="cuda")
+    plan.step_host(xh, yh, dx, dy, None)
+    torch.cuda.synchronize()
+    _sync_ok(kq)
+    assert torch.equal(dx.cpu(), xh)  # copied in
+    y2 = torch.empty(plan.y_floats, dtype=torch.float32, device="cuda")
+    plan.step(xh.cuda(), y2, None)
+    _sync_ok(kq)
+    assert torch.equal(yh, y2.cpu())
+    plan.close()
+
+
 def test_linked_plan_rejects_bad_links(kq, wl):
     mats = [wl.build_matrix("q8_0", 256, 256, 1, synth.stream_id("test", 0, 380 + i)) for i in range(3)]
     bad = [
