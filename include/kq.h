@@ -448,6 +448,17 @@ int kq_decode_plan_stages(const kq_plan* plan, int32_t* stages, int32_t* split_m
 int kq_stream_read(const void* d_src, int64_t bytes, int32_t stage_bytes, int32_t stages, uint32_t* d_sink,
                    void* stream);
 
+/* Self-test of the library's bounded device waits (an addition of this
+ * library, no counterpart on the pages).  Enqueues on `stream` one CTA whose
+ * thread waits, with the same bounded wait every kernel here uses, on an
+ * mbarrier phase that nothing completes; after limit_cycles SM clock cycles
+ * (1 .. about 2e9, one second) the wait gives up and KQ_ERR_TIMEOUT is
+ * recorded for kq_device_status, exactly as when a kernel's copy or peer
+ * never arrives.  The kernel then returns: nothing faults or hangs, and the
+ * GPU context stays usable.  Errors: KQ_ERR_INVALID_ARG (limit out of
+ * range), KQ_ERR_CUDA (launch). */
+int kq_selftest_bounded_wait(int64_t limit_cycles, void* stream);
+
 /* ---- PQ2_0 consumer at one activation row ------------------------------------ */
 
 /* Two consumers compute PQ2_0 products at one activation row (kq_gemv_pq2_0,

@@ -117,6 +117,7 @@ SIGNATURES = {
     "kq_decode_step_host": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _SZ, _P]),
     "kq_decode_plan_destroy": (None, [_P]),
     "kq_stream_read": (ctypes.c_int, [_P, _I64, _I32, _I32, _P, _P]),
+    "kq_selftest_bounded_wait": (ctypes.c_int, [_I64, _P]),
     "kq_device_status": (ctypes.c_int, [ctypes.c_int]),
     "kq_set_pq2_0_consumer": (ctypes.c_int, [ctypes.c_int]),
     "kq_get_pq2_0_consumer": (ctypes.c_int, []),
@@ -389,6 +390,10 @@ def kq_gemm_splitk_noalloc(W, d_X, m, d_Y, splits, stream=None):
 
 def kq_gemm_splitk_noalloc_max_bytes():
     return _lib.kq_gemm_splitk_noalloc_max_bytes()
+
+
+def kq_selftest_bounded_wait(limit_cycles, stream=None):
+    _check(_lib.kq_selftest_bounded_wait(int(limit_cycles), _stream(stream)), "kq_selftest_bounded_wait")
 
 
 def kq_stream_read(d_src, nbytes, d_sink, stage_bytes=34816, stages=4, stream=None):

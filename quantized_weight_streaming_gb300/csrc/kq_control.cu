@@ -103,6 +103,19 @@ __global__ void __launch_bounds__(kCtlThreads, 1)
   if (lane == 0 && acc) atomicXor(sink, acc);
 }
 
+// Self-test of the bounded waits: one thread waits on an mbarrier whose phase
+// nothing completes, with the library's bounded wait and a short limit, and
+// records KQ_ERR_TIMEOUT as every kernel of the library does when a wait
+// runs out.  No fault, no hang: the wait gives up and the kernel returns.
+__global__ void wait_selftest_kernel(long long limit_cycles) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    if (!mbar_wait_bounded(&bar, 0, limit_cycles)) atomicOr(&g_control_status, 1u << KQ_ERR_TIMEOUT);
+  }
+}
+
 int read_control_status(int clear) {
   unsigned int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_control_status, sizeof(v)) != cudaSuccess) return -1;
@@ -143,6 +156,16 @@ extern "C" int kq_stream_read(const void* d_src, int64_t bytes, int32_t stage_by
   const int grid = (int)std::min<int64_t>(nchunks, sms);
   stream_read_kernel<<<grid, kCtlThreads, smem, (cudaStream_t)stream>>>(static_cast<const uint8_t*>(d_src), bytes,
                                                                        stage_bytes, stages, d_sink);
+  KQ_CUDA_TRY(cudaGetLastError());
+  return KQ_OK;
+}
+
+extern "C" int kq_selftest_bounded_wait(int64_t limit_cycles, void* stream) {
+  clear_error();
+  if (limit_cycles < 1 || limit_cycles > kWaitLimitCycles)
+    return fail(KQ_ERR_INVALID_ARG, "limit_cycles = %lld (1 .. %lld)", (long long)limit_cycles,
+                (long long)kWaitLimitCycles);
+  wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((long long)limit_cycles);
   KQ_CUDA_TRY(cudaGetLastError());
   return KQ_OK;
 }

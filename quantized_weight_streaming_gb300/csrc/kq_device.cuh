@@ -77,12 +77,14 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint64_t* bar, uint32_t parity
   return true;
 }
 
-// Waits for the phase with the given parity to complete; false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Waits for the phase with the given parity to complete; false once
+// limit_cycles SM clock cycles have passed (about one second by default).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  long long limit_cycles = kWaitLimitCycles) {
   if (mbar_try_wait(bar, parity)) return true;
   long long start = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - start > kWaitLimitCycles) return false;
+    if (clock64() - start > limit_cycles) return false;
   }
   return true;
 }

@@ -201,6 +201,8 @@ def test_device_entry_points_validate_before_any_cuda_call(kq):
     assert lib.kq_decode_plan_create(mixed, 0, ctypes.byref(h)) == kq.KQ_ERR_SHAPE
     assert lib.kq_decode_step(None, A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
     assert lib.kq_decode_step_host(None, A, A, A, A, None, 0, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_selftest_bounded_wait(0, None) == kq.KQ_ERR_INVALID_ARG
+    assert lib.kq_selftest_bounded_wait(1 << 40, None) == kq.KQ_ERR_INVALID_ARG
     assert lib.kq_gemv_workspace_bytes(ctypes.byref(bad_k), 1) == 0
     h1024 = kq.kq_qmat(kq.KQ_PQ2_0, 1024, 8, 1536, A, A)  # k not a multiple of the rotation block
     assert lib.kq_gemv_pq2_0(ctypes.byref(h1024), A, A, None, 0, None) == kq.KQ_ERR_SHAPE

@@ -986,6 +986,26 @@ def test_decode_step_host_misaligned_pinned_buffers_are_copied(kq, wl):
     plan.close()
 
 
+def test_bounded_wait_timeout_is_reported_and_the_context_stays_usable(kq, wl):
+    """A bounded device wait that runs out (an mbarrier phase that nothing
+    completes, given up after ~1e6 cycles) is reported as KQ_ERR_TIMEOUT by
+    kq_device_status, which then reads clean; the context keeps working: a
+    GEMV afterwards matches the oracle."""
+    assert kq.kq_device_status(True) == kq.KQ_OK
+    kq.kq_selftest_bounded_wait(1_000_000)
+    assert kq.kq_device_status(True) == kq.KQ_ERR_TIMEOUT
+    assert kq.kq_device_status(True) == kq.KQ_OK  # cleared
+    n, k = 300, 1024
+    sw, sx = synth.stream_id("test", 0, 399), synth.stream_id("test", 1, 399)
+    W = wl.build_matrix("pq2_0", n, k, 9, sw)
+    x = wl.build_activation(k, 9, sx)
+    y = _run_gemv(kq, W, x)
+    _, _, y_ref, absdot = oracle.reference("pq2_0", synth.fill_host("w", n * k, 9, sw).reshape(n, k),
+                                           synth.fill_host("x", k, 9, sx))
+    ok, worst = oracle.within_bound(y, y_ref, absdot, TOL)
+    assert ok, worst
+
+
 def test_linked_plan_rejects_bad_links(kq, wl):
     mats = [wl.build_matrix("q8_0", 256, 256, 1, synth.stream_id("test", 0, 380 + i)) for i in range(3)]
     bad = [
