@@ -986,6 +986,45 @@ def test_decode_step_host_misaligned_pinned_buffers_are_copied(kq, wl):
     plan.close()
 
 
+@pytest.mark.parametrize("seed", range(4))
+def test_random_shapes_every_path_matches_oracle(kq, wl, seed):
+    """Seeded random cases: format, ragged n, k a random number of blocks
+    (ragged chunk tails), activation rows m and the entry point (GEMV, forced
+    split-K, small-M routing, the tensor-core GEMM with forced splits), every
+    row against the oracle."""
+    rng = np.random.default_rng(7000 + seed)
+    for case in range(6):
+        fmt = str(rng.choice(["q8_0", "pq2_0", "scale4"]))
+        block = 128 if fmt == "pq2_0" else 32
+        n = int(rng.integers(1, 900))
+        k = block * int(rng.integers(1, (48 if fmt == "pq2_0" else 160) + 1))
+        path = str(rng.choice(["gemv", "splitk", "small_m", "tc"]))
+        m = 1 if path == "gemv" else int(rng.choice([1, 2, 3, 4, 5, 16, 33, 64]))
+        splits = int(rng.integers(0, 4))
+        sw, sx = synth.stream_id("test", 0, 7100 + 10 * seed + case), synth.stream_id("test", 1, 7100 + 10 * seed + case)
+        W = wl.build_matrix(fmt, n, k, 11, sw)
+        X = wl.build_activation(k, 11, sx, rows=m)
+        if path == "gemv":
+            Y = _run_gemv(kq, W, X).reshape(1, n)
+        elif path == "splitk":
+            Y = _run_gemv(kq, W, X, splits=splits, m=m).reshape(m, n)
+        elif path == "small_m":
+            Yd = torch.empty(m * n, dtype=torch.float32, device="cuda")
+            nb = kq.kq_gemv_workspace_bytes(W, m)
+            ws = torch.empty(max(nb, 16), dtype=torch.uint8, device="cuda")
+            kq.kq_gemm_small_m(W, X, m, Yd, ws)
+            _sync_ok(kq)
+            Y = Yd.cpu().numpy().reshape(m, n)
+        else:
+            Y = _run_tc(kq, W, X, m, splits)
+        w = synth.fill_host("w", n * k, 11, sw).reshape(n, k)
+        Xh = synth.fill_host("x", m * k, 11, sx).reshape(m, k)
+        for i in range(m):
+            _, _, y_ref, absdot = oracle.reference(fmt, w, Xh[i])
+            ok, worst = oracle.within_bound(Y[i], y_ref, absdot, TOL)
+            assert ok, (fmt, n, k, path, m, splits, i, worst)
+
+
 def test_bounded_wait_timeout_is_reported_and_the_context_stays_usable(kq, wl):
     """A bounded device wait that runs out (an mbarrier phase that nothing
     completes, given up after ~1e6 cycles) is reported as KQ_ERR_TIMEOUT by
