@@ -574,6 +574,39 @@ def _sized_sample(config, step_budget_s, max_rows=ORACLE_MAX_ROWS):
     return OracleSample(config, max(1, min(max_rows, rows)), 1)
 
 
+def _step_bytes(config):
+    """Algorithmic bytes of one whole step of a workload: packed weights (codes and
+    fp16 scales) plus fp32 activations read and outputs written."""
+    import synth
+
+    total = 0
+    for _, fmt, n, k in synth.workload(config):
+        bs = 128 if fmt == synth.PQ2_0 else 32
+        code = {synth.PQ2_0: n * k // 4, synth.Q8_0: n * k, synth.SCALE4: n * k // 2}[fmt]
+        total += code + 2 * n * (k // bs) + 4 * (n + k)
+    return total
+
+
+def _cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+
+    return platform.machine()
+
+
 def cpu_baseline(config, budget_s=15.0):
     """The oracle as it stands, timed on the host cores on a bounded sample."""
     import oracle
@@ -589,7 +622,8 @@ def cpu_baseline(config, budget_s=15.0):
             break
     per = el / reps
     out = {"value": round(sample.bytes / per / 1e9, 5), "unit": "GB/s", "cores": oracle.max_threads(),
-           "kind": "oracle",
+           "kind": "oracle", "cpu_model": _cpu_model(),
+           "s_per_step_equivalent": round(per * _step_bytes(config) / sample.bytes, 1),
            "sample": f"{sample.describe()}, {reps} timed passes of {per * 1e3:.1f} ms each "
                      f"(FP64 dequantize + transform + GEMV)"}
     # the same code on one core, on a sample sized for it
@@ -648,7 +682,7 @@ def run_reference(args):
         "config": {"workload": args.workload, "sample_rows_per_matrix": rows, "sample_matrix_stride": sample.stride,
                    "parallelism": "host cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "kind": "oracle", "cores": oracle.max_threads(),
-                         "sample": desc},
+                         "cpu_model": _cpu_model(), "sample": desc},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
