@@ -317,7 +317,7 @@ def _gemv_graph_measure(kq, wl_mod, fmt, n, k, m, stream, replays=20):
     torch.cuda.synchronize()
     per_launch = start.elapsed_time(end) / 1e3 / (replays * len(mats))
     nbytes = W0.weight_bytes + 4 * m * (k + n)
-    if m >= 16:  # kq_gemm_small_m runs the tensor-core GEMM: prologue, GEMM, split second pass
+    if m >= (9 if fmt == "scale4" else 5):  # kq_gemm_small_m runs the tensor-core GEMM: prologue, GEMM, split pass
         split = kq.kq_gemm_tc_workspace_bytes(W0, m, 0) > kq.kq_gemm_tc_workspace_bytes(W0, m, 1)
         path, launches = "tcgen05", 2 + (1 if split else 0)
     else:

@@ -251,10 +251,11 @@ int kq_gemv_f16(const kq_qmat* W, const void* d_x, void* d_y, void* d_ws, size_t
 /* Batched decode / speculation: several activation rows against one weight
  * stream ("Kipp Benchmarks", tensor matmul section).
  * Y[m][n] = X[m][k] W^T (rotated per row for PQ2_0), X and Y row-major fp32,
- * 1 <= m <= 64.  From m = 16 on (and k <= 32768) this is kq_gemm_tc with an
- * automatic split; below, the streaming kernel applies each weight tile to
- * up to 4 activation rows per pass.  kq_gemv_workspace_bytes(W, m) sizes the
- * workspace of either. */
+ * 1 <= m <= 64.  From m = 5 on (m = 9 for SCALE4), when k <= 32768, this is
+ * kq_gemm_tc with an automatic split: it reads the weights once at any m.
+ * Below, the streaming kernel applies each weight tile to up to 4 activation
+ * rows per pass.  kq_gemv_workspace_bytes(W, m) sizes the workspace of
+ * either. */
 int kq_gemm_small_m(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, void* d_ws, size_t ws_bytes,
                     void* stream);
 

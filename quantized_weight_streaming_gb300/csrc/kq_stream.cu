@@ -1717,9 +1717,11 @@ static int launch_plan(const Params& p, int grid, bool cooperative, cudaStream_t
 
 extern "C" {
 
-// kq_gemm_small_m runs on the tensor cores from kTcMinM activation rows on
+// kq_gemm_small_m runs on the tensor cores from tc_min_m activation rows on
 // (when k fits the tensor-core prologue), else on the streaming kernel.
-static bool small_m_uses_tc(const kq_qmat* W, int64_t m) { return m >= kTcMinM && m <= kTcMaxM && W->k <= kTcMaxK; }
+static bool small_m_uses_tc(const kq_qmat* W, int64_t m) {
+  return m >= tc_min_m(W->fmt) && m <= kTcMaxM && W->k <= kTcMaxK;
+}
 
 size_t kq_gemv_workspace_bytes(const kq_qmat* W, int64_t m) {
   if (check_qmat(W, -1) != KQ_OK || m < 1) return 0;

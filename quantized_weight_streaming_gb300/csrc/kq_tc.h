@@ -10,7 +10,11 @@ namespace kq {
 
 constexpr int kTcMaxM = 64;      // activation rows per call (B holds 2 x 64 fp16 rows)
 constexpr int kTcMaxK = 32768;   // the activation prologue stages one fp32 row in shared memory
-constexpr int kTcMinM = 16;      // kq_gemm_small_m uses the tensor cores from this many rows on
+// kq_gemm_small_m uses the tensor cores from this many rows on: the
+// streaming kernel reads the weights once per 4 rows, the tensor-core GEMM
+// once at any M, so it wins from the second streaming pass on (Q8_0, PQ2_0);
+// scale4's streaming passes are half as long, so from the third.
+constexpr int tc_min_m(int fmt) { return fmt == KQ_SCALE4 ? 9 : 5; }
 
 // Validates m and k for the tensor-core path (the descriptor is checked by the caller).
 int tc_check(const kq_qmat* W, int64_t m);
