@@ -19,10 +19,11 @@
 //      warp 0       TMA producer: per chunk the codes of 128 rows, their
 //                   scales (a 16-byte box per row) and two 64-wide
 //                   128-byte-swizzled boxes of B;
-//      warp 1       allocates tensor memory; one thread issues tcgen05.mma
+//      warp 1       allocates tensor memory and issues tcgen05.mma
 //                   (kind::f16, M = 128, N = 2M', K = 16, A from tensor
-//                   memory, B from shared memory) and commits;
-//      warps 18-19  for PQ2_0, two more issuing threads: issuer g % 3 takes
+//                   memory, B from shared memory) and the commits: the warp
+//                   walks the list in step, one elected lane issues;
+//      warps 18-19  for PQ2_0, two more issuing warps: issuer g % 3 takes
 //                   the CTA's chunk g and owns accumulator buffer g % 3;
 //      warps 2-9    unpack the chunk into the A operand in tensor memory
 //                   (tcgen05.st): lane i of a warp owns weight row i of its
@@ -50,7 +51,9 @@
 //    small N one thread, not the tensor pipe, would set the pace.  PQ2_0 has
 //    three issuers that take whole chunks in turn and never wait for one
 //    another; Q8_0 and SCALE4 keep one, as their four accumulator blocks per
-//    chunk leave tensor memory for only three chunks' accumulators.
+//    chunk leave tensor memory for only three chunks' accumulators.  When a
+//    chunk's blocks share one accumulator group (M' = 16), their MMA chains
+//    are issued alternately (step t of every block, then step t + 1).
 //  * The unpack -> issuer barrier is per stage slot and waited on with the
 //    stage's phase right after that slot's tma_full, so an issuer that skips
 //    the other issuers' chunks can never take another chunk's phase for its
@@ -437,20 +440,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     }
   } else if (warp == 1 || warp >= kIssuer2Warp) {
     // ------------------------------ MMA issuers -------------------------------
+    // The whole warp walks the list in uniform control flow and waits; one
+    // elected lane issues the MMAs and commits (warp-uniform issue measured
+    // about twice as fast per MMA as a loop run by lane 0 alone).
     const int me = warp == 1 ? 0 : warp - kIssuer2Warp + 1;
-    if (lane == 0 && me < NI) {
+    if (me < NI) {
       const uint32_t idesc = idesc_f16(kRows, 2 * MP);
       Ring ring, dring, ar;  // the stage and A buffer of every chunk; this issuer's accumulator buffers
       int g = 0;
-      for (int item = ib; item < ie && !*abort_flag; ++item) {
+      bool stop = false;
+      for (int item = ib; item < ie && !stop; ++item) {
         const int split = item / p.tiles;
         const int c0 = chunk_begin(split), c1 = chunk_begin(split + 1);
-        for (int c = c0; c < c1 && !*abort_flag; ++c, ++g, ring.next(nstages), ar.next(na)) {
+        for (int c = c0; c < c1; ++c, ++g, ring.next(nstages), ar.next(na)) {
           if (g % NI != me) continue;
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+            stop = true;
+            break;
+          }
           const int slot = ring.slot, ab = ar.slot;
-          if (!mbar_wait_bounded(&tma_full[slot], ring.phase) ||
-              !mbar_wait_bounded(&a_full[slot], ring.phase)) {
-            fail_wait();
+          const bool got = mbar_wait_bounded(&tma_full[slot], ring.phase) && mbar_wait_bounded(&a_full[slot], ring.phase);
+          if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) fail_wait();
+            stop = true;
             break;
           }
           tc_fence_after();
@@ -459,38 +471,74 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           // descriptors of the two B boxes; a K step adds its 32-byte offset (>> 4) to the start field
           const uint64_t bd0 = sw128_desc(bt), bd1 = sw128_desc(bt + b_box_bytes(MP));
           bool ok = true;
+          if (kBlocks > 1 && gb == kBlocks) {
+            // one accumulator group per chunk: the blocks' chains alternate
+            const int dslot = me * ndi + dring.slot;
+            const bool free = mbar_wait_bounded(&d_empty[dslot], dring.phase ^ 1u);
+            if (!__all_sync(0xffffffffu, free)) {
+              if (lane == 0) fail_wait();
+              stop = true;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d0 = tmem_base + tmem_d + (uint32_t)(dslot * gb * 2 * MP);
+            if (elect_one()) {
+#pragma unroll
+              for (int t = 0; t < kSteps; ++t)
+#pragma unroll
+                for (int b = 0; b < kBlocks; ++b) {
+                  const int kk = b * kSteps + t;
+                  const int atom = kk >> 2, sub = (kk & 3) * 32;
+                  tc_mma_ts(d0 + (uint32_t)(b * 2 * MP), a_tmem + (uint32_t)(kk * 8),
+                            (atom ? bd1 : bd0) + (uint64_t)(sub >> 4), idesc, t > 0 ? 1u : 0u);
+                }
+              tc_commit(&d_full[dslot]);
+            }
+            __syncwarp();
+            dring.next(ndi);
+          } else
           for (int b = 0; b < kBlocks; ++b) {
             const int bg = b % gb;
             const int dslot = me * ndi + dring.slot;
             if (bg == 0) {
-              if (!mbar_wait_bounded(&d_empty[dslot], dring.phase ^ 1u)) {
-                fail_wait();
+              const bool free = mbar_wait_bounded(&d_empty[dslot], dring.phase ^ 1u);
+              if (!__all_sync(0xffffffffu, free)) {
+                if (lane == 0) fail_wait();
                 ok = false;
                 break;
               }
               tc_fence_after();
             }
             const uint32_t d_tmem = tmem_base + tmem_d + (uint32_t)((dslot * gb + bg) * 2 * MP);
+            if (elect_one()) {
 #pragma unroll
-            for (int t = 0; t < kSteps; ++t) {
-              const int kk = b * kSteps + t;
-              const int atom = kk >> 2, sub = (kk & 3) * 32;
-              tc_mma_ts(d_tmem, a_tmem + (uint32_t)(kk * 8), (atom ? bd1 : bd0) + (uint64_t)(sub >> 4), idesc,
-                        t > 0 ? 1u : 0u);
+              for (int t = 0; t < kSteps; ++t) {
+                const int kk = b * kSteps + t;
+                const int atom = kk >> 2, sub = (kk & 3) * 32;
+                tc_mma_ts(d_tmem, a_tmem + (uint32_t)(kk * 8), (atom ? bd1 : bd0) + (uint64_t)(sub >> 4), idesc,
+                          t > 0 ? 1u : 0u);
+              }
+              if (bg == gb - 1) tc_commit(&d_full[dslot]);
             }
-            if (bg == gb - 1) {
-              tc_commit(&d_full[dslot]);
-              dring.next(ndi);
-            }
+            __syncwarp();
+            if (bg == gb - 1) dring.next(ndi);
           }
-          if (!ok) break;
-          tc_commit(&a_empty[ab]);
-          tc_commit(&tma_empty[slot]);
+          if (!ok) {
+            stop = true;
+            break;
+          }
+          if (elect_one()) {
+            tc_commit(&a_empty[ab]);
+            tc_commit(&tma_empty[slot]);
+          }
+          __syncwarp();
         }
       }
-      // wait until every MMA this thread issued has completed
-      tc_commit(&drain[me]);
-      (void)mbar_wait_bounded(&drain[me], 0);
+      // wait until every MMA this warp issued has completed
+      if (elect_one()) tc_commit(&drain[me]);
+      __syncwarp();
+      if (lane == 0) (void)mbar_wait_bounded(&drain[me], 0);
+      __syncwarp();
     }
   } else if (warp < 2 + kDeqWarps) {
     // ------------------------------ unpack ----------------------------------
