@@ -81,7 +81,7 @@ namespace tc {
 
 constexpr int kRows = 128;     // W rows per tile (MMA M)
 constexpr int kChunk = 128;    // weights per K chunk
-constexpr int kMaxStages = 6;  // TMA ring depth limit
+constexpr int kMaxStages = 8;  // TMA ring depth limit
 constexpr int kMaxD = 4;       // accumulator buffers in tensor memory
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 8;
@@ -662,6 +662,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
             // this chunk's block scales of row r, from its 16-byte box
             const __half* srow = reinterpret_cast<const __half*>(st + off_scales + r * 16);
             const int s0 = kBlocks == 4 ? 4 * (c & 1) : (c & 7);
+            float dsc[kBlocks];
+#pragma unroll
+            for (int b = 0; b < kBlocks; ++b) dsc[b] = __half2float(srow[s0 + b]);
+            // the scales are in registers: the epilogue is done with the stage
+            // (the unpack warps and the MMA commit release it too)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tma_empty[ring.slot]);
+#pragma unroll
             for (int b = 0; b < kBlocks; ++b) {
               const int bg = b % gb;
               // one issuer: a ring over the buffers; several: buffer `me`, its (g / NI)-th use
@@ -674,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 }
                 tc_fence_after();
               }
-              const float d = __half2float(srow[s0 + b]);
+              const float d = dsc[b];
               const uint32_t t0 = d_lane + (uint32_t)((dslot * gb + bg) * 2 * MP);
 #pragma unroll
               for (int g = 0; g < 32; g += 8) {
@@ -694,8 +702,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
                 if (NI == 1) dr0.next(nd);
               }
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tma_empty[ring.slot]);
           }
         }
         ring.next(nstages);
