@@ -306,6 +306,122 @@ __global__ void act_hilo_kernel(const float* __restrict__ X, int m, int mp, int6
   }
 }
 
+// ---- epilogue role ------------------------------------------------------------------
+
+// What the epilogue warps need from the kernel's set-up.
+struct EpiCtx {
+  const uint8_t* stages;
+  uint64_t* tma_full;
+  uint64_t* tma_empty;
+  uint64_t* d_full;
+  uint64_t* d_empty;
+  volatile int* abort_flag;
+  int sbytes, off_scales, nstages, gb, nd, ib, ie, mp;
+  uint32_t d_lane;  // this warp's lane quarter and first activation column in the accumulators
+  int r, i0;        // this lane's tile row; this warp's first activation row
+};
+
+// The epilogue warps: per chunk, the block scales of row r from the stage
+// (then the stage is released), then per block d * (hi + lo) of the warp's
+// HALF activation columns added into registers.  The accumulator loads are
+// batched to few tensor-memory round trips: two blocks per wait at HALF = 8
+// (their group holds all four blocks of the chunk), sixteen columns (hi and
+// lo) per wait otherwise.
+template <int FMT, int HALF>
+__device__ __forceinline__ void epilogue_role(const TcParams& p, const EpiCtx& e, int lane) {
+  constexpr int kBlocks = blocks_per_chunk(FMT);
+  constexpr int NI = kBlocks == 1 ? kMaxIssuers : 1;
+  constexpr int kSeg = HALF >= 16 ? 16 : 8;                      // columns per load (hi and lo each)
+  constexpr int kPair = (HALF == 8 && kBlocks >= 2) ? 2 : 1;     // blocks per wait
+  const int MP = e.mp, gb = e.gb;
+  Ring ring, dr0;  // stages; the accumulator buffers (one issuer)
+  int g = 0;       // the chunk's place in this CTA's list (its issuer is g % NI)
+  for (int item = e.ib; item < e.ie; ++item) {
+    const int split = item / p.tiles, tile = item - split * p.tiles;
+    const int c0 = (int)((int64_t)split * p.chunks / p.splits), c1 = (int)((int64_t)(split + 1) * p.chunks / p.splits);
+    const int64_t row = (int64_t)tile * kRows + e.r;
+    float acc[HALF];
+#pragma unroll
+    for (int q = 0; q < HALF; ++q) acc[q] = 0.f;
+    for (int c = c0; c < c1; ++c, ++g) {
+      if (!*e.abort_flag) {
+        if (!mbar_wait_bounded(&e.tma_full[ring.slot], ring.phase)) {
+          *e.abort_flag = 1;
+          tc_flag(KQ_ERR_TIMEOUT);
+        } else {
+          const uint8_t* st = e.stages + (size_t)ring.slot * e.sbytes;
+          const int me = g % NI;
+          // this chunk's block scales of row r, from its 16-byte box
+          const __half* srow = reinterpret_cast<const __half*>(st + e.off_scales + e.r * 16);
+          const int s0 = kBlocks == 4 ? 4 * (c & 1) : (c & 7);
+          float dsc[kBlocks];
+#pragma unroll
+          for (int b = 0; b < kBlocks; ++b) dsc[b] = __half2float(srow[s0 + b]);
+          // the scales are in registers: the epilogue is done with the stage
+          // (the unpack warps and the MMA commit release it too)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&e.tma_empty[ring.slot]);
+#pragma unroll
+          for (int b = 0; b < kBlocks; b += kPair) {
+            const int bg = b % gb;
+            // one issuer: a ring over the buffers; several: buffer `me`, its (g / NI)-th use
+            const int dslot = NI == 1 ? dr0.slot : me;
+            const uint32_t dphase = NI == 1 ? dr0.phase : (uint32_t)((g / NI) & 1);
+            if (bg == 0) {
+              if (!mbar_wait_bounded(&e.d_full[dslot], dphase)) {
+                *e.abort_flag = 1;
+                tc_flag(KQ_ERR_TIMEOUT);
+                break;
+              }
+              tc_fence_after();
+            }
+            const uint32_t t0 = e.d_lane + (uint32_t)((dslot * gb + bg) * 2 * MP);
+#pragma unroll
+            for (int c8 = 0; c8 < HALF; c8 += kSeg) {
+              constexpr int kW = kSeg;
+              const int w = HALF - c8 < kW ? HALF - c8 : kW;  // 8 or 16 columns in this segment
+              float vh[kPair][kW], vl[kPair][kW];
+#pragma unroll
+              for (int pb = 0; pb < kPair; ++pb) {
+                const uint32_t tb = t0 + (uint32_t)(pb * 2 * MP);
+                if constexpr (kW == 16) {
+                  if (w == 16) {
+                    tmem_ld16(tb + (uint32_t)c8, vh[pb]);         // x high parts
+                    tmem_ld16(tb + (uint32_t)(MP + c8), vl[pb]);  // x low parts
+                    continue;
+                  }
+                }
+                tmem_ld8(tb + (uint32_t)c8, *reinterpret_cast<float(*)[8]>(vh[pb]));
+                tmem_ld8(tb + (uint32_t)(MP + c8), *reinterpret_cast<float(*)[8]>(vl[pb]));
+              }
+              tmem_ld_wait();
+#pragma unroll
+              for (int pb = 0; pb < kPair; ++pb)
+#pragma unroll
+                for (int q = 0; q < kW; ++q)
+                  if (q < w) acc[c8 + q] = fmaf(dsc[b + pb], vh[pb][q] + vl[pb][q], acc[c8 + q]);
+            }
+            if (bg + kPair - 1 == gb - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&e.d_empty[dslot]);
+              if (NI == 1) dr0.next(e.nd);
+            }
+          }
+        }
+      }
+      ring.next(e.nstages);
+    }
+    if (*e.abort_flag) continue;
+    float* out = p.y + (int64_t)split * p.m * p.n;
+#pragma unroll
+    for (int q = 0; q < HALF; ++q) {
+      const int i = e.i0 + q;
+      if (i < p.m && row < p.n) out[(int64_t)i * p.n + row] = acc[q] * p.bscale[i];
+    }
+  }
+}
+
 // ---- main kernel ------------------------------------------------------------------
 
 template <int FMT>
@@ -639,80 +755,38 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     // ------------------------------ epilogue ------------------------------------
     const int quarter = warp & 3;                   // tensor-memory lane quarter
     const int ahalf = (warp - 2 - kDeqWarps) >> 2;  // half of the activation columns
-    const int r = quarter * 32 + lane;
-    const int half = MP / 2;  // 8 .. 32 activation columns per warp
-    const int i0 = ahalf * half;
-    const uint32_t d_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + tmem_d + (uint32_t)i0;
-    Ring ring, dr0;  // stages; the accumulator buffers (one issuer)
-    int g = 0;            // the chunk's place in this CTA's list (its issuer is g % NI)
-    for (int item = ib; item < ie; ++item) {
-      const int split = item / p.tiles, tile = item - split * p.tiles;
-      const int c0 = chunk_begin(split), c1 = chunk_begin(split + 1);
-      const int64_t row = (int64_t)tile * kRows + r;
-      float acc[32];
-#pragma unroll
-      for (int q = 0; q < 32; ++q) acc[q] = 0.f;
-      for (int c = c0; c < c1; ++c, ++g) {
-        if (!*abort_flag) {
-          if (!mbar_wait_bounded(&tma_full[ring.slot], ring.phase)) {
-            fail_wait();
-          } else {
-            const uint8_t* st = stages + (size_t)ring.slot * sbytes;
-            const int me = g % NI;
-            // this chunk's block scales of row r, from its 16-byte box
-            const __half* srow = reinterpret_cast<const __half*>(st + off_scales + r * 16);
-            const int s0 = kBlocks == 4 ? 4 * (c & 1) : (c & 7);
-            float dsc[kBlocks];
-#pragma unroll
-            for (int b = 0; b < kBlocks; ++b) dsc[b] = __half2float(srow[s0 + b]);
-            // the scales are in registers: the epilogue is done with the stage
-            // (the unpack warps and the MMA commit release it too)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tma_empty[ring.slot]);
-#pragma unroll
-            for (int b = 0; b < kBlocks; ++b) {
-              const int bg = b % gb;
-              // one issuer: a ring over the buffers; several: buffer `me`, its (g / NI)-th use
-              const int dslot = NI == 1 ? dr0.slot : me;
-              const uint32_t dphase = NI == 1 ? dr0.phase : (uint32_t)((g / NI) & 1);
-              if (bg == 0) {
-                if (!mbar_wait_bounded(&d_full[dslot], dphase)) {
-                  fail_wait();
-                  break;
-                }
-                tc_fence_after();
-              }
-              const float d = dsc[b];
-              const uint32_t t0 = d_lane + (uint32_t)((dslot * gb + bg) * 2 * MP);
-#pragma unroll
-              for (int g = 0; g < 32; g += 8) {
-                if (g < half) {
-                  float vh[8], vl[8];
-                  tmem_ld8(t0 + (uint32_t)g, vh);       // x high parts
-                  tmem_ld8(t0 + (uint32_t)(MP + g), vl);  // x low parts
-                  tmem_ld_wait();
-#pragma unroll
-                  for (int q = 0; q < 8; ++q) acc[g + q] = fmaf(d, vh[q] + vl[q], acc[g + q]);
-                }
-              }
-              if (bg == gb - 1) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&d_empty[dslot]);
-                if (NI == 1) dr0.next(nd);
-              }
-            }
-          }
-        }
-        ring.next(nstages);
-      }
-      if (*abort_flag) continue;
-      float* out = p.y + (int64_t)split * p.m * p.n;
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int i = i0 + q;
-        if (q < half && i < p.m && row < p.n) out[(int64_t)i * p.n + row] = acc[q] * p.bscale[i];
-      }
+    const int half = MP / 2;                        // 8 .. 32 activation columns per warp
+    EpiCtx e;
+    e.stages = stages;
+    e.tma_full = tma_full;
+    e.tma_empty = tma_empty;
+    e.d_full = d_full;
+    e.d_empty = d_empty;
+    e.abort_flag = abort_flag;
+    e.sbytes = sbytes;
+    e.off_scales = off_scales;
+    e.nstages = nstages;
+    e.gb = gb;
+    e.nd = nd;
+    e.ib = ib;
+    e.ie = ie;
+    e.mp = MP;
+    e.r = quarter * 32 + lane;
+    e.i0 = ahalf * half;
+    e.d_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + tmem_d + (uint32_t)e.i0;
+    switch (half) {
+      case 8:
+        epilogue_role<FMT, 8>(p, e, lane);
+        break;
+      case 16:
+        epilogue_role<FMT, 16>(p, e, lane);
+        break;
+      case 24:
+        epilogue_role<FMT, 24>(p, e, lane);
+        break;
+      default:
+        epilogue_role<FMT, 32>(p, e, lane);
+        break;
     }
   }
 
