@@ -181,7 +181,12 @@ __device__ __forceinline__ int scale4_pos(int j) { return 2 * (j & 3) + (j >> 2)
 template <int FMT>
 __global__ void act_hilo_kernel(const float* __restrict__ X, int m, int mp, int64_t k, __half* __restrict__ B,
                                 float* __restrict__ bscale, int had, const int8_t* __restrict__ signs) {
-  // one CTA per activation row i < M' (rows i >= m are zero)
+  // one CTA per activation row i < M' (rows i >= m are zero).  Launched as a
+  // programmatic dependent: X is read only after the kernel before has
+  // completed; the GEMM may then launch at once and set itself up while this
+  // runs (it waits for this grid's completion before reading B).
+  grid_dependency_wait();
+  allow_dependent_launch();
   const int i = blockIdx.x;
   __half* hi = B + (int64_t)i * k;
   __half* lo = B + (int64_t)(mp + i) * k;
@@ -490,7 +495,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   const uint32_t tmem_base = *tmem_slot;
   if (warp == 1) tmem_relinquish();
   // everything above overlaps the activation prologue; its B matrix and
-  // scales are read below
+  // scales are read below.  (This grid lets its dependants launch only when
+  // its CTAs exit: an early trigger measured slower, the next call's prologue
+  // then taking SMs while this grid still runs.)
   grid_dependency_wait();
 
   const int items = p.tiles * p.splits;
@@ -903,8 +910,9 @@ int launch_act(const kq_qmat* W, const float* X, int m, int64_t k, int64_t mp, _
   });
   KQ_CUDA_TRY(attr);
   const int bytes = (int)(k * sizeof(float));
-  tc::act_hilo_kernel<FMT><<<(int)mp, 256, bytes, st>>>(X, m, (int)mp, k, B, bscale, W->had_block, W->signs);
-  KQ_CUDA_TRY(cudaGetLastError());
+  // a programmatic dependent of the stream's previous kernel
+  KQ_CUDA_TRY(launch_dependent(tc::act_hilo_kernel<FMT>, dim3((unsigned)mp), dim3(256), (size_t)bytes, st, X, m,
+                               (int)mp, k, B, bscale, (int)W->had_block, (const int8_t*)W->signs));
   return KQ_OK;
 }
 
