@@ -16,9 +16,8 @@
 //    relative.  One MMA multiplies A by both halves (N = 2M').
 //  * Main kernel (tc_gemm_kernel), one persistent CTA per SM over a list of
 //    items (128-row tile of W, K split), 128-weight K chunks:
-//      warp 0       TMA producer: per chunk the codes of 128 rows, their
-//                   scales (a 16-byte box per row) and two 64-wide
-//                   128-byte-swizzled boxes of B;
+//      warp 0       TMA producer: per chunk the codes of 128 rows and two
+//                   64-wide 128-byte-swizzled boxes of B;
 //      warp 1       allocates tensor memory and issues tcgen05.mma
 //                   (kind::f16, M = 128, N = 2M', K = 16, A from tensor
 //                   memory, B from shared memory) and the commits: the warp
@@ -29,7 +28,10 @@
 //                   (tcgen05.st): lane i of a warp owns weight row i of its
 //                   quarter, each warp half of the chunk's K;
 //      warps 10-17  epilogue (tcgen05.ld), each warp half of the activation
-//                   columns of its lane quarter.
+//                   columns of its lane quarter; it reads the block scales
+//                   of its rows from the scales plane itself, one or two
+//                   chunks ahead, so a stage is free once it has been
+//                   unpacked and multiplied.
 //    The A operand never touches shared memory (a 16-bit tile there would
 //    cost ~4 bytes of shared-memory traffic per weight).
 //  * A holds the integer code values only, exactly: q for Q8_0 (an fp16
@@ -88,7 +90,6 @@ constexpr int kEpiWarps = 8;
 constexpr int kIssuer2Warp = 2 + kDeqWarps + kEpiWarps;  // the second and third MMA issuers
 constexpr int kMaxIssuers = 3;
 constexpr int kThreads = 32 * (kIssuer2Warp + kMaxIssuers - 1);  // 640
-constexpr int kScaleBoxBytes = kRows * 16;                   // 8 fp16 scales per row
 constexpr int kBarBytes = 512;
 constexpr size_t kSmemBytes = 232448;  // the per-CTA maximum; carved at run time
 constexpr size_t kCarveBytes = kSmemBytes - 1024 /* alignment slack */ - kBarBytes;
@@ -105,7 +106,7 @@ __host__ __device__ constexpr int chunk_row_bytes(int fmt) {
 __host__ __device__ constexpr int code_chunk_bytes(int fmt) { return kRows * chunk_row_bytes(fmt); }
 __host__ __device__ constexpr int b_box_bytes(int mp) { return 2 * mp * 128; }  // 64 fp16 x 2M' rows
 __host__ __device__ constexpr int stage_tx_bytes(int fmt, int mp) {
-  return code_chunk_bytes(fmt) + kScaleBoxBytes + 2 * b_box_bytes(mp);
+  return code_chunk_bytes(fmt) + 2 * b_box_bytes(mp);
 }
 __host__ __device__ constexpr int stage_bytes(int fmt, int mp) { return (stage_tx_bytes(fmt, mp) + 1023) / 1024 * 1024; }
 // Accumulator groups: a group holds `gb` consecutive blocks' accumulators
@@ -137,7 +138,9 @@ __device__ __forceinline__ void tc_flag(int status) { atomicOr(&g_tc_status, 1u 
 
 struct TcParams {
   CUtensorMap map_codes;   // Q8_0: u32 [n][k/4], box 32 x 128, 128B swizzle; PQ2_0: u32 [n][k/16], box 8 x 128, 32B swizzle
-  CUtensorMap map_scales;  // fp16 [n][sstride], box 8 x 128
+  const uint16_t* scales;   // fp16 block scales [n][sstride]
+  int64_t sstride;          // scales per row (a multiple of 8)
+  int32_t kblocks;          // quantization blocks per row (k / block)
   CUtensorMap map_b;       // fp16 [2M'][k], box 64 x 2M', 128B swizzle
   const float* bscale;     // per activation row: the power of two the result is scaled by
   float* y;                // splits == 1: Y [m][n]; else partials [splits][m][n]
@@ -315,23 +318,40 @@ __global__ void act_hilo_kernel(const float* __restrict__ X, int m, int mp, int6
 
 // What the epilogue warps need from the kernel's set-up.
 struct EpiCtx {
-  const uint8_t* stages;
-  uint64_t* tma_full;
-  uint64_t* tma_empty;
   uint64_t* d_full;
   uint64_t* d_empty;
   volatile int* abort_flag;
-  int sbytes, off_scales, nstages, gb, nd, ib, ie, mp;
+  int gb, nd, ib, ie, mp;
   uint32_t d_lane;  // this warp's lane quarter and first activation column in the accumulators
   int r, i0;        // this lane's tile row; this warp's first activation row
 };
 
-// The epilogue warps: per chunk, the block scales of row r from the stage
-// (then the stage is released), then per block d * (hi + lo) of the warp's
-// HALF activation columns added into registers.  The accumulator loads are
-// batched to few tensor-memory round trips: two blocks per wait at HALF = 8
-// (their group holds all four blocks of the chunk), sixteen columns (hi and
-// lo) per wait otherwise.
+// The fp16 block scales of chunk c of a row, read past L1: four (8 bytes)
+// for Q8_0 and SCALE4, one for PQ2_0.
+template <int kBlocks>
+struct ChunkScales {
+  uint32_t w[kBlocks == 4 ? 2 : 1];
+  __device__ __forceinline__ void load(const uint16_t* srow, int c) {
+    if constexpr (kBlocks == 4) {
+      const uint2 v = __ldcg(reinterpret_cast<const uint2*>(srow) + c);
+      w[0] = v.x;
+      w[1] = v.y;
+    } else {
+      w[0] = __ldcg(reinterpret_cast<const unsigned short*>(srow) + c);
+    }
+  }
+  __device__ __forceinline__ float get(int b) const {
+    return __half2float(__ushort_as_half((uint16_t)(w[b >> 1] >> (16 * (b & 1)))));
+  }
+};
+
+// The epilogue warps: per chunk, the block scales of row r (read from the
+// scales plane one chunk ahead), then per block
+// d * (hi + lo) of the warp's HALF activation columns added into registers.
+// The accumulator loads are batched to few tensor-memory round trips: two
+// blocks per wait at HALF = 8 (their group holds all four blocks of the
+// chunk), sixteen columns (hi and lo) per wait otherwise.  The epilogue never
+// touches the stages.
 template <int FMT, int HALF>
 __device__ __forceinline__ void epilogue_role(const TcParams& p, const EpiCtx& e, int lane) {
   constexpr int kBlocks = blocks_per_chunk(FMT);
@@ -339,90 +359,92 @@ __device__ __forceinline__ void epilogue_role(const TcParams& p, const EpiCtx& e
   constexpr int kSeg = HALF >= 16 ? 16 : 8;                      // columns per load (hi and lo each)
   constexpr int kPair = (HALF == 8 && kBlocks >= 2) ? 2 : 1;     // blocks per wait
   const int MP = e.mp, gb = e.gb;
-  Ring ring, dr0;  // stages; the accumulator buffers (one issuer)
-  int g = 0;       // the chunk's place in this CTA's list (its issuer is g % NI)
+  Ring dr0;  // the accumulator buffers (one issuer)
+  int g = 0;  // the chunk's place in this CTA's list (its issuer is g % NI)
   for (int item = e.ib; item < e.ie; ++item) {
     const int split = item / p.tiles, tile = item - split * p.tiles;
     const int c0 = (int)((int64_t)split * p.chunks / p.splits), c1 = (int)((int64_t)(split + 1) * p.chunks / p.splits);
     const int64_t row = (int64_t)tile * kRows + e.r;
+    const bool live_row = row < p.n;
+    const uint16_t* srow = p.scales + (live_row ? row : 0) * p.sstride;
     float acc[HALF];
 #pragma unroll
     for (int q = 0; q < HALF; ++q) acc[q] = 0.f;
+    // the scales of the next kAhead chunks are in flight (two for PQ2_0, whose
+    // chunks are short; one for Q8_0 and SCALE4, whose registers are tight)
+    constexpr int kAhead = kBlocks == 1 ? 2 : 1;
+    ChunkScales<kBlocks> n1, n2;
+    n1.load(srow, c0);
+    if (kAhead > 1 && c0 + 1 < c1) n2.load(srow, c0 + 1);
     for (int c = c0; c < c1; ++c, ++g) {
-      if (!*e.abort_flag) {
-        if (!mbar_wait_bounded(&e.tma_full[ring.slot], ring.phase)) {
-          *e.abort_flag = 1;
-          tc_flag(KQ_ERR_TIMEOUT);
-        } else {
-          const uint8_t* st = e.stages + (size_t)ring.slot * e.sbytes;
-          const int me = g % NI;
-          // this chunk's block scales of row r, from its 16-byte box
-          const __half* srow = reinterpret_cast<const __half*>(st + e.off_scales + e.r * 16);
-          const int s0 = kBlocks == 4 ? 4 * (c & 1) : (c & 7);
-          float dsc[kBlocks];
+      if (*e.abort_flag) continue;
+      const int me = g % NI;
+      // this chunk's block scales of row r; blocks past k (a ragged last chunk) weigh 0
+      const ChunkScales<kBlocks> cur = n1;
+      if constexpr (kAhead > 1) {
+        n1 = n2;
+        if (c + 2 < c1) n2.load(srow, c + 2);
+      } else {
+        if (c + 1 < c1) n1.load(srow, c + 1);
+      }
+      const int blk0 = c * kBlocks;
+      float dsc[kBlocks];
 #pragma unroll
-          for (int b = 0; b < kBlocks; ++b) dsc[b] = __half2float(srow[s0 + b]);
-          // the scales are in registers: the epilogue is done with the stage
-          // (the unpack warps and the MMA commit release it too)
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&e.tma_empty[ring.slot]);
+      for (int b = 0; b < kBlocks; ++b) dsc[b] = live_row && blk0 + b < p.kblocks ? cur.get(b) : 0.f;
 #pragma unroll
-          for (int b = 0; b < kBlocks; b += kPair) {
-            const int bg = b % gb;
-            // one issuer: a ring over the buffers; several: buffer `me`, its (g / NI)-th use
-            const int dslot = NI == 1 ? dr0.slot : me;
-            const uint32_t dphase = NI == 1 ? dr0.phase : (uint32_t)((g / NI) & 1);
-            if (bg == 0) {
-              if (!mbar_wait_bounded(&e.d_full[dslot], dphase)) {
-                *e.abort_flag = 1;
-                tc_flag(KQ_ERR_TIMEOUT);
-                break;
-              }
-              tc_fence_after();
-            }
-            const uint32_t t0 = e.d_lane + (uint32_t)((dslot * gb + bg) * 2 * MP);
-#pragma unroll
-            for (int c8 = 0; c8 < HALF; c8 += kSeg) {
-              constexpr int kW = kSeg;
-              const int w = HALF - c8 < kW ? HALF - c8 : kW;  // 8 or 16 columns in this segment
-              float vh[kPair][kW], vl[kPair][kW];
-#pragma unroll
-              for (int pb = 0; pb < kPair; ++pb) {
-                const uint32_t tb = t0 + (uint32_t)(pb * 2 * MP);
-                if constexpr (kW == 16) {
-                  if (w == 16) {
-                    tmem_ld16(tb + (uint32_t)c8, vh[pb]);         // x high parts
-                    tmem_ld16(tb + (uint32_t)(MP + c8), vl[pb]);  // x low parts
-                    continue;
-                  }
-                }
-                tmem_ld8(tb + (uint32_t)c8, *reinterpret_cast<float(*)[8]>(vh[pb]));
-                tmem_ld8(tb + (uint32_t)(MP + c8), *reinterpret_cast<float(*)[8]>(vl[pb]));
-              }
-              tmem_ld_wait();
-#pragma unroll
-              for (int pb = 0; pb < kPair; ++pb)
-#pragma unroll
-                for (int q = 0; q < kW; ++q)
-                  if (q < w) acc[c8 + q] = fmaf(dsc[b + pb], vh[pb][q] + vl[pb][q], acc[c8 + q]);
-            }
-            if (bg + kPair - 1 == gb - 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&e.d_empty[dslot]);
-              if (NI == 1) dr0.next(e.nd);
-            }
+      for (int b = 0; b < kBlocks; b += kPair) {
+        const int bg = b % gb;
+        // one issuer: a ring over the buffers; several: buffer `me`, its (g / NI)-th use
+        const int dslot = NI == 1 ? dr0.slot : me;
+        const uint32_t dphase = NI == 1 ? dr0.phase : (uint32_t)((g / NI) & 1);
+        if (bg == 0) {
+          if (!mbar_wait_bounded(&e.d_full[dslot], dphase)) {
+            *e.abort_flag = 1;
+            tc_flag(KQ_ERR_TIMEOUT);
+            break;
           }
+          tc_fence_after();
+        }
+        const uint32_t t0 = e.d_lane + (uint32_t)((dslot * gb + bg) * 2 * MP);
+#pragma unroll
+        for (int c8 = 0; c8 < HALF; c8 += kSeg) {
+          constexpr int kW = kSeg;
+          const int w = HALF - c8 < kW ? HALF - c8 : kW;  // 8 or 16 columns in this segment
+          float vh[kPair][kW], vl[kPair][kW];
+#pragma unroll
+          for (int pb = 0; pb < kPair; ++pb) {
+            const uint32_t tb = t0 + (uint32_t)(pb * 2 * MP);
+            if constexpr (kW == 16) {
+              if (w == 16) {
+                tmem_ld16(tb + (uint32_t)c8, vh[pb]);         // x high parts
+                tmem_ld16(tb + (uint32_t)(MP + c8), vl[pb]);  // x low parts
+                continue;
+              }
+            }
+            tmem_ld8(tb + (uint32_t)c8, *reinterpret_cast<float(*)[8]>(vh[pb]));
+            tmem_ld8(tb + (uint32_t)(MP + c8), *reinterpret_cast<float(*)[8]>(vl[pb]));
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int pb = 0; pb < kPair; ++pb)
+#pragma unroll
+            for (int q = 0; q < kW; ++q)
+              if (q < w) acc[c8 + q] = fmaf(dsc[b + pb], vh[pb][q] + vl[pb][q], acc[c8 + q]);
+        }
+        if (bg + kPair - 1 == gb - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&e.d_empty[dslot]);
+          if (NI == 1) dr0.next(e.nd);
         }
       }
-      ring.next(e.nstages);
     }
     if (*e.abort_flag) continue;
     float* out = p.y + (int64_t)split * p.m * p.n;
 #pragma unroll
     for (int q = 0; q < HALF; ++q) {
       const int i = e.i0 + q;
-      if (i < p.m && row < p.n) out[(int64_t)i * p.n + row] = acc[q] * p.bscale[i];
+      if (i < p.m && live_row) out[(int64_t)i * p.n + row] = acc[q] * p.bscale[i];
     }
   }
 }
@@ -452,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   constexpr int NI = kBlocks == 1 ? kMaxIssuers : 1;  // MMA issuers
   const int ndi = nd / NI;                            // accumulator buffers per issuer (1 when NI > 1)
   const int sbytes = stage_bytes(FMT, MP);
-  const int off_scales = kCodes, off_b = kCodes + kScaleBoxBytes;
+  const int off_b = kCodes;  // B follows the codes (1024-byte aligned)
   uint8_t* stages = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kCarveBytes);
   uint64_t* tma_full = bars;                    // [kMaxStages] producer -> unpack, MMA, epilogue
@@ -471,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   if (threadIdx.x == 0) {
     for (int s = 0; s < nstages; ++s) {
       mbar_init(&tma_full[s], 1);
-      mbar_init(&tma_empty[s], kDeqWarps + 1 + kEpiWarps);  // codes, B (MMA commit), scales
+      mbar_init(&tma_empty[s], kDeqWarps + 1);  // codes (unpack warps), B (MMA commit)
     }
     // a_full per stage, with the stage's phase: an issuer waits on it only
     // after tma_full of the same stage and phase, which already implies that
@@ -514,7 +536,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     if (lane == 0) {
       const uint64_t policy = l2_policy_evict_first();
       prefetch_tmap(&p.map_codes);
-      prefetch_tmap(&p.map_scales);
       prefetch_tmap(&p.map_b);
       Ring ring;
       int issued = 0;
@@ -532,16 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           uint64_t* bar = &tma_full[ring.slot];
           mbar_arrive_expect_tx(bar, stage_tx);
           const int32_t y0 = tile * kRows;
-          if (FMT == KQ_Q8_0) {
-            tma_load_2d(st, &p.map_codes, c * (kChunk / 4), y0, bar, policy);
-            tma_load_2d(st + off_scales, &p.map_scales, (4 * c) & ~7, y0, bar, policy);
-          } else if (FMT == KQ_SCALE4) {
-            tma_load_2d(st, &p.map_codes, c * (kChunk / 8), y0, bar, policy);
-            tma_load_2d(st + off_scales, &p.map_scales, (4 * c) & ~7, y0, bar, policy);
-          } else {
-            tma_load_2d(st, &p.map_codes, c * (kChunk / 16), y0, bar, policy);
-            tma_load_2d(st + off_scales, &p.map_scales, c & ~7, y0, bar, policy);
-          }
+          tma_load_2d(st, &p.map_codes, c * (chunk_row_bytes(FMT) / 4), y0, bar, policy);
           tma_load_2d(st + off_b, &p.map_b, c * kChunk, 0, bar, policy);
           tma_load_2d(st + off_b + b_box_bytes(MP), &p.map_b, c * kChunk + 64, 0, bar, policy);
           ring.next(nstages);
@@ -764,15 +776,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     const int ahalf = (warp - 2 - kDeqWarps) >> 2;  // half of the activation columns
     const int half = MP / 2;                        // 8 .. 32 activation columns per warp
     EpiCtx e;
-    e.stages = stages;
-    e.tma_full = tma_full;
-    e.tma_empty = tma_empty;
     e.d_full = d_full;
     e.d_empty = d_empty;
     e.abort_flag = abort_flag;
-    e.sbytes = sbytes;
-    e.off_scales = off_scales;
-    e.nstages = nstages;
     e.gb = gb;
     e.nd = nd;
     e.ib = ib;
@@ -981,9 +987,9 @@ int tc_gemm(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, int split
   if (int s = encode(fn, &p.map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, W->codes, rowbytes / 4, W->n, rowbytes,
                      box_u32, tc::kRows, cswz, "the codes plane"))
     return s;
-  if (int s = encode(fn, &p.map_scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, W->scales, ss, W->n, ss * 2, 8u, tc::kRows,
-                     CU_TENSOR_MAP_SWIZZLE_NONE, "the scales plane"))
-    return s;
+  p.scales = reinterpret_cast<const uint16_t*>(W->scales);
+  p.sstride = ss;
+  p.kblocks = (int32_t)(W->k / (W->fmt == KQ_PQ2_0 ? 128 : 32));
   if (int s = encode(fn, &p.map_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, W->k, g.nb, W->k * 2, 64u, (uint32_t)g.nb,
                      CU_TENSOR_MAP_SWIZZLE_128B, "the activation matrix"))
     return s;
