@@ -917,7 +917,7 @@ int launch_act(const kq_qmat* W, const float* X, int m, int64_t k, int64_t mp, _
   KQ_CUDA_TRY(attr);
   const int bytes = (int)(k * sizeof(float));
   // a programmatic dependent of the stream's previous kernel
-  KQ_CUDA_TRY(launch_dependent(tc::act_hilo_kernel<FMT>, dim3((unsigned)mp), dim3(256), (size_t)bytes, st, X, m,
+  KQ_CUDA_TRY(launch_dependent(tc::act_hilo_kernel<FMT>, dim3((unsigned)mp), dim3(512), (size_t)bytes, st, X, m,
                                (int)mp, k, B, bscale, (int)W->had_block, (const int8_t*)W->signs));
   return KQ_OK;
 }
