@@ -1644,19 +1644,37 @@ static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count,
     p->counter_bytes = (size_t)round_up((int64_t)nstages * 4, 256);
     p->ws_bytes = p->counter_bytes + (size_t)part_floats * sizeof(float);
   } else {
-    // byte-balanced contiguous item ranges, one per CTA
+    // Contiguous item ranges, one per CTA, by bytes.  On a full grid the
+    // shares are skewed: CTA c gets bytes in proportion to
+    // 1 + kDealSkew * (1/2 - c / (G - 1)).  Measured on GB300 (per-CTA
+    // finish stamps of one launch): with equal shares the finish time grows
+    // about linearly with the CTA index, ~5% from the first CTAs to the last,
+    // reproducibly, with the work of every CTA alike and whatever the order
+    // in which the weights were allocated; the skew of 0.06 took the
+    // Bonsai-shaped step from 4992 to 5076 GB/s and the Qwen-shaped one from
+    // 6611 to 6685 (0.04: 5062 / 6623; 0.08: 5047 / 6679).
+    constexpr double kDealSkew = 0.06;
     p->total_items = items;
     p->grid = (int)std::min<int64_t>(items, sms);
     const int G = p->grid;
+    const double skew = G >= 128 ? kDealSkew : 0.0;
     bounds.assign((size_t)(G + 1), items);
     bounds[0] = 0;
     double total = 0;
     for (double b : item_bytes) total += b;
+    std::vector<double> target((size_t)G + 1, 0.0);  // cumulative byte targets
+    double wsum = 0;
+    for (int c = 0; c < G; ++c) wsum += 1.0 + skew * (0.5 - (G > 1 ? (double)c / (G - 1) : 0.0));
+    double run = 0;
+    for (int c = 0; c < G; ++c) {
+      run += 1.0 + skew * (0.5 - (G > 1 ? (double)c / (G - 1) : 0.0));
+      target[(size_t)c + 1] = total * run / wsum;
+    }
     double accum = 0;
     int c = 1;
     for (int64_t it = 0; it < items && c < G; ++it) {
       accum += item_bytes[(size_t)it];
-      while (c < G && accum >= total * c / G) bounds[(size_t)c++] = it + 1;
+      while (c < G && accum >= target[(size_t)c]) bounds[(size_t)c++] = it + 1;
     }
   }
   cudaError_t e = cudaMalloc(&p->d_jobs, sizeof(Job) * (size_t)count);
