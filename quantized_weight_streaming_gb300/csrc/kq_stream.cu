@@ -6,13 +6,14 @@
 // but keep HBM busy and dequantize in registers:
 //
 //  * One persistent CTA per SM: warp 0 is the producer, sixteen consumer
-//    warps compute.  A tile is 128 weight rows x 256 bytes of codes (256
-//    Q8_0 weights or 1024 PQ2_0 weights per row) plus the matching 128 x 8
-//    fp16 scales.  The producer brings each tile into a ring of four
-//    shared-memory stages with two 2-D TMA loads (cp.async.bulk.tensor over
-//    tensor maps of the row-major planes; rows past n and columns past k come
-//    back as zeros), completion counted on an mbarrier, L2 evict-first since
-//    every weight byte is read exactly once.
+//    warps compute.  A tile is 256 bytes of codes per row (256 Q8_0 weights,
+//    1024 PQ2_0 weights or 512 SCALE4 weights) plus the row's fp16 scales of
+//    those weights: 128 rows for Q8_0 in a ring of four shared-memory
+//    stages, 256 rows for PQ2_0 and SCALE4 in a ring of two.  The producer
+//    brings each tile in with 2-D TMA loads (cp.async.bulk.tensor over tensor
+//    maps of the row-major planes; rows past n and columns past k come back
+//    as zeros), completion counted on an mbarrier, L2 evict-first since every
+//    weight byte is read exactly once.
 //  * Work is a list of items (matrix, 128-row block, K split).  Each CTA owns
 //    a contiguous run of items, so it changes matrices rarely; an item walks
 //    its K range one 256-byte chunk (one tile) at a time.
@@ -29,8 +30,8 @@
 //    27B - ternary g128 + blockwise Hadamard", section 4.2) in registers and
 //    warp shuffles, fused into the load.
 //  * PQ2_0 consumers run on the tensor cores (mma.sync m16n8k16, fp16 in,
-//    fp32 accumulate): warp w owns 32 rows (two 16-row slabs) and a quarter
-//    of the tile's K, so each B fragment it loads serves both slabs.  A
+//    fp32 accumulate): warp w owns 64 rows (four 16-row slabs) and a quarter
+//    of the tile's K, so each B fragment it loads serves four slabs.  A
 //    2-bit code masked in place inside its 32-bit word is the exact fp16
 //    subnormal c * 2^(s-24): one AND per two codes builds an A register.  B
 //    holds x' as an fp16 high/low pair scaled per block by 2^(14-s-E); the
