@@ -1646,37 +1646,60 @@ static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count,
     p->ws_bytes = p->counter_bytes + (size_t)part_floats * sizeof(float);
   } else {
     // Contiguous item ranges, one per CTA, by bytes.  On a full grid the
-    // shares are skewed: CTA c gets bytes in proportion to
-    // 1 + kDealSkew * (1/2 - c / (G - 1)).  Measured on GB300 (per-CTA
+    // shares are skewed: CTA c's capacity is proportional to
+    // w_c = 1 + kDealSkew * (1/2 - c / (G - 1)).  Measured on GB300 (per-CTA
     // finish stamps of one launch): with equal shares the finish time grows
     // about linearly with the CTA index, ~5% from the first CTAs to the last,
     // reproducibly, with the work of every CTA alike and whatever the order
     // in which the weights were allocated; the skew of 0.06 took the
     // Bonsai-shaped step from 4992 to 5076 GB/s and the Qwen-shaped one from
     // 6611 to 6685 (0.04: 5062 / 6623; 0.08: 5047 / 6679).
+    // The cut points minimise the largest load relative to its capacity,
+    // max_c bytes_c / w_c: the least T for which filling each CTA in turn
+    // with whole items up to T w_c places every item (taking each range as
+    // long as it fits is optimal for a given T), found by bisection.  An
+    // item holds a whole row block (up to 1.2 MB at K = 17408), so cutting
+    // at the cumulative targets instead could leave a CTA an item above its
+    // share.
     constexpr double kDealSkew = 0.06;
     p->total_items = items;
     p->grid = (int)std::min<int64_t>(items, sms);
     const int G = p->grid;
     const double skew = G >= 128 ? kDealSkew : 0.0;
+    std::vector<double> wgt((size_t)G);
+    double wsum = 0, total = 0, biggest = 0;
+    for (int c = 0; c < G; ++c) wsum += wgt[(size_t)c] = 1.0 + skew * (0.5 - (G > 1 ? (double)c / (G - 1) : 0.0));
+    for (double b : item_bytes) {
+      total += b;
+      biggest = std::max(biggest, b);
+    }
     bounds.assign((size_t)(G + 1), items);
     bounds[0] = 0;
-    double total = 0;
-    for (double b : item_bytes) total += b;
-    std::vector<double> target((size_t)G + 1, 0.0);  // cumulative byte targets
-    double wsum = 0;
-    for (int c = 0; c < G; ++c) wsum += 1.0 + skew * (0.5 - (G > 1 ? (double)c / (G - 1) : 0.0));
-    double run = 0;
-    for (int c = 0; c < G; ++c) {
-      run += 1.0 + skew * (0.5 - (G > 1 ? (double)c / (G - 1) : 0.0));
-      target[(size_t)c + 1] = total * run / wsum;
+    // fills CTA after CTA up to T w_c; true if every item found a place
+    auto fill = [&](double T, bool record) {
+      int c = 0;
+      double load = 0;
+      for (int64_t it = 0; it < items; ++it) {
+        const double b = item_bytes[(size_t)it];
+        while (load + b > T * wgt[(size_t)c]) {
+          if (load == 0 || c + 1 == G) return false;  // the item fits no CTA from c on
+          ++c;
+          if (record) bounds[(size_t)c] = it;
+          load = 0;
+        }
+        load += b;
+      }
+      if (record)
+        for (int r = c + 1; r <= G; ++r) bounds[(size_t)r] = items;
+      return true;
+    };
+    double lo = total / wsum, hi = (total + (double)G * biggest) / wsum * 2.0;
+    for (int r = 0; r < 64 && !fill(hi, false); ++r) hi *= 2.0;
+    for (int r = 0; r < 60; ++r) {
+      const double mid = 0.5 * (lo + hi);
+      (fill(mid, false) ? hi : lo) = mid;
     }
-    double accum = 0;
-    int c = 1;
-    for (int64_t it = 0; it < items && c < G; ++it) {
-      accum += item_bytes[(size_t)it];
-      while (c < G && accum >= target[(size_t)c]) bounds[(size_t)c++] = it + 1;
-    }
+    fill(hi, true);
   }
   cudaError_t e = cudaMalloc(&p->d_jobs, sizeof(Job) * (size_t)count);
   if (e == cudaSuccess) e = cudaMalloc(&p->d_maps, sizeof(CUtensorMap) * (size_t)(2 * count));
