@@ -227,7 +227,9 @@ size_t kq_gemv_workspace_bytes(const kq_qmat* W, int64_t m);
 
 /* y[n] = W x for a Q8_0 matrix: d_x fp32 [k], d_y fp32 [n].  The batch-1
  * product that bounds decode, every weight streamed once ("Kipp Benchmarks",
- * "Decode is weight-bandwidth-bound"). */
+ * "Decode is weight-bandwidth-bound").  A small matrix (k <= 4096 and at
+ * most 20 MB of codes) runs in one launch with no K split and needs no
+ * workspace; larger ones use the streaming kernel's split plan. */
 int kq_gemv_q8_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
 
 /* y[n] = W x for a SCALE4 matrix: d_x fp32 [k], d_y fp32 [n]. */

@@ -11,7 +11,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libkq.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["kq_host.cpp", "kq_prep.cu", "kq_stream.cu", "kq_tcs.cu", "kq_tc.cu", "kq_control.cu"]
+SOURCES = ["kq_host.cpp", "kq_prep.cu", "kq_stream.cu", "kq_tcs.cu", "kq_tc.cu", "kq_control.cu", "kq_direct.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("kq_internal.h", "kq_device.cuh", "kq_tc.h", "kq_stream.cuh", "kq_tcgen05.cuh")] + [os.path.join(INCLUDE, "kq.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]

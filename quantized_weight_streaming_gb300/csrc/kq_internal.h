@@ -29,6 +29,14 @@ inline int64_t code_row_bytes(int fmt, int64_t k) { return fmt == KQ_Q8_0 ? k : 
 // Checks a kq_qmat descriptor (format, shape, plane pointers and alignment).
 int check_qmat(const kq_qmat* W, int expect_fmt);
 
+// The one-launch Q8_0 GEMV (kq_direct.cu): taken by the automatic choice
+// (splits = 0) at one activation row, fp32 or fp16 chain, for k up to 4096
+// and at most kGemvDirectMaxBytes of codes; it needs no workspace.
+constexpr int64_t kGemvDirectMaxBytes = 20ll << 20;
+bool gemv_direct_applies(const kq_qmat* W, int64_t m);
+// d_x / d_y: fp32, or fp16 with io16 (the fp16 chain).
+int gemv_direct(const kq_qmat* W, const void* d_x, void* d_y, bool io16, void* stream);
+
 }  // namespace kq
 
 #define KQ_CUDA_TRY(expr)                                                                           \

@@ -1224,6 +1224,7 @@ static int sms_or_default() {
 }
 
 static size_t splitk_ws_bytes(const kq_qmat* W, int64_t m, int splits) {
+  if (splits == 0 && gemv_direct_applies(W, m)) return 0;
   int64_t mm = std::min<int64_t>(m, kMaxRowsPerLaunch);
   Geometry g = make_geometry(W->fmt, W->n, W->k, mm, splits, splits == 0 ? sms_or_default() : 0,
                              staging_floats(W, mm));
@@ -1237,6 +1238,8 @@ static int gemm_impl(const kq_qmat* W, const float* d_X, int64_t m, float* d_Y, 
   if (splits < 0) return fail(KQ_ERR_INVALID_ARG, "splits = %d", splits);
   if (!d_X || !d_Y) return fail(KQ_ERR_INVALID_ARG, "NULL activation or output");
   if (!aligned16(d_X) || !aligned16(d_Y)) return fail(KQ_ERR_ALIGNMENT, "x or y not 16-byte aligned");
+  // a small Q8_0 matrix at one row: the one-launch GEMV
+  if (splits == 0 && gemv_direct_applies(W, m)) return gemv_direct(W, d_X, d_Y, io16, stream);
   const size_t need = splitk_ws_bytes(W, m, splits);
   if (need > 0 && (d_ws == nullptr || ws_bytes < need))
     return fail(KQ_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, d_ws ? ws_bytes : (size_t)0);

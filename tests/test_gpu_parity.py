@@ -311,6 +311,32 @@ def test_pq2_0_activation_scale_extremes(kq, consumer, wl):
         assert ok, (scale, worst)
 
 
+@pytest.mark.parametrize("n,k", [(1023, 4096), (8, 64), (2049, 2560), (5120, 4096)])
+def test_q8_0_one_launch_gemv(kq, wl, n, k):
+    """A small Q8_0 matrix at one row runs in one launch with no K split: it
+    asks for no workspace, is deterministic and within the bound, and so is
+    the split streaming path (explicit split counts) on the same inputs.  The
+    shapes: k at the path's limit of 4096, a single CTA, rows not a multiple
+    of the CTA's 8, and the largest matrix the path takes (20 MB of codes)."""
+    sw, sx = synth.stream_id("test", 0, 315), synth.stream_id("test", 1, 315)
+    W = wl.build_matrix("q8_0", n, k, 2, sw)
+    x = wl.build_activation(k, 2, sx)
+    assert kq.kq_gemv_workspace_bytes(W, 1) == 0
+    w = synth.fill_host("w", n * k, 2, sw).reshape(n, k)
+    _, _, y_ref, absdot = oracle.reference("q8_0", w, synth.fill_host("x", k, 2, sx))
+    y = torch.full((n,), float("nan"), dtype=torch.float32, device="cuda")
+    kq.kq_gemv_q8_0(W, x, y, None)  # no workspace at all
+    _sync_ok(kq)
+    y = y.cpu().numpy()
+    ok, worst = oracle.within_bound(y, y_ref, absdot, TOL)
+    assert ok, worst
+    assert np.array_equal(_run_gemv(kq, W, x), y)
+    for splits in (1, 2):
+        ys = _run_gemv(kq, W, x, splits=splits)
+        ok, worst = oracle.within_bound(ys, y_ref, absdot, TOL)
+        assert ok, (splits, worst)
+
+
 @pytest.mark.parametrize("fmt,n,k", [("q8_0", 200, 9728), ("pq2_0", 120, 20480), ("pq2_0", 64, 5120)])
 def test_split_k(kq, consumer, wl, fmt, n, k):
     sw, sx = synth.stream_id("test", 0, 320), synth.stream_id("test", 1, 320)
