@@ -8,7 +8,9 @@
 // Here each warp owns one row and loads it straight into registers, 16 bytes
 // per lane at a time, all of the row's loads in flight at once; the CTA
 // stages the activation in shared memory meanwhile.  No K split: one launch
-// per call, and each output is one warp's sum in a fixed order.
+// per call, and each output is one warp's sum in a fixed order.  The CTA is
+// small enough to start beside the kernel ahead of it, and it has L2 fetch
+// its rows while it waits for that kernel.
 //
 //   y[r] = sum_b d[r][b] * sum_{j in b} q[r][j] * x[j]
 //
@@ -49,14 +51,20 @@ __global__ void __launch_bounds__(kThreads) q8_0_gemv_kernel(const int8_t* __res
   // The activation, k floats, as float4 q of granule g at [q * (k / 16) + g]:
   // the lanes of a warp, on consecutive granules, read consecutive entries.
   extern __shared__ float4 xs4[];
-  // launched as a programmatic dependent: nothing is read before the
-  // kernel ahead has completed
-  grid_dependency_wait();
-  allow_dependent_launch();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kWarps + warp;
   const int ngran = k / 16;
   const bool live = row < n;
+  // Launched as a programmatic dependent, the CTA may start while the kernel
+  // ahead still runs: it asks L2 for its row's codes (a prefetch, which
+  // returns no data: L2 is where that kernel's writes land, so the loads
+  // after the wait still see them), then reads nothing before that kernel
+  // has completed.
+  if (live && lane == 0)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(codes + row * (int64_t)k), "r"((uint32_t)k)
+                 : "memory");
+  grid_dependency_wait();
+  allow_dependent_launch();
 
   // the row's codes and scales, all in flight before the activation staging
   uint4 cw[kMaxGranules];
