@@ -33,7 +33,8 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxGranules = 8;              // per lane: k up to 32 x 8 x 16 = 4096
 constexpr int64_t kMaxK = 32 * kMaxGranules * 16;
 
-// the four codes of word u (biased by 128 each) as exact floats
+// the four int8 codes of word w as exact floats: each, biased by 128, is the low
+// byte of the mantissa of 2^23, and the subtract takes 2^23 + 128 off again
 __device__ __forceinline__ void codes4(uint32_t w, float (&f)[4]) {
   const uint32_t u = w ^ 0x80808080u;  // q + 128 in each byte
 #pragma unroll
