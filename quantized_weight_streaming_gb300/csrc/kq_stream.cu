@@ -1650,25 +1650,29 @@ static int create_plan(const kq_qmat* mats, const kq_link* links, int64_t count,
   } else {
     // Contiguous item ranges, one per CTA, by bytes.  On a full grid the
     // shares are skewed: CTA c's capacity is proportional to
-    // w_c = 1 + kDealSkew * (1/2 - c / (G - 1)).  Measured on GB300 (per-CTA
+    // w_c = 1 + skew * (1/2 - c / (G - 1)).  Measured on GB300 (per-CTA
     // finish stamps of one launch): with equal shares the finish time grows
     // about linearly with the CTA index, ~5% from the first CTAs to the last,
     // reproducibly, with the work of every CTA alike and whatever the order
-    // in which the weights were allocated; the skew of 0.06 took the
-    // Bonsai-shaped step from 4992 to 5076 GB/s and the Qwen-shaped one from
-    // 6611 to 6685 (0.04: 5062 / 6623; 0.08: 5047 / 6679).
+    // in which the weights were allocated.  The skew that compensates it
+    // depends on the consumer; swept on the full steps with the cut points
+    // below (GB/s):
+    //  - PQ2_0, Bonsai-shaped: 0.03 5094, 0.045 5110, 0.06 5137, 0.075 5128,
+    //    0.09 5092;
+    //  - Q8_0, Qwen-shaped: 0.06 6702, 0.09 6763, 0.12 6759, 0.15 6660;
+    //  - SCALE4, Qwen-shaped: 0.06 5975, 0.09 6047, 0.12 6099, 0.15 6115.
     // The cut points minimise the largest load relative to its capacity,
     // max_c bytes_c / w_c: the least T for which filling each CTA in turn
     // with whole items up to T w_c places every item (taking each range as
     // long as it fits is optimal for a given T), found by bisection.  An
-    // item holds a whole row block (up to 1.2 MB at K = 17408), so cutting
-    // at the cumulative targets instead could leave a CTA an item above its
-    // share.
-    constexpr double kDealSkew = 0.06;
+    // item holds a whole row block (up to 1.3 MB), so cutting at the
+    // cumulative targets instead could leave a CTA an item above its share.
+    const int pf = plane_format(fmt);
+    const double deal_skew = pf == KQ_PQ2_0 ? 0.06 : (pf == KQ_Q8_0 ? 0.09 : 0.15);
     p->total_items = items;
     p->grid = (int)std::min<int64_t>(items, sms);
     const int G = p->grid;
-    const double skew = G >= 128 ? kDealSkew : 0.0;
+    const double skew = G >= 128 ? deal_skew : 0.0;
     std::vector<double> wgt((size_t)G);
     double wsum = 0, total = 0, biggest = 0;
     for (int c = 0; c < G; ++c) wsum += wgt[(size_t)c] = 1.0 + skew * (0.5 - (G > 1 ? (double)c / (G - 1) : 0.0));
