@@ -322,7 +322,8 @@ def _gemv_graph_measure(kq, wl_mod, fmt, n, k, m, stream, replays=20):
         path, launches = "tcgen05", 2 + (1 if split else 0)
     else:
         path, launches = "stream", ((m + 3) // 4) * (1 + (1 if nb else 0))
-        if fmt == "q8_0" and m == 1 and k <= 4096 and n * k <= 20 << 20:  # the library's one-launch GEMV
+        if m == 1 and ((fmt == "q8_0" and k <= 4096 and n * k <= 20 << 20) or
+                       (fmt == "pq2_0" and k <= 5376 and n * k // 4 <= 16 << 20)):  # the library's one-launch GEMVs
             path = "direct"
     out = {"fmt": fmt, "n": n, "k": k, "m": m, "path": path, "us_per_call": per_launch * 1e6,
            "gbs": nbytes / per_launch / 1e9, "copies": copies, "launches_per_call": launches}

@@ -238,7 +238,9 @@ int kq_gemv_scale4(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, s
 /* y[n] = W' (R x) for a PQ2_0 matrix: d_x is the UNROTATED fp32 activation
  * [k]; the blockwise transform runs in the kernel's activation prologue (the
  * activation side of every folded matmul: "Bonsai 2 27B", section 4.2; the
- * ternary matvec of section 8.5). */
+ * ternary matvec of section 8.5).  With the 128-block rotation and no signs,
+ * a small matrix (k <= 5376 and at most 16 MB of codes) runs in one launch
+ * with no K split and needs no workspace, on the default consumer. */
 int kq_gemv_pq2_0(const kq_qmat* W, const float* d_x, float* d_y, void* d_ws, size_t ws_bytes, void* stream);
 
 /* The fp16 chain of the Bonsai page, section 4.4 (its token-identity
